@@ -1,0 +1,131 @@
+"""fp64 CPU oracle for the frame-wise Gated DeltaNet forward pass.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline may use this package; the product library never does.  The arithmetic
+lives in ``gdn_oracle.c`` (plain C, fp64); this module only marshals numpy
+arrays into it.  Every function states the passage it follows, on the summary
+page "SANA-WM: Efficient Minute-Scale World Modeling with Hybrid Linear
+Diffusion Transformer":
+
+* section 方法步骤详情 (method details), module 2: the recurrence
+  S_t = S_{t-1}(gamma_t I - K^ beta K^T) + V beta K^T and the output O_t = S_t Q^_t;
+* section 前置知识 "Gated DeltaNet": S_t = S_{t-1} M_t + U_t;
+* section 技术新颖性 (novelty): ||M_t||_2 <= gamma_t <= 1 and the exact
+  composite prefix scan (C_p, H_p) used for context parallelism.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c into liboracle.so (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        Dbl = ctypes.c_double
+        lib.oracle_gdn_frame_fwd.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
+        lib.oracle_gdn_frame_fwd_tokacc.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
+        lib.oracle_gdn_frame_transitions.argtypes = [P] * 4 + [I] * 5 + [Dbl, P, P]
+        lib.oracle_gdn_composite.argtypes = [P, P, I, I, P, P]
+        lib.oracle_gdn_compose.argtypes = [P, P, P, P, I, P, P]
+        lib.oracle_num_threads.restype = I
+        _lib = lib
+    return _lib
+
+
+def _f32(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor -> exact fp32 copy on the host
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _shapes(q):
+    B, FN, H, D = q.shape
+    return B, FN, H, D
+
+
+def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulation="recurrence"):
+    """Frame-wise GDN forward in fp64.
+
+    Shapes: q, k, v [B, F*N, H, D]; beta [B, F*N, H]; gamma [B, F, H];
+    S_in [B, H, D, D] or None.  Returns (o [B, F*N, H, D] fp64, S_out [B, H, D, D] fp64).
+    ``formulation`` picks the printed recurrence ("recurrence", module 2 of the
+    method-details section) or the token-accumulation rewrite ("tokacc").
+    """
+    q, k, v, beta, gamma, S_in = (_f32(x) for x in (q, k, v, beta, gamma, S_in))
+    B, FN, H, D = _shapes(q)
+    F = gamma.shape[1]
+    N = FN // F if N is None else N
+    assert F * N == FN and k.shape == q.shape and v.shape == q.shape
+    assert beta.shape == (B, FN, H) and gamma.shape == (B, F, H)
+    if S_in is not None:
+        assert S_in.shape == (B, H, D, D)
+    o = np.zeros((B, FN, H, D), np.float64)
+    S_out = np.zeros((B, H, D, D), np.float64)
+    fn = {"recurrence": _load().oracle_gdn_frame_fwd,
+          "tokacc": _load().oracle_gdn_frame_fwd_tokacc}[formulation]
+    fn(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(S_in),
+       B, H, F, N, D, float(key_scale), _ptr(o), _ptr(S_out))
+    return o, S_out
+
+
+def frame_transitions(k, v, beta, gamma, key_scale=0.0):
+    """Per-frame (M_f, U_f), each [B, H, F, D, D] fp64 (module 2: M_t = gamma_t I - K^ beta K^T)."""
+    k, v, beta, gamma = (_f32(x) for x in (k, v, beta, gamma))
+    B, FN, H, D = _shapes(k)
+    F = gamma.shape[1]
+    N = FN // F
+    M = np.zeros((B, H, F, D, D), np.float64)
+    U = np.zeros((B, H, F, D, D), np.float64)
+    _load().oracle_gdn_frame_transitions(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),
+                                         B, H, F, N, D, float(key_scale), _ptr(M), _ptr(U))
+    return M, U
+
+
+def composite(M, U):
+    """(C, H) of a run of frames: C = prod M_f, H = state reached from zero (novelty section, C_p / H_p)."""
+    M = np.ascontiguousarray(M, dtype=np.float64)
+    U = np.ascontiguousarray(U, dtype=np.float64)
+    nF, D, _ = M.shape
+    C = np.zeros((D, D)); Hc = np.zeros((D, D))
+    _load().oracle_gdn_composite(_ptr(M), _ptr(U), nF, D, _ptr(C), _ptr(Hc))
+    return C, Hc
+
+
+def compose(C1, H1, C2, H2):
+    """(C1, H1) followed by (C2, H2) -> (C1 C2, H1 C2 + H2)."""
+    arrs = [np.ascontiguousarray(x, dtype=np.float64) for x in (C1, H1, C2, H2)]
+    D = arrs[0].shape[0]
+    C = np.zeros((D, D)); Hc = np.zeros((D, D))
+    _load().oracle_gdn_compose(*(_ptr(a) for a in arrs), D, _ptr(C), _ptr(Hc))
+    return C, Hc
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())

@@ -1,0 +1,281 @@
+/*
+ * Frame-wise Gated DeltaNet — plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load, call or link
+ * this file: it exists so that tests, the smoke check and the benchmark's CPU
+ * baseline can compare the CUDA library against an obviously-correct restatement
+ * of the method.  It shares no code, header, constant or helper with the CUDA
+ * sources.
+ *
+ * Source of the method: the paper-summary page "SANA-WM: Efficient Minute-Scale
+ * World Modeling with Hybrid Linear Diffusion Transformer", section 方法步骤详情
+ * (method details), module 2 "Memory-Efficient Long-Context": the GDN scans the
+ * video one latent frame at a time; the state S_t (D x D) follows
+ *     S_t = S_{t-1} (gamma_t I - K^_t beta_t K^_t^T) + V_t beta_t K^_t^T,
+ * the frame's output is O_t = S_t Q^_t, and the keys carry a 1/sqrt(D S) scale.
+ * Same page, section 前置知识 "Gated DeltaNet": the update written as
+ * S_t = S_{t-1} M_t + U_t with decay gate gamma_t.  Same page, section
+ * 技术新颖性 (novelty): the key scale makes ||M_t||_2 <= gamma_t <= 1, and context
+ * parallelism composes a transition composite C_p and an input composite H_p
+ * by a prefix scan that reproduces the single-device result exactly.
+ *
+ * Readings taken where the page is silent or garbled (each is listed in the
+ * design notes):
+ *   - k^_n = k_n / ||k_n||_2 * c_k with c_k = key_scale, default 1/sqrt(D*N)
+ *     ("DS" read as head dim times tokens per frame);
+ *   - q^_n = q_n / ||q_n||_2, no further factor;
+ *   - ||x||_2 = sqrt(sum x^2 + 1e-12);
+ *   - the frame output reads the post-update state S_f;
+ *   - M_f is the sum form gamma_f I - sum_n beta_n k^_n k^_n^T exactly as
+ *     printed (not the token-ordered product);
+ *   - gamma is per (batch, frame, head), beta per (batch, token, head).
+ *
+ * Layouts (row-major):
+ *   q, k, v : [B][F*N][H][D]  (fp32 values; bf16 inputs are passed exactly)
+ *   beta    : [B][F*N][H]
+ *   gamma   : [B][F][H]
+ *   S_in    : [B][H][D][D] or NULL for zeros; S[i][j] with i the value index
+ *             (row) and j the key index (column)
+ *   o       : [B][F*N][H][D]  (fp64)
+ *   S_out   : [B][H][D][D]    (fp64)
+ *
+ * Parallel execution: the B*H chains are independent problems, run one per
+ * OpenMP thread; inside a chain everything is the plain sequential loop.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_NORM_EPS 1e-12
+
+static double oracle_key_scale(double key_scale, int D, int N)
+{
+    return key_scale > 0.0 ? key_scale : 1.0 / sqrt((double)D * (double)N);
+}
+
+/* Index helpers for the [B][F*N][H][D] token layout. */
+static size_t tok_index(int b, int f, int n, int h, int d, int F, int N, int H, int D)
+{
+    return ((((size_t)b * F * N + (size_t)f * N + n) * H + h) * D) + d;
+}
+static size_t beta_index(int b, int f, int n, int h, int F, int N, int H)
+{
+    return ((size_t)b * F * N + (size_t)f * N + n) * H + h;
+}
+
+/* x^ = x / ||x||_2 * scale for one token-head vector. */
+static void normalise(const float *x, int D, double scale, double *out)
+{
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) ss += (double)x[d] * (double)x[d];
+    double inv = scale / sqrt(ss + ORACLE_NORM_EPS);
+    for (int d = 0; d < D; ++d) out[d] = (double)x[d] * inv;
+}
+
+/*
+ * Per-frame transition of one chain: A_f = sum_n beta_n k^_n k^_n^T and
+ * U_f = sum_n beta_n v_n k^_n^T, then M_f = gamma_f I - A_f.
+ * (summary page, 方法步骤详情 module 2: M_t = gamma_t I - K^_t beta_t K^_t^T,
+ *  U_t = V_t beta_t K^_t^T.)  M and U are D x D, row-major.
+ */
+static void frame_transition(const float *k, const float *v, const float *beta,
+                             const float *gamma, int b, int h, int f,
+                             int H, int F, int N, int D, double c,
+                             double *M, double *U, double *khat)
+{
+    memset(M, 0, sizeof(double) * D * D);
+    memset(U, 0, sizeof(double) * D * D);
+    for (int n = 0; n < N; ++n) {
+        normalise(k + tok_index(b, f, n, h, 0, F, N, H, D), D, c, khat);
+        const float *vn = v + tok_index(b, f, n, h, 0, F, N, H, D);
+        double bn = beta[beta_index(b, f, n, h, F, N, H)];
+        for (int i = 0; i < D; ++i)
+            for (int j = 0; j < D; ++j) {
+                M[i * D + j] -= bn * khat[i] * khat[j];      /* -A_f */
+                U[i * D + j] += bn * (double)vn[i] * khat[j];
+            }
+    }
+    double g = gamma[((size_t)b * F + f) * H + h];
+    for (int i = 0; i < D; ++i) M[i * D + i] += g;
+}
+
+/* C = A * B for D x D row-major matrices. */
+static void matmul(const double *A, const double *B, double *C, int D)
+{
+    for (int i = 0; i < D; ++i)
+        for (int j = 0; j < D; ++j) {
+            double s = 0.0;
+            for (int l = 0; l < D; ++l) s += A[i * D + l] * B[l * D + j];
+            C[i * D + j] = s;
+        }
+}
+
+/* o_{f,n} = S_f q^_n for every token of frame f (module 2: O_t = S_t Q^_t). */
+static void frame_output(const float *q, const double *S, int b, int h, int f,
+                         int H, int F, int N, int D, double *o, double *qhat)
+{
+    for (int n = 0; n < N; ++n) {
+        size_t base = tok_index(b, f, n, h, 0, F, N, H, D);
+        normalise(q + base, D, 1.0, qhat);
+        for (int i = 0; i < D; ++i) {
+            double s = 0.0;
+            for (int j = 0; j < D; ++j) s += S[i * D + j] * qhat[j];
+            o[base + i] = s;
+        }
+    }
+}
+
+static void load_state(const float *S_in, int b, int h, int H, int D, double *S)
+{
+    size_t base = ((size_t)b * H + h) * D * D;
+    for (int e = 0; e < D * D; ++e) S[e] = S_in ? (double)S_in[base + e] : 0.0;
+}
+
+static void store_state(double *S_out, const double *S, int b, int h, int H, int D)
+{
+    if (!S_out) return;
+    memcpy(S_out + ((size_t)b * H + h) * D * D, S, sizeof(double) * D * D);
+}
+
+/*
+ * Formulation 1 (the printed recurrence): for each frame build M_f and U_f
+ * explicitly, S_f = S_{f-1} M_f + U_f, then o = S_f q^.
+ */
+void oracle_gdn_frame_fwd(const float *q, const float *k, const float *v,
+                          const float *beta, const float *gamma, const float *S_in,
+                          int B, int H, int F, int N, int D, double key_scale,
+                          double *o, double *S_out)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        double *S = malloc(sizeof(double) * D * D);
+        double *Sn = malloc(sizeof(double) * D * D);
+        double *M = malloc(sizeof(double) * D * D);
+        double *U = malloc(sizeof(double) * D * D);
+        double *vec = malloc(sizeof(double) * D);
+        load_state(S_in, b, h, H, D, S);
+        for (int f = 0; f < F; ++f) {
+            frame_transition(k, v, beta, gamma, b, h, f, H, F, N, D, c, M, U, vec);
+            matmul(S, M, Sn, D);
+            for (int e = 0; e < D * D; ++e) S[e] = Sn[e] + U[e];
+            if (o) frame_output(q, S, b, h, f, H, F, N, D, o, vec);
+        }
+        store_state(S_out, S, b, h, H, D);
+        free(S); free(Sn); free(M); free(U); free(vec);
+    }
+}
+
+/*
+ * Formulation 2 (token accumulation, an independent loop structure used to
+ * check formulation 1): because M_f is a sum over the frame's tokens,
+ *   S_f = gamma_f S_{f-1} + sum_n beta_n (v_n - S_{f-1} k^_n) k^_n^T,
+ * i.e. every token of the frame writes a delta-rule correction against the
+ * frame-start state.
+ */
+void oracle_gdn_frame_fwd_tokacc(const float *q, const float *k, const float *v,
+                                 const float *beta, const float *gamma,
+                                 const float *S_in, int B, int H, int F, int N,
+                                 int D, double key_scale, double *o, double *S_out)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        double *S = malloc(sizeof(double) * D * D);
+        double *P = malloc(sizeof(double) * D * D);
+        double *kh = malloc(sizeof(double) * D);
+        double *err = malloc(sizeof(double) * D);
+        load_state(S_in, b, h, H, D, S);
+        for (int f = 0; f < F; ++f) {
+            memcpy(P, S, sizeof(double) * D * D);           /* frame-start state */
+            double g = gamma[((size_t)b * F + f) * H + h];
+            for (int e = 0; e < D * D; ++e) S[e] = g * P[e];
+            for (int n = 0; n < N; ++n) {
+                normalise(k + tok_index(b, f, n, h, 0, F, N, H, D), D, c, kh);
+                const float *vn = v + tok_index(b, f, n, h, 0, F, N, H, D);
+                double bn = beta[beta_index(b, f, n, h, F, N, H)];
+                for (int i = 0; i < D; ++i) {               /* v_n - S_{f-1} k^_n */
+                    double s = 0.0;
+                    for (int j = 0; j < D; ++j) s += P[i * D + j] * kh[j];
+                    err[i] = (double)vn[i] - s;
+                }
+                for (int i = 0; i < D; ++i)
+                    for (int j = 0; j < D; ++j) S[i * D + j] += bn * err[i] * kh[j];
+            }
+            if (o) frame_output(q, S, b, h, f, H, F, N, D, o, kh);
+        }
+        store_state(S_out, S, b, h, H, D);
+        free(S); free(P); free(kh); free(err);
+    }
+}
+
+/*
+ * The per-frame pair (M_f, U_f) for every (b, f, h), written to
+ * M_out, U_out : [B][H][F][D][D].  Used by the tests to check the printed norm
+ * bound ||M_t||_2 <= gamma_t and to build composites.
+ */
+void oracle_gdn_frame_transitions(const float *k, const float *v, const float *beta,
+                                  const float *gamma, int B, int H, int F, int N,
+                                  int D, double key_scale, double *M_out, double *U_out)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bhf = 0; bhf < B * H * F; ++bhf) {
+        int b = bhf / (H * F), h = (bhf / F) % H, f = bhf % F;
+        double *vec = malloc(sizeof(double) * D);
+        size_t off = (size_t)bhf * D * D;
+        frame_transition(k, v, beta, gamma, b, h, f, H, F, N, D, c,
+                         M_out + off, U_out + off, vec);
+        free(vec);
+    }
+}
+
+/*
+ * Composite of a run of frames (technical-novelty section: transition composite
+ * C_p and input composite H_p).  For frames f0..f1-1 of one chain,
+ *   C = M_{f0} M_{f0+1} ... M_{f1-1},   H = state reached from S = 0,
+ * so that S_{f1-1} = S_{f0-1} C + H.  M, U are [nF][D][D] for the run.
+ */
+void oracle_gdn_composite(const double *M, const double *U, int nF, int D,
+                          double *C, double *Hc)
+{
+    double *T = malloc(sizeof(double) * D * D);
+    for (int e = 0; e < D * D; ++e) { C[e] = 0.0; Hc[e] = 0.0; }
+    for (int i = 0; i < D; ++i) C[i * D + i] = 1.0;
+    for (int f = 0; f < nF; ++f) {
+        const double *Mf = M + (size_t)f * D * D, *Uf = U + (size_t)f * D * D;
+        matmul(C, Mf, T, D);
+        memcpy(C, T, sizeof(double) * D * D);
+        matmul(Hc, Mf, T, D);
+        for (int e = 0; e < D * D; ++e) Hc[e] = T[e] + Uf[e];
+    }
+    free(T);
+}
+
+/*
+ * Composition of two adjacent composites (earlier run 1, later run 2):
+ *   (C1, H1) then (C2, H2)  ->  (C1 C2, H1 C2 + H2).
+ */
+void oracle_gdn_compose(const double *C1, const double *H1, const double *C2,
+                        const double *H2, int D, double *C, double *Hc)
+{
+    double *T = malloc(sizeof(double) * D * D);
+    matmul(C1, C2, C, D);
+    matmul(H1, C2, T, D);
+    for (int e = 0; e < D * D; ++e) Hc[e] = T[e] + H2[e];
+    free(T);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
