@@ -1,0 +1,244 @@
+// gdn_api.cu — the C ABI (include/gdn.h): argument validation, workspace
+// sizing, the per-device status word, and dispatch to the kernels.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+// One status word per device.  Kernels OR status bits into it; the host reads
+// and clears it in gdn_device_status().
+__device__ unsigned g_status_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+float default_key_scale(float key_scale, int D, int N)
+{
+    if (key_scale > 0.f) return key_scale;
+    return N > 0 ? (float)(1.0 / sqrt((double)D * (double)N)) : 0.f;
+}
+}  // namespace
+
+unsigned *device_status_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char *gdn_status_string(gdn_status_t s)
+{
+    switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDN_ERR_CUDA: return "CUDA runtime error";
+    case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+    case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
+    if (D != 112) return (size_t)-1;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 0, &plan)) return (size_t)-1;
+    return plan.ws_bytes;
+}
+
+static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, const float *beta,
+                                   const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int F,
+                                   int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
+                                   gdn_stream_t stream, void **events)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (F == 0 || N == 0) {
+        if (F > 0 && (!gamma || !aligned(gamma, 4))) return GDN_ERR_INVALID_ARG;
+        if (!S_out) return GDN_OK;
+        return launch_decay_only(gamma, S_in, S_out, B, H, F, D, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (!q || !k || !v || !o || !beta || !gamma) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4) ||
+        !aligned(gamma, 4))
+        return GDN_ERR_INVALID_ARG;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 0, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_frame_fwd_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, default_key_scale(key_scale, D, N),
+                                        workspace, status, st, reinterpret_cast<cudaEvent_t *>(events));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                           const float *S_in, float *S_out, void *o, int B, int H, int F, int N, int D,
+                           float key_scale, void *workspace, size_t workspace_bytes, gdn_stream_t stream)
+{
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+                          workspace_bytes, stream, nullptr);
+}
+
+gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v, const float *beta,
+                                    const float *gamma, const float *S_in, float *S_out, void *o, int B, int H,
+                                    int F, int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
+                                    gdn_stream_t stream, void **events)
+{
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+                          workspace_bytes, stream, events);
+}
+
+// Device staging of the host-buffer form: q, k, v, o (bf16), beta, gamma,
+// S_in, S_out (fp32), then the workspace, each 256-byte aligned.
+struct HostLayout {
+    size_t tok, beta, gamma, state, ws;
+    size_t off_q, off_k, off_v, off_o, off_beta, off_gamma, off_sin, off_sout, off_ws, total;
+};
+
+static bool host_layout(int B, int H, int F, int N, int D, HostLayout *L)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return false;
+    const size_t ws = gdn_frame_fwd_workspace_size(B, H, F, N, D);
+    if (ws == (size_t)-1) return false;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    L->tok = (size_t)B * F * N * H * D * 2;
+    L->beta = (size_t)B * F * N * H * 4;
+    L->gamma = (size_t)B * F * H * 4;
+    L->state = (size_t)B * H * D * D * 4;
+    L->ws = ws;
+    size_t o = 0;
+    L->off_q = o; o = up(o + L->tok);
+    L->off_k = o; o = up(o + L->tok);
+    L->off_v = o; o = up(o + L->tok);
+    L->off_o = o; o = up(o + L->tok);
+    L->off_beta = o; o = up(o + L->beta);
+    L->off_gamma = o; o = up(o + L->gamma);
+    L->off_sin = o; o = up(o + L->state);
+    L->off_sout = o; o = up(o + L->state);
+    L->off_ws = o; o = up(o + L->ws);
+    L->total = o;
+    return true;
+}
+
+size_t gdn_frame_fwd_host_buffer_size(int B, int H, int F, int N, int D)
+{
+    HostLayout L;
+    return host_layout(B, H, F, N, D, &L) ? L.total : (size_t)-1;
+}
+
+gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o, int B, int H, int F, int N, int D,
+                                float key_scale, void *device_buffer, size_t device_buffer_bytes,
+                                gdn_stream_t stream)
+{
+    HostLayout L;
+    if (!host_layout(B, H, F, N, D, &L)) return D > 0 && D != 112 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (!device_buffer || device_buffer_bytes < L.total) return GDN_ERR_WORKSPACE;
+    if (!aligned(device_buffer, 256)) return GDN_ERR_INVALID_ARG;
+    const bool has_tokens = F > 0 && N > 0;
+    if (has_tokens && (!q || !k || !v || !o || !beta)) return GDN_ERR_INVALID_ARG;
+    if (F > 0 && !gamma) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *d = static_cast<uint8_t *>(device_buffer);
+    auto h2d = [&](size_t off, const void *src, size_t n) {
+        return n == 0 || cudaMemcpyAsync(d + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    auto d2h = [&](void *dst, size_t off, size_t n) {
+        return n == 0 || cudaMemcpyAsync(dst, d + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    };
+    if (has_tokens && (!h2d(L.off_q, q, L.tok) || !h2d(L.off_k, k, L.tok) || !h2d(L.off_v, v, L.tok) ||
+                       !h2d(L.off_beta, beta, L.beta)))
+        return GDN_ERR_CUDA;
+    if (F > 0 && !h2d(L.off_gamma, gamma, L.gamma)) return GDN_ERR_CUDA;
+    if (S_in && !h2d(L.off_sin, S_in, L.state)) return GDN_ERR_CUDA;
+    gdn_status_t s = frame_fwd_impl(d + L.off_q, d + L.off_k, d + L.off_v, reinterpret_cast<float *>(d + L.off_beta),
+                                    reinterpret_cast<float *>(d + L.off_gamma),
+                                    S_in ? reinterpret_cast<float *>(d + L.off_sin) : nullptr,
+                                    reinterpret_cast<float *>(d + L.off_sout), d + L.off_o, B, H, F, N, D, key_scale,
+                                    L.ws ? d + L.off_ws : nullptr, L.ws, stream, nullptr);
+    if (s != GDN_OK) return s;
+    if (has_tokens && o && !d2h(o, L.off_o, L.tok)) return GDN_ERR_CUDA;
+    if (S_out && !d2h(S_out, L.off_sout, L.state)) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+size_t gdn_frame_step_workspace_size(int B, int H, int N, int D) { return gdn_frame_fwd_workspace_size(B, H, 1, N, D); }
+
+gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                            const float *S_in, float *S_out, void *o, int B, int H, int N, int D, float key_scale,
+                            void *workspace, size_t workspace_bytes, gdn_stream_t stream)
+{
+    return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, workspace, workspace_bytes,
+                         stream);
+}
+
+gdn_status_t gdn_frame_fwd_f32(const float *q, const float *k, const float *v, const float *beta,
+                               const float *gamma, const float *S_in, float *S_out, float *o, int B, int H, int F,
+                               int N, int D, float key_scale, gdn_stream_t stream)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D > 128) return GDN_ERR_UNSUPPORTED;
+    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (F == 0 || N == 0) {
+        if (F > 0 && (!gamma || !aligned(gamma, 4))) return GDN_ERR_INVALID_ARG;
+        if (!S_out) return GDN_OK;
+        return launch_decay_only(gamma, S_in, S_out, B, H, F, D, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (!q || !k || !v || !o || !beta || !gamma) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(o, 4) || !aligned(beta, 4) ||
+        !aligned(gamma, 4))
+        return GDN_ERR_INVALID_ARG;
+    cudaError_t e = launch_frame_fwd_f32(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D,
+                                         default_key_scale(key_scale, D, N), st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_device_status(gdn_stream_t stream)
+{
+    unsigned *p = device_status_word();
+    if (!p) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
+        return GDN_ERR_TIMEOUT;
+    }
+    return GDN_OK;
+}
+
+}  // extern "C"

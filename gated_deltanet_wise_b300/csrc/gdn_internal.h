@@ -1,0 +1,36 @@
+// gdn_internal.h — declarations shared by the library's translation units
+// (never installed, never seen by callers of include/gdn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// fp32 validation path (gdn_f32.cu)
+size_t f32_smem_bytes(int D);
+cudaError_t launch_frame_fwd_f32(const float *q, const float *k, const float *v, const float *beta,
+                                 const float *gamma, const float *S_in, float *S_out, float *o, int B, int H, int F,
+                                 int N, int D, float c, cudaStream_t stream);
+cudaError_t launch_decay_only(const float *gamma, const float *S_in, float *S_out, int B, int H, int F, int D,
+                              cudaStream_t stream);
+
+// Address of the current device's status word (device memory), or nullptr.
+unsigned *device_status_word();
+
+// tensor-core path (gdn_tc.cu); D == 112.
+struct TcPlan {
+    int B, H, F, N;
+    int chunk;       // frames per chunk (K1 / K2 work unit)
+    int n_chunks;    // chunks per chain
+    size_t ws_bytes; // total workspace
+    size_t off_frames, off_comp, off_start;  // workspace sections
+};
+bool tc_plan(int B, int H, int F, int N, int num_sms, TcPlan *plan);
+cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o, const TcPlan &plan, float c,
+                                void *workspace, unsigned *status, cudaStream_t stream,
+                                cudaEvent_t *events = nullptr);
+
+}  // namespace gdn

@@ -1,0 +1,933 @@
+// gdn_tc.cu — tensor-core (tcgen05 + TMA) path of the frame-wise GDN forward,
+// head size D = 112, bf16 q/k/v/o, fp32 beta/gamma/state.
+//
+// The method (summary page "SANA-WM: Efficient Minute-Scale World Modeling with
+// Hybrid Linear Diffusion Transformer", section 方法步骤详情, module 2):
+//   A_f = sum_n beta_n k^_n k^_n^T,  U_f = sum_n beta_n v_n k^_n^T,
+//   S_f = S_{f-1} (gamma_f I - A_f) + U_f,   o_{f,n} = S_f q^_n,
+// k^ = k / ||k|| * c, q^ = q / ||q||.  The frame axis is cut into chunks of L
+// frames; a chunk's transition composite C = prod M_f and input composite
+// H (state reached from zero) let every chunk find its start state with a short
+// prefix scan — the C_p / H_p composites of the same page's section 技术新颖性,
+// used here across SMs instead of across GPUs.
+//
+// Three launches:
+//   K1 (frame statistics), one CTA per (chunk, chain): streams K and V through
+//      shared memory in 64-token stages; CUDA cores turn each token into the
+//      MMA operands X = beta c^2/r^2 k, Y = beta c/r v (Y as bf16 hi + lo);
+//      tcgen05 accumulates A_f = X^T K and U_f = Y^T K in TMEM.  It writes
+//      A_f (bf16, as the MMA-ready image) and U_f (fp32) to the workspace and
+//      folds the chunk composite (C, H) with two more MMAs per frame.
+//   K1b (chunk boundaries), row-parallel fp32: S_start(c+1) = S_start(c) C_c + H_c.
+//   K2 (state scan + output), one CTA per (chunk, chain): walks the chunk's
+//      frames with S in fp32 registers, S_f = gamma S - (S_hi + S_lo) A_f + U_f
+//      on tcgen05, and computes O = Q (S_hi + S_lo)^T for 128-token tiles of Q
+//      (TMA in, TMA out), scaling each row by 1/||q|| in the epilogue.
+//
+// Precision: raw bf16 k, v, q are exact MMA operands; the per-token fp32
+// weights are folded into X and Y; U (the part of S that matters) uses a
+// hi/lo bf16 split of Y, and O uses a hi/lo split of S, so the only
+// unavoidable rounding is the bf16 output.  A_f itself is ~1/D in norm, so a
+// single bf16 rounding of A_f and of C/H in the composite products stays at
+// ~u/D relative.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "gdn_internal.h"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+
+// ------------------------------------------------------------------ sizes
+constexpr int kD = 112;               // head size this path is built for
+constexpr int kSms = 148;             // B300 SM count: the chunk plan targets it
+constexpr float kEps = 1e-12f;        // ||x|| = sqrt(sum x^2 + eps)
+
+constexpr uint32_t kRowB = 128;                      // one swizzled row: 64 bf16
+constexpr uint32_t kAimgPanel = kD * kRowB;          // 14336: A_f image, 112 rows
+constexpr uint32_t kAimgBytes = 2 * kAimgPanel;      // 28672
+constexpr uint32_t kUStride = 116;                   // floats per U_f row (padded: conflict-free smem rows)
+constexpr uint32_t kUimgBytes = kD * kUStride * 4;   // 51968
+constexpr uint32_t kFrameWs = kAimgBytes + kUimgBytes;  // 80640 bytes per (chain, frame)
+constexpr uint32_t kImgPanel = 128 * kRowB;          // 16384: 128-row bf16 image panel
+constexpr uint32_t kImgBytes = 2 * kImgPanel;        // 32768
+constexpr uint32_t kStateFloats = kD * kD;           // 12544
+constexpr size_t kStateBytes = kStateFloats * 4;     // 50176
+
+// K1
+constexpr int kTS = 64;                               // tokens per stage
+constexpr uint32_t kTSPanel = kTS * kRowB;            // 8192
+constexpr uint32_t kStageBytes = 8 * kTSPanel;        // K, V->Y_hi, Y_lo, X (2 panels each) = 65536
+constexpr uint32_t kOffK = 0, kOffY = 2 * kTSPanel, kOffYlo = 4 * kTSPanel, kOffX = 6 * kTSPanel;
+constexpr int kK1Stages = 2;
+constexpr int kK1Threads = 320;                       // producer, MMA, 8 math warps
+constexpr uint32_t kK1OffAimg = kK1Stages * kStageBytes;   // 131072
+constexpr uint32_t kK1OffCimg = kK1OffAimg + kAimgBytes;   // 159744
+constexpr uint32_t kK1OffHimg = kK1OffCimg + kImgBytes;    // 192512
+constexpr uint32_t kK1OffBar = kK1OffHimg + kImgBytes;     // 225280
+constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
+
+// K2
+constexpr int kTQ = 128;                              // tokens per Q/O tile
+constexpr int kK2QStages = 2;
+constexpr int kK2Threads = 320;                       // producer, MMA, 4 state warps, 4 output warps
+constexpr uint32_t kK2OffA = kK2QStages * kImgBytes;       // 65536
+constexpr uint32_t kK2OffU = kK2OffA + kAimgBytes;         // 94208
+constexpr uint32_t kK2OffShi = 146432;                     // 1024-aligned after U
+constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 179200
+constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 211968
+constexpr uint32_t kK2Smem = kK2OffBar + 256 + 1024;
+static_assert(kK2OffU + kUimgBytes <= kK2OffShi, "K2 smem layout");
+static_assert(kK1Smem <= 232448 && kK2Smem <= 232448, "shared memory budget");
+
+// instruction descriptors (M = 128, N = 112)
+constexpr uint32_t kIdescMN = idesc_bf16(128, kD, true, true);    // token-contraction GEMMs
+constexpr uint32_t kIdescK = idesc_bf16(128, kD, false, false);   // D-contraction GEMMs
+
+__device__ __forceinline__ void raise_status(unsigned *status)
+{
+    if (status) atomicOr(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float *f)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float *f)
+{
+    uint4 u;
+    u.x = pack_bf16x2(f[0], f[1]);
+    u.y = pack_bf16x2(f[2], f[3]);
+    u.z = pack_bf16x2(f[4], f[5]);
+    u.w = pack_bf16x2(f[6], f[7]);
+    return u;
+}
+
+// hi = bf16(x), lo = bf16(x - hi) for 8 values.
+__device__ __forceinline__ void split_bf16x8(const float *x, uint4 &hi, uint4 &lo)
+{
+    float r[8];
+    hi = f32x8_to_bf16(x);
+    bf16x8_to_f32(hi, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = x[i] - r[i];
+    lo = f32x8_to_bf16(r);
+}
+
+// ===================================================================== K1
+struct K1Params {
+    const float *beta;
+    const float *gamma;
+    uint8_t *ws_frames;  // [BH][F] x kFrameWs
+    float *ws_comp;      // [BH][n_chunks] x (C, H) fp32
+    unsigned *status;
+    int B, H, F, N, chunk, n_chunks;
+    float c;
+};
+
+__global__ void __launch_bounds__(kK1Threads, 1)
+    k1_frame_stats_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                          const K1Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK1OffBar);
+    uint64_t *st_full = bars + 0, *st_prep = bars + 2, *st_empty = bars + 4;
+    uint64_t *acc_full = bars + 6, *comp_full = bars + 8, *acc_free = bars + 10, *aimg_ready = bars + 12;
+    uint64_t *drain = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p.B * p.H;
+    const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int f_begin = chunk_idx * p.chunk;
+    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+    const int n_st = (p.N + kTS - 1) / kTS;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&st_full[i], 1);
+            mbar_init(&st_prep[i], 8);
+            mbar_init(&st_empty[i], 1);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&comp_full[i], 1);
+            mbar_init(&acc_free[i], 8);
+        }
+        mbar_init(aimg_ready, 8);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    // Math warps: composite images start as -I (C) and 0 (H); rows 112..127 stay 0.
+    if (warp >= 2) {
+        const int mt = threadIdx.x - 64;
+        uint4 z = make_uint4(0, 0, 0, 0);
+        for (int o = mt * 16; o < 2 * (int)kImgBytes; o += 256 * 16)
+            *reinterpret_cast<uint4 *>(sm + kK1OffCimg + o) = z;
+    }
+    __syncthreads();
+    if (warp >= 2) {
+        const int mt = threadIdx.x - 64;
+        if (mt < kD) {  // -1 on the diagonal of the C image
+            __nv_bfloat16 m1 = __float2bfloat16(-1.f);
+            const int col = mt, panel = col >> 6, chunk = (col & 63) >> 3;
+            *reinterpret_cast<__nv_bfloat16 *>(sm + kK1OffCimg + panel * kImgPanel + sw128_off(mt, chunk) +
+                                               2 * (col & 7)) = m1;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int it = 0, issued[2] = {0, 0};
+            bool ok = true;
+            for (int fl = 0; fl < nf && ok; ++fl) {
+                const int bf = b * p.F + f_begin + fl;
+                for (int st = 0; st < n_st; ++st, ++it) {
+                    const int s = it & 1;
+                    if (it >= 2 && !(ok = mbar_wait(&st_empty[s], ((it >> 1) - 1) & 1, abort_flag))) break;
+                    uint8_t *stg = sm + s * kStageBytes;
+                    mbar_arrive_expect_tx(&st_full[s], 4 * kTSPanel);
+                    tma_load_4d(stg + kOffK, &mapK, &st_full[s], 0, h, st * kTS, bf, pol);
+                    tma_load_4d(stg + kOffK + kTSPanel, &mapK, &st_full[s], 64, h, st * kTS, bf, pol);
+                    tma_load_4d(stg + kOffY, &mapV, &st_full[s], 0, h, st * kTS, bf, pol);
+                    tma_load_4d(stg + kOffY + kTSPanel, &mapV, &st_full[s], 64, h, st * kTS, bf, pol);
+                    ++issued[s];
+                }
+            }
+            if (*abort_flag)  // let loads already in flight land before the CTA exits
+                for (int s = 0; s < 2; ++s)
+                    if (issued[s]) mbar_wait_drain(&st_full[s], (issued[s] - 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int pending = -1;  // frame whose composite MMAs are not issued yet
+            auto issue_composite = [&](int fc) {
+                tc_fence_after();
+                const uint32_t acc_c = tmem + (fc & 1) * 256, acc_h = acc_c + 128;
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                    const uint64_t bdesc =
+                        sdesc_sw128(sbase + kK1OffAimg + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
+                    mma_bf16(acc_c, sdesc_sw128(sbase + kK1OffCimg + koff, 16, 1024), bdesc, kIdescK, ks > 0);
+                    mma_bf16(acc_h, sdesc_sw128(sbase + kK1OffHimg + koff, 16, 1024), bdesc, kIdescK, 1);
+                }
+                mma_commit(&comp_full[fc & 1]);
+            };
+            // Wait on `bar`, issuing the pending composite as soon as its A_f image is ready.
+            auto wait_serving = [&](uint64_t *bar, uint32_t par) -> bool {
+                const long long t0 = clock64();
+                while (true) {
+                    if (mbar_try_wait(bar, par)) return true;
+                    if (pending >= 0 && mbar_try_wait(aimg_ready, pending & 1)) {
+                        issue_composite(pending);
+                        pending = -1;
+                        continue;
+                    }
+                    if (*abort_flag) return false;
+                    if (clock64() - t0 > kSpinLimitCycles) {
+                        *abort_flag = 1;
+                        return false;
+                    }
+                }
+            };
+            int it = 0;
+            bool ok = true;
+            for (int fl = 0; fl < nf && ok; ++fl) {
+                const int buf = fl & 1;
+                const uint32_t acc_a = tmem + buf * 256, acc_u = acc_a + 128;
+                if (fl >= 2) ok = wait_serving(&acc_free[buf], ((fl >> 1) - 1) & 1);
+                for (int st = 0; st < n_st && ok; ++st, ++it) {
+                    const int s = it & 1;
+                    if (!(ok = wait_serving(&st_prep[s], (it >> 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t stg = sbase + s * kStageBytes;
+#pragma unroll
+                    for (int ks = 0; ks < kTS / 16; ++ks) {
+                        const uint32_t o = ks * 2048;
+                        const uint64_t bk = sdesc_sw128(stg + kOffK + o, kTSPanel, 1024);
+                        const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
+                        mma_bf16(acc_a, sdesc_sw128(stg + kOffX + o, kTSPanel, 1024), bk, kIdescMN, acc);
+                        mma_bf16(acc_u, sdesc_sw128(stg + kOffY + o, kTSPanel, 1024), bk, kIdescMN, acc);
+                        mma_bf16(acc_u, sdesc_sw128(stg + kOffYlo + o, kTSPanel, 1024), bk, kIdescMN, 1u);
+                    }
+                    mma_commit(&st_empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[buf]);
+                if (pending >= 0) {
+                    if (!(ok = mbar_wait(aimg_ready, pending & 1, abort_flag))) break;
+                    issue_composite(pending);
+                }
+                pending = fl;
+            }
+            if (ok && pending >= 0 && mbar_wait(aimg_ready, pending & 1, abort_flag)) issue_composite(pending);
+            mma_commit(drain);  // every MMA issued above has completed once this phase lands
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        // ------------------------------------------ math warps (prep + epilogue)
+        const int mt = threadIdx.x - 64;          // 0..255
+        const int quad = warp & 3;                 // TMEM lane quadrant
+        const int half = (warp - 2) >> 2;          // column half: 0 -> cols 0..63, 1 -> 64..111
+        const int row = quad * 32 + lane;          // TMEM lane = matrix row
+        const int ncc = half ? 3 : 4;              // 16-column chunks in this half
+        const int col0 = half * 64;
+        // prep mapping: token r, quarter qq (panel qq>>1, chunks (qq&1)*4..+3)
+        const int r = mt >> 2, qq = mt & 3;
+        const uint32_t prep_off = (qq >> 1) * kTSPanel + r * kRowB;
+        float Creg[64], Hreg[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            Creg[j] = (row == col0 + j) ? 1.f : 0.f;
+            Hreg[j] = 0.f;
+        }
+        const size_t FN = (size_t)p.F * p.N;
+        int it = 0;
+        bool ok = true;
+
+        auto prep_stage = [&](int fl, int st) {
+            const int s = it & 1;
+            if (!(ok = mbar_wait_warp(&st_full[s], (it >> 1) & 1, abort_flag))) return;
+            uint8_t *stg = sm + s * kStageBytes;
+            const int n = st * kTS + r;
+            const int f = f_begin + fl;
+            float bt = 0.f;
+            if (n < p.N) bt = p.beta[((size_t)b * FN + (size_t)f * p.N + n) * p.H + h];
+            float kf[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stg + kOffK + prep_off + pos), kf + 8 * i);
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ss = fmaf(kf[i], kf[i], ss);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            const float inv = p.c * rsqrtf(ss + kEps);
+            const float wx = bt * inv * inv, wy = bt * inv;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
+                float x[8], vf[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = wx * kf[8 * i + e];
+                *reinterpret_cast<uint4 *>(stg + kOffX + prep_off + pos) = f32x8_to_bf16(x);
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stg + kOffY + prep_off + pos), vf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vf[e] *= wy;
+                uint4 hi, lo;
+                split_bf16x8(vf, hi, lo);
+                *reinterpret_cast<uint4 *>(stg + kOffY + prep_off + pos) = hi;
+                *reinterpret_cast<uint4 *>(stg + kOffYlo + prep_off + pos) = lo;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st_prep[s]);
+            ++it;
+        };
+
+        // This warp's slice of the A_f image: rows 32*quad.. of panel `half`
+        // (contiguous in shared memory and in the workspace image).
+        const int img_rows = quad == 3 ? kD - 96 : 32;
+        const uint32_t img_off = half * kAimgPanel + quad * 32 * kRowB;
+
+        auto epilogue = [&](int fe) {
+            const int buf = fe & 1;
+            const int f = f_begin + fe;
+            const uint32_t acc_a = tmem + buf * 256 + col0, acc_u = acc_a + 128;
+            const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+            // this warp's previous A_f bulk store must have finished reading its slice
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (!(ok = mbar_wait_warp(&acc_full[buf], (fe >> 1) & 1, abort_flag))) return;
+            tc_fence_after();
+            uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
+            float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < ncc) {
+                    uint32_t ra[16], ru[16];
+                    tmem_ld16(acc_a + lane_off + cc * 16, ra);
+                    tmem_ld16(acc_u + lane_off + cc * 16, ru);
+                    tmem_ld_wait();
+                    if (row < kD) {
+                        float a[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) a[j] = __uint_as_float(ra[j]);
+                        uint8_t *dst = sm + kK1OffAimg + half * kAimgPanel;
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc)) = f32x8_to_bf16(a);
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(a + 8);
+                        float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col0 + cc * 16);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            u4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                                __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+                    }
+                }
+            }
+            if (half == 1 && row < kD) {  // key columns 112..127 of the image: zero
+                uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
+                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(aimg_ready);
+                bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
+                bulk_commit();
+            }
+            // composite: C <- gamma C + acc_C (= -C A_f), H <- gamma H + acc_H (= U_f - H A_f)
+            if (!(ok = mbar_wait_warp(&comp_full[buf], (fe >> 1) & 1, abort_flag))) return;
+            tc_fence_after();
+            const float g = p.gamma[((size_t)b * p.F + f) * p.H + h];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < ncc) {
+                    uint32_t rc[16], rh[16];
+                    tmem_ld16(acc_a + lane_off + cc * 16, rc);
+                    tmem_ld16(acc_u + lane_off + cc * 16, rh);
+                    tmem_ld_wait();
+                    float cn[16], hn[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        Creg[cc * 16 + j] = fmaf(g, Creg[cc * 16 + j], __uint_as_float(rc[j]));
+                        Hreg[cc * 16 + j] = fmaf(g, Hreg[cc * 16 + j], __uint_as_float(rh[j]));
+                        cn[j] = -Creg[cc * 16 + j];
+                        hn[j] = -Hreg[cc * 16 + j];
+                    }
+                    if (row < kD) {
+                        uint8_t *dc = sm + kK1OffCimg + half * kImgPanel;
+                        uint8_t *dh = sm + kK1OffHimg + half * kImgPanel;
+                        *reinterpret_cast<uint4 *>(dc + sw128_off(row, 2 * cc)) = f32x8_to_bf16(cn);
+                        *reinterpret_cast<uint4 *>(dc + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(cn + 8);
+                        *reinterpret_cast<uint4 *>(dh + sw128_off(row, 2 * cc)) = f32x8_to_bf16(hn);
+                        *reinterpret_cast<uint4 *>(dh + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(hn + 8);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free[buf]);
+        };
+
+        for (int fl = 0; fl < nf && ok; ++fl) {
+            for (int st = 0; st < n_st && ok; ++st) {
+                prep_stage(fl, st);
+                if (ok && fl >= 1 && st == min(1, n_st - 1)) epilogue(fl - 1);
+            }
+        }
+        if (ok) epilogue(nf - 1);
+        if (ok && row < kD) {
+            float *comp = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < ncc) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const int col = col0 + cc * 16 + j;
+                        *reinterpret_cast<float4 *>(comp + row * kD + col) =
+                            make_float4(Creg[cc * 16 + j], Creg[cc * 16 + j + 1], Creg[cc * 16 + j + 2],
+                                        Creg[cc * 16 + j + 3]);
+                        *reinterpret_cast<float4 *>(comp + kStateFloats + row * kD + col) =
+                            make_float4(Hreg[cc * 16 + j], Hreg[cc * 16 + j + 1], Hreg[cc * 16 + j + 2],
+                                        Hreg[cc * 16 + j + 3]);
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ===================================================================== K1b
+// S_start(c) for every chunk, row-parallel fp32: rows [8*y, 8*y+8) of chain x.
+constexpr int kK1bRows = 8;
+constexpr int kK1bThreads = 224;
+constexpr uint32_t kK1bSmem = (kD * kD + kK1bRows * kD) * 4;
+
+__global__ void __launch_bounds__(kK1bThreads)
+    k1b_chunk_boundary_kernel(const float *__restrict__ ws_comp, float *__restrict__ ws_start, const float *S_in,
+                              float *S_out, int n_chunks)
+{
+    extern __shared__ __align__(16) float k1b_smem[];
+    float *Cs = k1b_smem;                                                   // [kD][kD]
+    float(*Srows)[kD] = reinterpret_cast<float(*)[kD]>(k1b_smem + kD * kD);  // [kK1bRows][kD]
+    const int bh = blockIdx.x, r0 = blockIdx.y * kK1bRows;
+    const int t = threadIdx.x, j = t % kD, rp = t / kD;  // rows r0 + 4*rp + 0..3
+    for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
+        const int rr = e / kD, cc = e % kD;
+        Srows[rr][cc] = S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
+    }
+    __syncthreads();
+    for (int c = 0; c < n_chunks; ++c) {
+        float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
+        for (int e = t; e < kK1bRows * kD; e += kK1bThreads) dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
+        const float *C = ws_comp + ((size_t)bh * n_chunks + c) * 2 * kStateFloats;
+        const float *Hc = C + kStateFloats;
+        for (int e = t * 4; e < kStateFloats; e += kK1bThreads * 4)
+            *reinterpret_cast<float4 *>(&Cs[e]) = *reinterpret_cast<const float4 *>(C + e);
+        __syncthreads();
+        float acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = Hc[(r0 + 4 * rp + q) * kD + j];
+        for (int l = 0; l < kD; ++l) {
+            const float cl = Cs[l * kD + j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = fmaf(Srows[4 * rp + q][l], cl, acc[q]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Srows[4 * rp + q][j] = acc[q];
+        __syncthreads();
+    }
+    if (S_out)
+        for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
+            S_out[(size_t)bh * kStateFloats + (r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
+}
+
+// ===================================================================== K2
+struct K2Params {
+    const float *gamma;
+    const uint8_t *ws_frames;
+    const float *ws_start;
+    unsigned *status;
+    int B, H, F, N, chunk, n_chunks;
+};
+
+__global__ void __launch_bounds__(kK2Threads, 1)
+    k2_scan_output_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO,
+                          const K2Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK2OffBar);
+    uint64_t *q_full = bars + 0, *q_empty = bars + 2;
+    uint64_t *a_full = bars + 4, *a_empty = bars + 5, *u_full = bars + 6, *u_empty = bars + 7;
+    uint64_t *s_ready = bars + 8, *accS_full = bars + 9, *o_done = bars + 10;
+    uint64_t *o_full = bars + 11, *o_free = bars + 14, *drain = bars + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p.B * p.H;
+    const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int f_begin = chunk_idx * p.chunk;
+    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+    const int n_tiles = (p.N + kTQ - 1) / kTQ;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 4);
+        }
+        mbar_init(drain, 1);
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        mbar_init(u_full, 1);
+        mbar_init(u_empty, 4);
+        mbar_init(s_ready, 4);
+        mbar_init(accS_full, 1);
+        mbar_init(o_done, 1);
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    // zero the S images (rows 112..127 and key columns 112..127 stay zero)
+    for (int o = threadIdx.x * 16; o < 2 * (int)kImgBytes; o += kK2Threads * 16)
+        *reinterpret_cast<uint4 *>(sm + kK2OffShi + o) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+    const uint8_t *ws_chain = p.ws_frames + ((size_t)bh * p.F + f_begin) * kFrameWs;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int qc = 0, q_issued[2] = {0, 0}, a_issued = 0, u_issued = 0;
+            bool ok = true;
+            for (int it = 0; it <= nf && ok; ++it) {
+                if (it < nf) {
+                    if (it >= 1 && !(ok = mbar_wait(a_empty, (it - 1) & 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(a_full, kAimgBytes);
+                    bulk_g2s(sm + kK2OffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
+                    ++a_issued;
+                }
+                if (it >= 1) {
+                    const int bf = b * p.F + f_begin + it - 1;
+                    for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
+                        const int s = qc & 1;
+                        if (qc >= 2 && !(ok = mbar_wait(&q_empty[s], ((qc >> 1) - 1) & 1, abort_flag))) break;
+                        mbar_arrive_expect_tx(&q_full[s], kImgBytes);
+                        uint8_t *dst = sm + s * kImgBytes;
+                        tma_load_4d(dst, &mapQ, &q_full[s], 0, h, t * kTQ, bf, pol);
+                        tma_load_4d(dst + kImgPanel, &mapQ, &q_full[s], 64, h, t * kTQ, bf, pol);
+                        ++q_issued[s];
+                    }
+                }
+                if (ok && it < nf) {
+                    if (it >= 1 && !(ok = mbar_wait(u_empty, (it - 1) & 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(u_full, kUimgBytes);
+                    bulk_g2s(sm + kK2OffU, ws_chain + (size_t)it * kFrameWs + kAimgBytes, kUimgBytes, u_full);
+                    ++u_issued;
+                }
+            }
+            if (*abort_flag) {  // let copies already in flight land before the CTA exits
+                for (int s = 0; s < 2; ++s)
+                    if (q_issued[s]) mbar_wait_drain(&q_full[s], (q_issued[s] - 1) & 1);
+                if (a_issued) mbar_wait_drain(a_full, (a_issued - 1) & 1);
+                if (u_issued) mbar_wait_drain(u_full, (u_issued - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int qc = 0;
+            bool ok = true;
+            for (int it = 0; it <= nf && ok; ++it) {
+                if (!(ok = mbar_wait(s_ready, it & 1, abort_flag))) break;
+                tc_fence_after();
+                if (it < nf) {
+                    if (!(ok = mbar_wait(a_full, it & 1, abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 7; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                        const uint64_t bd =
+                            sdesc_sw128(sbase + kK2OffA + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
+                        mma_bf16(tmem, sdesc_sw128(sbase + kK2OffShi + koff, 16, 1024), bd, kIdescK, ks > 0);
+                        mma_bf16(tmem, sdesc_sw128(sbase + kK2OffSlo + koff, 16, 1024), bd, kIdescK, 1);
+                    }
+                    mma_commit(accS_full);
+                    mma_commit(a_empty);
+                }
+                if (it >= 1) {
+                    for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
+                        const int s = qc & 1, slot = qc % 3;
+                        if (!(ok = mbar_wait(&q_full[s], (qc >> 1) & 1, abort_flag))) break;
+                        if (qc >= 3 && !(ok = mbar_wait(&o_free[slot], ((qc / 3) - 1) & 1, abort_flag))) break;
+                        tc_fence_after();
+                        const uint32_t acc = tmem + 128 * (slot + 1);
+                        const uint32_t qb = sbase + s * kImgBytes;
+#pragma unroll
+                        for (int ks = 0; ks < 7; ++ks) {
+                            const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                            const uint64_t ad = sdesc_sw128(qb + koff, 16, 1024);
+                            mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffShi + koff, 16, 1024), kIdescK, ks > 0);
+                            mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffSlo + koff, 16, 1024), kIdescK, 1);
+                        }
+                        mma_commit(&o_full[slot]);
+                    }
+                    if (ok) mma_commit(o_done);
+                }
+            }
+            mma_commit(drain);  // every MMA issued above has completed once this phase lands
+            mbar_wait_drain(drain, 0);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------- state warps (rows)
+        const int quad = warp & 3, row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        float S[kD];
+        const float *s0 = p.ws_start + ((size_t)bh * p.n_chunks + chunk_idx) * kStateFloats;
+#pragma unroll
+        for (int j = 0; j < kD; j += 4) {
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < kD) v4 = *reinterpret_cast<const float4 *>(s0 + row * kD + j);
+            S[j] = v4.x;
+            S[j + 1] = v4.y;
+            S[j + 2] = v4.z;
+            S[j + 3] = v4.w;
+        }
+        auto write_images = [&]() {
+            if (row < kD) {
+#pragma unroll
+                for (int c8 = 0; c8 < kD / 8; ++c8) {
+                    uint4 hi, lo;
+                    split_bf16x8(S + 8 * c8, hi, lo);
+                    const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
+                    *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + kK2OffSlo + off) = lo;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_ready);
+        };
+        write_images();
+        for (int it = 0; it < nf; ++it) {
+            if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
+            if (!mbar_wait_warp(u_full, it & 1, abort_flag)) break;
+            tc_fence_after();
+            const float g = p.gamma[((size_t)b * p.F + f_begin + it) * p.H + h];
+            const float *U = reinterpret_cast<const float *>(sm + kK2OffU) + (row < kD ? row : 0) * kUStride;
+#pragma unroll
+            for (int cc = 0; cc < 7; ++cc) {
+                uint32_t ra[16];
+                tmem_ld16(tmem + lane_off + cc * 16, ra);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 u4 = *reinterpret_cast<const float4 *>(U + cc * 16 + j);
+                    S[cc * 16 + j] = fmaf(g, S[cc * 16 + j], u4.x - __uint_as_float(ra[j]));
+                    S[cc * 16 + j + 1] = fmaf(g, S[cc * 16 + j + 1], u4.y - __uint_as_float(ra[j + 1]));
+                    S[cc * 16 + j + 2] = fmaf(g, S[cc * 16 + j + 2], u4.z - __uint_as_float(ra[j + 2]));
+                    S[cc * 16 + j + 3] = fmaf(g, S[cc * 16 + j + 3], u4.w - __uint_as_float(ra[j + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(u_empty);
+            if (it >= 1 && !mbar_wait_warp(o_done, (it - 1) & 1, abort_flag)) break;
+            write_images();
+        }
+    } else {
+        // ------------------------------------------------ output warps (tokens)
+        // Each warp owns 32 token rows of a tile: it scales them, writes bf16 in
+        // place over its Q rows and stores its own 32-row boxes with TMA.
+        const int quad = warp & 3, r = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int qc = 0;
+        bool ok = true;
+        for (int it = 1; it <= nf && ok; ++it) {
+            const int bf = b * p.F + f_begin + it - 1;
+            for (int t = 0; t < n_tiles; ++t, ++qc) {
+                const int s = qc & 1, slot = qc % 3;
+                if (!(ok = mbar_wait_warp(&o_full[slot], (qc / 3) & 1, abort_flag))) break;
+                tc_fence_after();
+                uint8_t *qs = sm + s * kImgBytes;
+                float ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(qs + (c >> 3) * kImgPanel + r * kRowB +
+                                                                     (((c & 7) ^ (r & 7)) << 4));
+                    float f8[8];
+                    bf16x8_to_f32(u, f8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
+                }
+                const float rq = rsqrtf(ss + kEps);
+                const uint32_t acc = tmem + 128 * (slot + 1) + lane_off;
+#pragma unroll
+                for (int cc = 0; cc < 7; ++cc) {
+                    uint32_t ra[16];
+                    tmem_ld16(acc + cc * 16, ra);
+                    tmem_ld_wait();
+                    float o[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
+                    const int c8 = cc * 2;
+                    *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
+                        f32x8_to_bf16(o);
+                    *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
+                        f32x8_to_bf16(o + 8);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&o_free[slot]);
+                    const int row0 = t * kTQ + quad * 32;
+                    if (row0 < p.N) {
+                        tma_store_4d(&mapO, qs + quad * 32 * kRowB, 0, h, row0, bf);
+                        tma_store_4d(&mapO, qs + kImgPanel + quad * 32 * kRowB, 64, h, row0, bf);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
+                    mbar_arrive(&q_empty[s]);
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ================================================================= host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 4-D view [B*F][N][H][D] of a bf16 [B][F*N][H][D] tensor, 128B swizzle,
+// boxes of 64 head-dim elements x `rows` tokens of one head of one frame.
+bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N, int rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B * F};
+    cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2, (cuuint64_t)N * H * kD * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+bool tc_plan(int B, int H, int F, int N, int /*num_sms*/, TcPlan *plan)
+{
+    if (B <= 0 || H <= 0 || F <= 0 || N <= 0) return false;
+    const long long BH = (long long)B * H;
+    if (BH > (1 << 20) || (long long)F * N > (1LL << 30)) return false;
+    // Chunk count minimising (waves of one-CTA-per-SM) x (frames per chunk),
+    // plus a small charge for each sequential boundary step.
+    int best_n = 1;
+    double best = 1e300;
+    for (int n = 1; n <= F; ++n) {
+        const int L = (F + n - 1) / n;
+        const int n_real = (F + L - 1) / L;
+        if (n_real != n) continue;
+        const long long ctas = BH * n;
+        const double waves = (double)((ctas + kSms - 1) / kSms);
+        const double cost = waves * L * 1.0 + 0.04 * n;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_n = n;
+        }
+    }
+    plan->B = B;
+    plan->H = H;
+    plan->F = F;
+    plan->N = N;
+    plan->n_chunks = best_n;
+    plan->chunk = (F + best_n - 1) / best_n;
+    plan->off_frames = 0;
+    plan->off_comp = align_up((size_t)BH * F * kFrameWs, 256);
+    plan->off_start = align_up(plan->off_comp + (size_t)BH * best_n * 2 * kStateBytes, 256);
+    plan->ws_bytes = align_up(plan->off_start + (size_t)BH * best_n * kStateBytes, 256);
+    return true;
+}
+
+cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o, const TcPlan &pl, float c, void *workspace,
+                                unsigned *status, cudaStream_t stream, cudaEvent_t *events)
+{
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS) ||
+        !make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, 32))
+        return cudaErrorInvalidValue;
+    static bool attrs_done = false;
+    if (!attrs_done) {
+        cudaError_t e = cudaFuncSetAttribute(k1_frame_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kK1Smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k2_scan_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK2Smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k1b_chunk_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kK1bSmem);
+        if (e != cudaSuccess) return e;
+        attrs_done = true;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int BH = pl.B * pl.H;
+    K1Params p1;
+    p1.beta = beta;
+    p1.gamma = gamma;
+    p1.ws_frames = ws + pl.off_frames;
+    p1.ws_comp = reinterpret_cast<float *>(ws + pl.off_comp);
+    p1.status = status;
+    p1.B = pl.B;
+    p1.H = pl.H;
+    p1.F = pl.F;
+    p1.N = pl.N;
+    p1.chunk = pl.chunk;
+    p1.n_chunks = pl.n_chunks;
+    p1.c = c;
+    cudaError_t e;
+    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
+    k1_frame_stats_kernel<<<BH * pl.n_chunks, kK1Threads, kK1Smem, stream>>>(mk, mv, p1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
+    k1b_chunk_boundary_kernel<<<dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream>>>(
+        p1.ws_comp, reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
+    K2Params p2;
+    p2.gamma = gamma;
+    p2.ws_frames = ws + pl.off_frames;
+    p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
+    p2.status = status;
+    p2.B = pl.B;
+    p2.H = pl.H;
+    p2.F = pl.F;
+    p2.N = pl.N;
+    p2.chunk = pl.chunk;
+    p2.n_chunks = pl.n_chunks;
+    k2_scan_output_kernel<<<BH * pl.n_chunks, kK2Threads, kK2Smem, stream>>>(mq, mo, p2);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+}  // namespace gdn

@@ -1,0 +1,231 @@
+"""Thin Python binding over the C ABI of libgdn_b300.so (include/gdn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  If the
+library is missing or fails to load, every call raises — there is no fallback.
+
+The raw C entry points are exposed under their C names (``gdn_frame_fwd`` ...)
+taking torch tensors; ``frame_fwd`` / ``frame_step`` / ``frame_fwd_f32`` are
+conveniences that allocate outputs and workspace with torch and check status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn_b300.so")
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_UNSUPPORTED = 2
+GDN_ERR_CUDA = 3
+GDN_ERR_TIMEOUT = 4
+GDN_ERR_WORKSPACE = 5
+
+EXPORTED = [
+    "gdn_version", "gdn_status_string", "gdn_frame_fwd_workspace_size", "gdn_frame_fwd",
+    "gdn_frame_step_workspace_size", "gdn_frame_step", "gdn_frame_fwd_f32", "gdn_device_status",
+    "gdn_frame_fwd_profiled", "gdn_frame_fwd_host_buffer_size", "gdn_frame_fwd_host",
+]
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgdn_b300.so (built in-tree by gated_deltanet_wise_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libgdn_b300.so not built ({LIB_PATH}); run python -m gated_deltanet_wise_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.gdn_version.restype = I
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [I]
+        L.gdn_frame_fwd_workspace_size.restype = Z
+        L.gdn_frame_fwd_workspace_size.argtypes = [I] * 5
+        L.gdn_frame_step_workspace_size.restype = Z
+        L.gdn_frame_step_workspace_size.argtypes = [I] * 4
+        L.gdn_frame_fwd.restype = I
+        L.gdn_frame_fwd.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
+        L.gdn_frame_step.restype = I
+        L.gdn_frame_step.argtypes = [P] * 8 + [I] * 4 + [F, P, Z, P]
+        L.gdn_frame_fwd_f32.restype = I
+        L.gdn_frame_fwd_f32.argtypes = [P] * 8 + [I] * 5 + [F, P]
+        L.gdn_device_status.restype = I
+        L.gdn_device_status.argtypes = [P]
+        L.gdn_frame_fwd_profiled.restype = I
+        L.gdn_frame_fwd_profiled.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P, P]
+        L.gdn_frame_fwd_host_buffer_size.restype = Z
+        L.gdn_frame_fwd_host_buffer_size.argtypes = [I] * 5
+        L.gdn_frame_fwd_host.restype = I
+        L.gdn_frame_fwd_host.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_status(st: int, what: str):
+    if st != GDN_OK:
+        raise GdnError(st, what)
+
+
+# ---------------------------------------------------------------- raw C entry points
+def gdn_frame_fwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
+    return int(lib().gdn_frame_fwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_frame_step_workspace_size(B: int, H: int, N: int, D: int) -> int:
+    return int(lib().gdn_frame_step_workspace_size(B, H, N, D))
+
+
+def gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace, workspace_bytes,
+                  stream=None) -> int:
+    return int(lib().gdn_frame_fwd(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                   B, H, F, N, D, float(key_scale), _p(workspace), int(workspace_bytes),
+                                   _stream(stream)))
+
+
+def gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, workspace, workspace_bytes,
+                   stream=None) -> int:
+    return int(lib().gdn_frame_step(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                    B, H, N, D, float(key_scale), _p(workspace), int(workspace_bytes),
+                                    _stream(stream)))
+
+
+def gdn_frame_fwd_f32(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, stream=None) -> int:
+    return int(lib().gdn_frame_fwd_f32(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                       B, H, F, N, D, float(key_scale), _stream(stream)))
+
+
+def gdn_device_status(stream=None) -> int:
+    return int(lib().gdn_device_status(_stream(stream)))
+
+
+def gdn_frame_fwd_profiled(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+                           workspace_bytes, events, stream=None) -> int:
+    """``events``: 4 torch.cuda.Event(enable_timing=True) recorded around the internal launches."""
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events]) if events else None
+    return int(lib().gdn_frame_fwd_profiled(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                            B, H, F, N, D, float(key_scale), _p(workspace), int(workspace_bytes),
+                                            _stream(stream), arr))
+
+
+def gdn_frame_fwd_host_buffer_size(B: int, H: int, F: int, N: int, D: int) -> int:
+    return int(lib().gdn_frame_fwd_host_buffer_size(B, H, F, N, D))
+
+
+def gdn_frame_fwd_host(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, device_buffer,
+                       device_buffer_bytes, stream=None) -> int:
+    """Host tensors in (pinned CPU memory for asynchronous copies), host tensors out."""
+    return int(lib().gdn_frame_fwd_host(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                        B, H, F, N, D, float(key_scale), _p(device_buffer),
+                                        int(device_buffer_bytes), _stream(stream)))
+
+
+# ---------------------------------------------------------------- conveniences
+def _shape(q: torch.Tensor, gamma: torch.Tensor) -> Tuple[int, int, int, int, int]:
+    B, FN, H, D = q.shape
+    F = gamma.shape[1]
+    if F == 0:
+        return B, H, 0, 0, D
+    if FN % F:
+        raise ValueError("q.shape[1] must be F * N")
+    return B, H, F, FN // F, D
+
+
+def _check(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Workspace:
+    """Grow-only device workspace owned by the caller (the library never allocates)."""
+
+    def __init__(self):
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int, device) -> Optional[torch.Tensor]:
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = Workspace()
+
+
+def frame_fwd(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, o=None, S_out=None,
+              workspace: Optional[Workspace] = None, stream=None):
+    """bf16 frame-wise GDN forward.  Returns (o [B, F*N, H, D] bf16, S_out [B, H, D, D] fp32)."""
+    B, H, F, N, D = _shape(q, gamma)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, torch.bfloat16, n)
+    _check(beta, torch.float32, "beta")
+    _check(gamma, torch.float32, "gamma")
+    if S_in is not None:
+        _check(S_in, torch.float32, "S_in")
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device) if S_out is None else S_out
+    nbytes = gdn_frame_fwd_workspace_size(B, H, F, N, D)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_fwd_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, q.device)
+    st = gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_fwd")
+    return o, S_out
+
+
+def frame_step(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, o=None, S_out=None,
+               workspace: Optional[Workspace] = None, stream=None):
+    """One latent frame: q/k/v [B, N, H, D] bf16, beta [B, N, H], gamma [B, H]."""
+    B, N, H, D = q.shape
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device) if S_out is None else S_out
+    nbytes = gdn_frame_step_workspace_size(B, H, N, D)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_step_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, q.device)
+    st = gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_step")
+    return o, S_out
+
+
+def frame_fwd_f32(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, stream=None):
+    """fp32 validation path.  Returns (o fp32, S_out fp32)."""
+    B, H, F, N, D = _shape(q, gamma)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, torch.float32, n)
+    o = torch.empty_like(q)
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device)
+    st = gdn_frame_fwd_f32(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, stream)
+    _check_status(st, "gdn_frame_fwd_f32")
+    return o, S_out

@@ -1,0 +1,169 @@
+/*
+ * gdn.h — C ABI of the B300 (sm_103a) frame-wise Gated DeltaNet forward library
+ * (libgdn_b300.so).
+ *
+ * The operation (summary page "SANA-WM: Efficient Minute-Scale World Modeling
+ * with Hybrid Linear Diffusion Transformer", section 方法步骤详情, module 2
+ * "Memory-Efficient Long-Context"; section 前置知识 "Gated DeltaNet"):
+ * for every chain (b, h) the D x D state is carried across latent frames
+ * f = 0..F-1,
+ *     k^_n   = k_n / ||k_n||_2 * c_k          (c_k = key_scale, default 1/sqrt(D*N))
+ *     q^_n   = q_n / ||q_n||_2
+ *     A_f    = sum_n beta_n k^_n k^_n^T,  U_f = sum_n beta_n v_n k^_n^T
+ *     S_f    = S_{f-1} (gamma_f I - A_f) + U_f      (= S_{f-1} M_f + U_f)
+ *     o_{f,n} = S_f q^_n                             (every token of frame f)
+ * with ||x||_2 = sqrt(sum x^2 + 1e-12).  S[i][j]: i = value index (row),
+ * j = key index (column).
+ *
+ * Layouts (all row-major, innermost dimension contiguous):
+ *   q, k, v, o : [B][F*N][H][D]   token-major, heads interleaved (bf16 or fp32)
+ *   beta       : [B][F*N][H]      fp32
+ *   gamma      : [B][F][H]        fp32
+ *   S_in/S_out : [B][H][D][D]     fp32
+ *
+ * Conventions shared by every entry point:
+ *   - Memory: the caller owns every buffer.  The library never allocates;
+ *     scratch comes from the caller as `workspace` of at least the size the
+ *     matching *_workspace_size() returns.  All pointers are device pointers.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and the call returns without synchronising.  Argument
+ *     errors are detected on the host and returned before anything is
+ *     enqueued.  A device-side failure (a bounded wait that expired) is
+ *     recorded in a per-device status word, read by gdn_device_status().
+ *   - Alignment: q, k, v, o, S_in, S_out and workspace must be 16-byte
+ *     aligned; beta and gamma 4-byte aligned.
+ *   - Aliasing: S_out may alias S_in; no other buffers may overlap.
+ *   - S_in == NULL means a zero initial state; S_out == NULL skips writing the
+ *     final state.
+ *   - Degenerate sizes: B*H == 0 is a no-op; F == 0 copies S_in (or zeros) to
+ *     S_out; N == 0 applies pure decay S_f = gamma_f S_{f-1} and writes no o.
+ */
+#ifndef GDN_B300_GDN_H
+#define GDN_B300_GDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad workspace size */
+    GDN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. D != 112 on bf16) */
+    GDN_ERR_CUDA = 3,         /* a CUDA runtime call failed (no device, launch failure, ...) */
+    GDN_ERR_TIMEOUT = 4,      /* a bounded device-side wait expired (see gdn_device_status) */
+    GDN_ERR_WORKSPACE = 5     /* workspace pointer missing or smaller than required */
+} gdn_status_t;
+
+/* A cudaStream_t, passed through untouched. */
+typedef void *gdn_stream_t;
+
+/* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
+int gdn_version(void);
+
+/* Static text for a status code (never NULL). */
+const char *gdn_status_string(gdn_status_t status);
+
+/*
+ * Bytes of device workspace gdn_frame_fwd needs for these sizes (bf16 path).
+ * Returns 0 for sizes that need none (degenerate sizes) and (size_t)-1 for
+ * invalid sizes.  The layout is private to the library.
+ */
+size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D);
+
+/*
+ * Frame-wise GDN forward over F frames, bf16 q/k/v/o, fp32 beta/gamma/state.
+ * Computes the recurrence above for every (b, h) chain; writes o for every
+ * token and the final state S_{F-1} to S_out.
+ *   q, k, v   : bf16 [B][F*N][H][D], read only
+ *   o         : bf16 [B][F*N][H][D], written
+ *   beta      : fp32 [B][F*N][H];  gamma: fp32 [B][F][H]
+ *   S_in      : fp32 [B][H][D][D] or NULL;  S_out: fp32 [B][H][D][D] or NULL
+ *   key_scale : c_k; <= 0 selects the default 1/sqrt(D*N)
+ *   workspace : >= gdn_frame_fwd_workspace_size(B,H,F,N,D) bytes, 16-byte aligned
+ * This build implements D == 112 (the model's head size); other D return
+ * GDN_ERR_UNSUPPORTED.  Results match the fp64 definition within a relative
+ * Frobenius error of 5e-3 on o and S_out for inputs drawn as in the tests.
+ */
+gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v,
+                           const float *beta, const float *gamma,
+                           const float *S_in, float *S_out, void *o,
+                           int B, int H, int F, int N, int D, float key_scale,
+                           void *workspace, size_t workspace_bytes,
+                           gdn_stream_t stream);
+
+/*
+ * Streaming step: one latent frame (F = 1) per call, state carried by the
+ * caller (chunk-causal / autoregressive generation; resume by passing the
+ * previous call's S_out as S_in).  Same layouts with F = 1:
+ *   q, k, v, o : bf16 [B][N][H][D];  beta: fp32 [B][N][H];  gamma: fp32 [B][H]
+ * Workspace: gdn_frame_step_workspace_size(B, H, N, D) bytes.
+ * Output equals gdn_frame_fwd run frame by frame on the same S_in.
+ */
+size_t gdn_frame_step_workspace_size(int B, int H, int N, int D);
+gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v,
+                            const float *beta, const float *gamma,
+                            const float *S_in, float *S_out, void *o,
+                            int B, int H, int N, int D, float key_scale,
+                            void *workspace, size_t workspace_bytes,
+                            gdn_stream_t stream);
+
+/*
+ * fp32 validation entry: the same operation with fp32 q/k/v/o, computed with
+ * fp32 CUDA-core arithmetic (one CTA per chain).  Any 1 <= D <= 128.  Needs no
+ * workspace.  Intended for numerical validation (relative error ~1e-6), not
+ * for speed.
+ */
+gdn_status_t gdn_frame_fwd_f32(const float *q, const float *k, const float *v,
+                               const float *beta, const float *gamma,
+                               const float *S_in, float *S_out, float *o,
+                               int B, int H, int F, int N, int D, float key_scale,
+                               gdn_stream_t stream);
+
+/*
+ * gdn_frame_fwd that also records CUDA events around its internal launches,
+ * for per-stage timing.  `events` points to 4 cudaEvent_t created by the
+ * caller; they are recorded on `stream` before the frame-statistics kernel,
+ * after it, after the chunk-boundary scan and after the output kernel, so that
+ * cudaEventElapsedTime(e[i], e[i+1]) is the duration of stage i.  Same
+ * arguments, errors and results as gdn_frame_fwd otherwise; `events` may be
+ * NULL.  For degenerate sizes no event is recorded.
+ */
+gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v,
+                                    const float *beta, const float *gamma,
+                                    const float *S_in, float *S_out, void *o,
+                                    int B, int H, int F, int N, int D, float key_scale,
+                                    void *workspace, size_t workspace_bytes,
+                                    gdn_stream_t stream, void **events);
+
+/*
+ * Host-buffer form of gdn_frame_fwd: q/k/v/beta/gamma/S_in are host pointers
+ * (pinned memory gives asynchronous copies), o and S_out are host pointers
+ * written on completion.  `device_buffer` (caller-owned device memory of
+ * gdn_frame_fwd_host_buffer_size() bytes, 256-byte aligned) holds the device
+ * copies and the workspace.  The call enqueues the host-to-device copies, the
+ * forward pass and the device-to-host copies on `stream` and returns; the
+ * results are valid after the stream is synchronised.  S_in may be NULL (zero
+ * state); S_out may be NULL.
+ */
+size_t gdn_frame_fwd_host_buffer_size(int B, int H, int F, int N, int D);
+gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,
+                                const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o,
+                                int B, int H, int F, int N, int D, float key_scale,
+                                void *device_buffer, size_t device_buffer_bytes,
+                                gdn_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: GDN_OK, or GDN_ERR_TIMEOUT if a kernel's bounded wait expired since the
+ * last call (that launch's outputs are then undefined).
+ */
+gdn_status_t gdn_device_status(gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_B300_GDN_H */

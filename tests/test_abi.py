@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/gdn.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_deltanet_wise_b300 import build
+    build.build()
+    from gated_deltanet_wise_b300 import gdn
+    return gdn.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    from gated_deltanet_wise_b300 import gdn
+    assert sorted(gdn.EXPORTED) == names
+
+
+def test_version_and_status_strings(L):
+    from gated_deltanet_wise_b300 import gdn
+    assert L.gdn_version() >= 100
+    for s in range(6):
+        assert gdn.status_string(s)
+    assert gdn.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(L):
+    from gated_deltanet_wise_b300 import gdn
+    SZ_ERR = 2 ** 64 - 1
+    assert gdn.gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112) > 20 * 121 * 80000
+    assert gdn.gdn_frame_fwd_workspace_size(1, 20, 0, 880, 112) == 0
+    assert gdn.gdn_frame_fwd_workspace_size(0, 20, 4, 880, 112) == 0
+    assert gdn.gdn_frame_fwd_workspace_size(1, 20, 4, 0, 112) == 0
+    assert gdn.gdn_frame_fwd_workspace_size(-1, 20, 4, 8, 112) == SZ_ERR
+    assert gdn.gdn_frame_fwd_workspace_size(1, 1, 4, 8, 64) == SZ_ERR   # bf16 path is D = 112
+    assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 112) == gdn.gdn_frame_fwd_workspace_size(1, 20, 1, 880, 112)
+    # the workspace grows linearly in frames (per-frame images dominate)
+    a = gdn.gdn_frame_fwd_workspace_size(1, 4, 10, 880, 112)
+    b = gdn.gdn_frame_fwd_workspace_size(1, 4, 20, 880, 112)
+    assert 1.8 < b / a < 2.2
+
+
+def test_host_side_validation_without_gpu(L):
+    from gated_deltanet_wise_b300 import gdn
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    args = dict(q=fake, k=fake, v=fake, beta=fake, gamma=fake, S_in=None, S_out=fake, o=fake)
+
+    def fwd(B, H, F, N, D, ws=None, nbytes=0, **over):
+        a = dict(args, **over)
+        return L.gdn_frame_fwd(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"],
+                               B, H, F, N, D, 0.0, ws, nbytes, None)
+
+    assert fwd(-1, 1, 1, 1, 112) == gdn.GDN_ERR_INVALID_ARG
+    assert fwd(1, 1, 1, 1, 0) == gdn.GDN_ERR_INVALID_ARG
+    assert fwd(0, 4, 4, 4, 112) == gdn.GDN_OK            # empty batch: no-op
+    assert fwd(1, 1, 2, 8, 64) == gdn.GDN_ERR_UNSUPPORTED
+    assert fwd(1, 1, 2, 8, 112, q=None) == gdn.GDN_ERR_INVALID_ARG
+    assert fwd(1, 1, 2, 8, 112, k=P(0x10008)) == gdn.GDN_ERR_INVALID_ARG   # misaligned
+    assert fwd(1, 1, 2, 8, 112, S_out=P(0x10004)) == gdn.GDN_ERR_INVALID_ARG
+    assert fwd(1, 1, 2, 8, 112, ws=None, nbytes=0) == gdn.GDN_ERR_WORKSPACE
+    need = gdn.gdn_frame_fwd_workspace_size(1, 1, 2, 8, 112)
+    assert fwd(1, 1, 2, 8, 112, ws=fake, nbytes=need - 16) == gdn.GDN_ERR_WORKSPACE
+    assert fwd(1, 1, 2, 8, 112, ws=P(0x10008), nbytes=need) == gdn.GDN_ERR_INVALID_ARG
+    f32 = L.gdn_frame_fwd_f32
+    assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, 1, 1, 1, 129, 0.0, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, -1, 1, 1, 16, 0.0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert f32(None, fake, fake, fake, fake, None, fake, fake, 1, 1, 1, 1, 16, 0.0, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from gated_deltanet_wise_b300 import gdn
+    monkeypatch.setattr(gdn, "_lib", None)
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        gdn.lib()

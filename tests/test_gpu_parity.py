@@ -1,0 +1,206 @@
+"""CUDA path vs the fp64 oracle, element by element on the same seeded inputs.
+
+Tolerances: relative Frobenius error <= 5e-3 on o and S_out for the bf16 path
+(bf16 I/O, fp32 state) and <= 1e-5 for the fp32 validation path.  Large
+workloads are checked on sampled (batch, head) chains, each over every frame:
+chains are independent, so a sampled chain is an exact oracle case.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_wise_b300 import gdn
+from gated_deltanet_wise_b300.inputs import make_inputs, make_workload
+from tests.conftest import rel_fro
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 5e-3
+TOL_F32 = 1e-5
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    gdn.lib()
+    yield
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def chain_slice(x, b, h):
+    """Inputs of one (b, h) chain as a B=1, H=1 problem."""
+    S0 = None if x.S0 is None else x.S0[b:b + 1, h:h + 1]
+    return (x.q[b:b + 1, :, h:h + 1], x.k[b:b + 1, :, h:h + 1], x.v[b:b + 1, :, h:h + 1],
+            x.beta[b:b + 1, :, h:h + 1], x.gamma[b:b + 1, :, h:h + 1], S0)
+
+
+def check_chains(x, o, S, chains, tol=TOL_BF16):
+    worst = 0.0
+    for (b, h) in chains:
+        o_ref, S_ref = oracle.frame_fwd(*chain_slice(x, b, h))
+        eo = rel_fro(o[b:b + 1, :, h:h + 1].float().cpu().numpy(), o_ref)
+        es = rel_fro(S[b:b + 1, h:h + 1].float().cpu().numpy(), S_ref)
+        assert eo <= tol and es <= tol, ((b, h), eo, es)
+        worst = max(worst, eo, es)
+    return worst
+
+
+# ------------------------------------------------------------------ fp32 path
+def test_f32_tiny_config_seed0():
+    """B=1, H=1, D=16, F=4, N=8, fp32, seed 0, S_0 = 0."""
+    x = make_workload("tiny_f32", device=DEV)
+    o, S = gdn.frame_fwd_f32(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert rel_fro(o.cpu().numpy(), o_ref) <= TOL_F32
+    assert rel_fro(S.cpu().numpy(), S_ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("B,H,F,N,D", [(2, 3, 5, 37, 16), (1, 2, 3, 200, 112), (1, 1, 2, 65, 128), (2, 1, 3, 9, 7)])
+def test_f32_shapes(B, H, F, N, D):
+    x = make_inputs(B, H, F, N, D, dtype="f32", seed=B * 100 + N, device=DEV, s0_std=0.3)
+    o, S = gdn.frame_fwd_f32(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert rel_fro(o.cpu().numpy(), o_ref) <= TOL_F32
+    assert rel_fro(S.cpu().numpy(), S_ref) <= TOL_F32
+
+
+# ------------------------------------------------------------------ bf16 path
+def test_bf16_single_head_config():
+    """B=1, H=1, D=112, F=16, N=880 (40 x 22 latent grid), S_0 = 0."""
+    x = make_workload("single_head", device=DEV)
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    eo, es = rel_fro(o.float().cpu().numpy(), o_ref), rel_fro(S.cpu().numpy(), S_ref)
+    print(f"single head: rel_fro o={eo:.3e} S={es:.3e}")
+    assert eo <= TOL_BF16 and es <= TOL_BF16
+    # output error is dominated by the final bf16 rounding (~1.7e-3)
+    assert eo < 2.5e-3 and es < 1e-4
+
+
+@pytest.mark.parametrize("B,H,F,N", [(1, 1, 1, 1), (2, 3, 5, 15), (1, 2, 7, 64), (1, 2, 9, 65), (2, 1, 3, 130),
+                                     (1, 3, 4, 200), (1, 1, 40, 16)])
+def test_bf16_ragged_shapes(B, H, F, N):
+    """Tails of 64-token stages and 128-token tiles, several chunks, random S_0."""
+    x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=7 * F + N, device=DEV, s0_std=0.1)
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+    assert rel_fro(S.cpu().numpy(), S_ref) <= TOL_BF16
+
+
+def test_bf16_layer_60s_720p_sampled_chains():
+    """B=1, H=20, D=112, F=121, N=880: full run, oracle on three whole chains."""
+    x = make_workload("layer_60s_720p", device=DEV)
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    torch.cuda.synchronize()
+    w = check_chains(x, o, S, [(0, 0), (0, 7), (0, 19)])
+    print(f"layer 60s 720p: worst sampled rel_fro {w:.3e}")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+
+
+@pytest.mark.parametrize("N", [220, 880, 3520])
+def test_bf16_cfg_batch_sweep_sampled_chains(N):
+    """B=2 (cond/uncond), H=20, F=121, N in {220, 880, 3520}: oracle on two chains."""
+    x = make_workload(f"cfg_b2_n{N}", device=DEV)
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    torch.cuda.synchronize()
+    check_chains(x, o, S, [(0, 3), (1, 17)])
+
+
+def test_streaming_step_equals_full_forward():
+    """121 single-frame calls carrying S (S_0 ~ N(0, 0.01)) equal one full forward on the same S_0."""
+    x = make_workload("streaming_60s_720p", device=DEV)
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    o_full, S_full = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    S = x.S0.clone()
+    o_steps = torch.empty_like(o_full)
+    ws = gdn.Workspace()
+    for f in range(F):
+        sl = slice(f * N, (f + 1) * N)
+        o_f, S = gdn.frame_step(x.q[:, sl].contiguous(), x.k[:, sl].contiguous(), x.v[:, sl].contiguous(),
+                                x.beta[:, sl].contiguous(), x.gamma[:, f].contiguous(), S, workspace=ws)
+        o_steps[:, sl] = o_f
+    torch.cuda.synchronize()
+    for f in range(0, F, 10):
+        sl = slice(f * N, (f + 1) * N)
+        assert rel_fro(o_steps[:, sl].float().cpu().numpy(), o_full[:, sl].float().cpu().numpy()) <= TOL_BF16
+    assert rel_fro(S.cpu().numpy(), S_full.cpu().numpy()) <= TOL_BF16
+    check_chains(x, o_steps, S, [(0, 5)])
+
+
+def test_split_calls_equal_one_call():
+    x = make_inputs(1, 4, 12, 300, 112, dtype="bf16", seed=3, device=DEV, s0_std=0.1)
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    p = 5 * x.N
+    oa, Sa = gdn.frame_fwd(x.q[:, :p].contiguous(), x.k[:, :p].contiguous(), x.v[:, :p].contiguous(),
+                           x.beta[:, :p].contiguous(), x.gamma[:, :5].contiguous(), x.S0)
+    ob, Sb = gdn.frame_fwd(x.q[:, p:].contiguous(), x.k[:, p:].contiguous(), x.v[:, p:].contiguous(),
+                           x.beta[:, p:].contiguous(), x.gamma[:, 5:].contiguous(), Sa)
+    assert rel_fro(torch.cat([oa, ob], 1).float().cpu().numpy(), o.float().cpu().numpy()) <= TOL_BF16
+    assert rel_fro(Sb.cpu().numpy(), S.cpu().numpy()) <= TOL_BF16
+
+
+def test_deterministic_and_aliasing():
+    x = make_inputs(1, 5, 9, 333, 112, dtype="bf16", seed=11, device=DEV, s0_std=0.2)
+    o1, S1 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o2, S2 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    S_alias = x.S0.clone()
+    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, S_alias, S_out=S_alias)
+    assert S3.data_ptr() == S_alias.data_ptr()
+    assert torch.equal(o3, o1) and torch.equal(S3, S1)
+
+
+def test_output_canaries_untouched():
+    """o is written exactly inside its extent: guard regions before and after stay intact."""
+    B, H, F, N, D = 1, 3, 4, 150, 112
+    x = make_inputs(B, H, F, N, D, dtype="bf16", seed=5, device=DEV)
+    n = B * F * N * H * D
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device=DEV)
+    o = buf[pad:pad + n].view(B, F * N, H, D)
+    S_buf = torch.full((B * H * D * D + 2 * pad,), 3.0, dtype=torch.float32, device=DEV)
+    S_out = S_buf[pad:pad + B * H * D * D].view(B, H, D, D)
+    gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, None, o=o, S_out=S_out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + n:] == 7.0)
+    assert torch.all(S_buf[:pad] == 3.0) and torch.all(S_buf[pad + B * H * D * D:] == 3.0)
+    o_ref, _ = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, None)
+    assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_degenerate_sizes():
+    D = 112
+    S0 = torch.randn(2, 3, D, D, device=DEV)
+    gamma = torch.rand(2, 4, 3, device=DEV) * 0.9 + 0.05
+    e = torch.empty(2, 0, 3, D, dtype=torch.bfloat16, device=DEV)
+    be = torch.empty(2, 0, 3, device=DEV)
+    # N = 0: pure decay by prod gamma
+    S_out = torch.empty_like(S0)
+    st = gdn.gdn_frame_fwd(e, e, e, be, gamma, S0, S_out, e, 2, 3, 4, 0, D, 0.0, None, 0)
+    assert st == gdn.GDN_OK
+    expect = gamma.prod(1)[:, :, None, None] * S0
+    torch.testing.assert_close(S_out, expect, rtol=1e-5, atol=1e-6)
+    # F = 0: state passes through
+    st = gdn.gdn_frame_fwd(e, e, e, be, gamma[:, :0].contiguous(), S0, S_out, e, 2, 3, 0, 5, D, 0.0, None, 0)
+    assert st == gdn.GDN_OK
+    torch.testing.assert_close(S_out, S0)
+
+
+def test_beta_zero_pure_decay_on_gpu():
+    x = make_inputs(1, 2, 6, 100, 112, dtype="bf16", seed=2, device=DEV, s0_std=0.5)
+    x.beta.zero_()
+    o, S = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    expect = x.gamma.prod(1)[:, :, None, None] * x.S0
+    assert rel_fro(S.cpu().numpy(), expect.cpu().numpy()) < 1e-5
+    o_ref, _ = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def test_device_status_clean():
+    x = make_inputs(1, 1, 2, 10, 112, dtype="bf16", seed=1, device=DEV)
+    gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma)
+    assert gdn.gdn_device_status() == gdn.GDN_OK
