@@ -81,24 +81,39 @@ def ncu_traffic(kernel):
 
 # ------------------------------------------------------------- clock sampling
 class ClockSampler:
-    """Polls NVML (read-only) every ~2 ms on a thread while the timed region runs."""
+    """Samples SM clocks and clock-event reasons (read-only) while the timed region runs.
+
+    NVML is polled every ~2 ms on a thread (the device is found by PCI bus id,
+    since NVML numbers every GPU of the machine); if NVML is unavailable the
+    recipe's nvidia-smi query runs as a subprocess instead.
+    """
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
-    def __init__(self, index):
-        self.samples, self.reasons, self.max_mhz = [], 0, None
+    def __init__(self, device):
+        import torch
+        self.samples, self.reasons, self.max_mhz, self.error = [], 0, None, None
         self._stop = threading.Event()
         self._th = None
+        self._proc = None
+        self.bus = None
+        try:
+            props = torch.cuda.get_device_properties(device)
+            self.bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except Exception as e:  # pragma: no cover - depends on the torch build
+            self.error = f"pci id: {e}"
+        self.nv = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
+            h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus.encode()) if self.bus else \
+                pynvml.nvmlDeviceGetHandleByIndex(0)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self.nv, self.h = pynvml, h
+        except Exception as e:
+            self.error = f"nvml: {e}"
 
     def _run(self):
         nv = self.nv
@@ -106,7 +121,8 @@ class ClockSampler:
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
                 self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-            except Exception:
+            except Exception as e:
+                self.error = f"nvml poll: {e}"
                 break
             time.sleep(0.002)
 
@@ -114,19 +130,51 @@ class ClockSampler:
         if self.nv:
             self._th = threading.Thread(target=self._run, daemon=True)
             self._th.start()
+        else:
+            import subprocess
+            import tempfile
+            self._log = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "20"]
+            if self.bus:
+                cmd += ["-i", self.bus]
+            try:
+                self._proc = subprocess.Popen(cmd, stdout=self._log, stderr=subprocess.DEVNULL)
+            except Exception as e:
+                self.error = f"nvidia-smi: {e}"
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self._th:
             self._th.join()
+        if self._proc:
+            self._proc.terminate()
+            self._proc.wait()
+            self._log.seek(0)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in self._log.read().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons |= {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40,
+                                         "sw_thermal_slowdown": 0x20, "sw_power_cap": 0x4}[n]
 
     def summary(self):
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+               "reasons": [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"],
+               "samples": len(self.samples), "source": "nvml" if self.nv else "nvidia-smi"}
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
-        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples)}
+            out["error"] = self.error or "no samples"
+        return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -147,7 +195,7 @@ def cpu_baseline(x, target_s=15.0):
     """Oracle timed on the host cores on a bounded sample; value in full-layer tokens/s."""
     import oracle
     threads = oracle.num_threads()
-    heads = min(x.H, threads)
+    heads = x.H
     t1 = oracle_sample(x, heads, 1)
     frames = max(1, min(x.F, int(target_s / max(t1, 1e-3))))
     t = oracle_sample(x, heads, frames) if frames > 1 else t1
@@ -196,7 +244,7 @@ def run_ours(args):
 
     world, rank, local = dist_setup(args)
     dev = torch.device("cuda", torch.cuda.current_device())
-    x = make_workload(args.workload, device=dev, seed=rank)
+    x = make_workload(args.workload, device=dev, seed=rank, F=args.frames)
     B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
     o = torch.empty_like(x.q)
     S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
@@ -215,10 +263,12 @@ def run_ours(args):
         step()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in [t0, t1] + [e for row in ev for e in row]:
+        e.record(stream)  # creates the CUDA events outside the timed region
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if world == 1 else local) as clk:
+    with ClockSampler(dev) as clk:
         t0.record(stream)
         for i in range(K):
             step(ev[i])
@@ -263,7 +313,7 @@ def run_ours(args):
                 "warmup": W, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": args.workload, "B": B, "H": H, "D": D, "F": F, "N": N, "tokens": tokens,
-                           "l2": "inputs 1.92 GB per step > 126 MB L2; no flush needed",
+                           "l2": f"inputs {alg['total'] / 1e9:.2f} GB per step > 126 MB L2; no flush needed",
                            "parallelism": f"replica x{world} (independent chains per rank)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K,
                 "clocks": clk.summary()}
@@ -351,6 +401,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--frames", type=int, default=None, help="override F (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

@@ -17,7 +17,8 @@
 //      MMA operands X = beta c^2/r^2 k, Y = beta c/r v (Y as bf16 hi + lo);
 //      tcgen05 accumulates A_f = X^T K and U_f = Y^T K in TMEM.  It writes
 //      A_f (bf16, as the MMA-ready image) and U_f (fp32) to the workspace and
-//      folds the chunk composite (C, H) with two more MMAs per frame.
+//      folds the chunk composite (C, H), held in TMEM, with two more MMAs per
+//      frame whose A operands (-bf16 C, -bf16 H) are staged in TMEM as well.
 //   K1b (chunk boundaries), row-parallel fp32: S_start(c+1) = S_start(c) C_c + H_c.
 //   K2 (state scan + output), one CTA per (chunk, chain): walks the chunk's
 //      frames with S in fp32 registers, S_f = gamma S - (S_hi + S_lo) A_f + U_f
@@ -61,12 +62,10 @@ constexpr int kTS = 64;                               // tokens per stage
 constexpr uint32_t kTSPanel = kTS * kRowB;            // 8192
 constexpr uint32_t kStageBytes = 8 * kTSPanel;        // K, V->Y_hi, Y_lo, X (2 panels each) = 65536
 constexpr uint32_t kOffK = 0, kOffY = 2 * kTSPanel, kOffYlo = 4 * kTSPanel, kOffX = 6 * kTSPanel;
-constexpr int kK1Stages = 2;
+constexpr int kK1Stages = 3;
 constexpr int kK1Threads = 320;                       // producer, MMA, 8 math warps
-constexpr uint32_t kK1OffAimg = kK1Stages * kStageBytes;   // 131072
-constexpr uint32_t kK1OffCimg = kK1OffAimg + kAimgBytes;   // 159744
-constexpr uint32_t kK1OffHimg = kK1OffCimg + kImgBytes;    // 192512
-constexpr uint32_t kK1OffBar = kK1OffHimg + kImgBytes;     // 225280
+constexpr uint32_t kK1OffAimg = kK1Stages * kStageBytes;   // 196608
+constexpr uint32_t kK1OffBar = kK1OffAimg + kAimgBytes;    // 225280
 constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
 
 // K2
@@ -133,6 +132,15 @@ struct K1Params {
     float c;
 };
 
+// Tensor memory of K1 (512 columns, fp32 unless noted):
+//   [  0,128) acc_A: A_f = X^T K; after read-out it holds the composite MMAs'
+//             A operands: -bf16(C) in columns [0,56), -bf16(H) in [56,112)
+//             (bf16 pairs per column, one matrix row per lane)
+//   [128,256) acc_U: U_f = Y_hi^T K + Y_lo^T K
+//   [256,384) T_C: chunk transition composite C = prod M_f
+//   [384,512) T_H: chunk input composite H (state reached from zero)
+constexpr uint32_t kTmAccA = 0, kTmAccU = 128, kTmC = 256, kTmH = 384, kTmImgC = 0, kTmImgH = 56;
+
 __global__ void __launch_bounds__(kK1Threads, 1)
     k1_frame_stats_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                           const K1Params p)
@@ -140,11 +148,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK1OffBar);
-    uint64_t *st_full = bars + 0, *st_prep = bars + 2, *st_empty = bars + 4;
-    uint64_t *acc_full = bars + 6, *comp_full = bars + 8, *acc_free = bars + 10, *aimg_ready = bars + 12;
-    uint64_t *drain = bars + 13;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+    uint64_t *st_full = bars + 0, *st_prep = bars + kK1Stages, *st_empty = bars + 2 * kK1Stages;
+    uint64_t *acc_full = bars + 3 * kK1Stages, *comp_ready = acc_full + 1, *comp_done = acc_full + 2;
+    uint64_t *drain = acc_full + 3, *grp = acc_full + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(acc_full + 6);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = p.B * p.H;
@@ -155,40 +163,22 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const int n_st = (p.N + kTS - 1) / kTS;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kK1Stages; ++i) {
             mbar_init(&st_full[i], 1);
             mbar_init(&st_prep[i], 8);
             mbar_init(&st_empty[i], 1);
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&comp_full[i], 1);
-            mbar_init(&acc_free[i], 8);
         }
-        mbar_init(aimg_ready, 8);
+        mbar_init(acc_full, 1);
+        mbar_init(comp_ready, 8);
+        mbar_init(comp_done, 1);
         mbar_init(drain, 1);
+        mbar_init(grp, 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
-    }
-    // Math warps: composite images start as -I (C) and 0 (H); rows 112..127 stay 0.
-    if (warp >= 2) {
-        const int mt = threadIdx.x - 64;
-        uint4 z = make_uint4(0, 0, 0, 0);
-        for (int o = mt * 16; o < 2 * (int)kImgBytes; o += 256 * 16)
-            *reinterpret_cast<uint4 *>(sm + kK1OffCimg + o) = z;
-    }
-    __syncthreads();
-    if (warp >= 2) {
-        const int mt = threadIdx.x - 64;
-        if (mt < kD) {  // -1 on the diagonal of the C image
-            __nv_bfloat16 m1 = __float2bfloat16(-1.f);
-            const int col = mt, panel = col >> 6, chunk = (col & 63) >> 3;
-            *reinterpret_cast<__nv_bfloat16 *>(sm + kK1OffCimg + panel * kImgPanel + sw128_off(mt, chunk) +
-                                               2 * (col & 7)) = m1;
-        }
-        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -200,13 +190,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int it = 0, issued[2] = {0, 0};
+            int it = 0, issued[kK1Stages] = {};
             bool ok = true;
             for (int fl = 0; fl < nf && ok; ++fl) {
                 const int bf = b * p.F + f_begin + fl;
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const int s = it & 1;
-                    if (it >= 2 && !(ok = mbar_wait(&st_empty[s], ((it >> 1) - 1) & 1, abort_flag))) break;
+                    const int s = it % kK1Stages, use = it / kK1Stages;
+                    if (use >= 1 && !(ok = mbar_wait(&st_empty[s], (use - 1) & 1, abort_flag))) break;
                     uint8_t *stg = sm + s * kStageBytes;
                     mbar_arrive_expect_tx(&st_full[s], 4 * kTSPanel);
                     tma_load_4d(stg + kOffK, &mapK, &st_full[s], 0, h, st * kTS, bf, pol);
@@ -217,52 +207,21 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                 }
             }
             if (*abort_flag)  // let loads already in flight land before the CTA exits
-                for (int s = 0; s < 2; ++s)
+                for (int s = 0; s < kK1Stages; ++s)
                     if (issued[s]) mbar_wait_drain(&st_full[s], (issued[s] - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int pending = -1;  // frame whose composite MMAs are not issued yet
-            auto issue_composite = [&](int fc) {
-                tc_fence_after();
-                const uint32_t acc_c = tmem + (fc & 1) * 256, acc_h = acc_c + 128;
-#pragma unroll
-                for (int ks = 0; ks < 7; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
-                    const uint64_t bdesc =
-                        sdesc_sw128(sbase + kK1OffAimg + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
-                    mma_bf16(acc_c, sdesc_sw128(sbase + kK1OffCimg + koff, 16, 1024), bdesc, kIdescK, ks > 0);
-                    mma_bf16(acc_h, sdesc_sw128(sbase + kK1OffHimg + koff, 16, 1024), bdesc, kIdescK, 1);
-                }
-                mma_commit(&comp_full[fc & 1]);
-            };
-            // Wait on `bar`, issuing the pending composite as soon as its A_f image is ready.
-            auto wait_serving = [&](uint64_t *bar, uint32_t par) -> bool {
-                const long long t0 = clock64();
-                while (true) {
-                    if (mbar_try_wait(bar, par)) return true;
-                    if (pending >= 0 && mbar_try_wait(aimg_ready, pending & 1)) {
-                        issue_composite(pending);
-                        pending = -1;
-                        continue;
-                    }
-                    if (*abort_flag) return false;
-                    if (clock64() - t0 > kSpinLimitCycles) {
-                        *abort_flag = 1;
-                        return false;
-                    }
-                }
-            };
             int it = 0;
             bool ok = true;
             for (int fl = 0; fl < nf && ok; ++fl) {
-                const int buf = fl & 1;
-                const uint32_t acc_a = tmem + buf * 256, acc_u = acc_a + 128;
-                if (fl >= 2) ok = wait_serving(&acc_free[buf], ((fl >> 1) - 1) & 1);
+                // the previous frame's composite MMAs read their A operands from the
+                // acc_A columns: they must finish before this frame accumulates there
+                if (fl >= 1 && !(ok = mbar_wait(comp_done, (fl - 1) & 1, abort_flag))) break;
                 for (int st = 0; st < n_st && ok; ++st, ++it) {
-                    const int s = it & 1;
-                    if (!(ok = wait_serving(&st_prep[s], (it >> 1) & 1))) break;
+                    const int s = it % kK1Stages, use = it / kK1Stages;
+                    if (!(ok = mbar_wait(&st_prep[s], use & 1, abort_flag))) break;
                     tc_fence_after();
                     const uint32_t stg = sbase + s * kStageBytes;
 #pragma unroll
@@ -270,21 +229,26 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                         const uint32_t o = ks * 2048;
                         const uint64_t bk = sdesc_sw128(stg + kOffK + o, kTSPanel, 1024);
                         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
-                        mma_bf16(acc_a, sdesc_sw128(stg + kOffX + o, kTSPanel, 1024), bk, kIdescMN, acc);
-                        mma_bf16(acc_u, sdesc_sw128(stg + kOffY + o, kTSPanel, 1024), bk, kIdescMN, acc);
-                        mma_bf16(acc_u, sdesc_sw128(stg + kOffYlo + o, kTSPanel, 1024), bk, kIdescMN, 1u);
+                        mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffX + o, kTSPanel, 1024), bk, kIdescMN, acc);
+                        mma_bf16(tmem + kTmAccU, sdesc_sw128(stg + kOffY + o, kTSPanel, 1024), bk, kIdescMN, acc);
+                        mma_bf16(tmem + kTmAccU, sdesc_sw128(stg + kOffYlo + o, kTSPanel, 1024), bk, kIdescMN, 1u);
                     }
                     mma_commit(&st_empty[s]);
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[buf]);
-                if (pending >= 0) {
-                    if (!(ok = mbar_wait(aimg_ready, pending & 1, abort_flag))) break;
-                    issue_composite(pending);
+                mma_commit(acc_full);
+                // composite: T_C += (-C) A_f, T_H += (-H) A_f (T_C, T_H pre-scaled by gamma, T_H += U_f)
+                if (!(ok = mbar_wait(comp_ready, fl & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint64_t bdesc =
+                        sdesc_sw128(sbase + kK1OffAimg + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
+                    mma_bf16_tmem_a(tmem + kTmC, tmem + kTmImgC + ks * 8, bdesc, kIdescK, 1u);
+                    mma_bf16_tmem_a(tmem + kTmH, tmem + kTmImgH + ks * 8, bdesc, kIdescK, 1u);
                 }
-                pending = fl;
+                mma_commit(comp_done);
             }
-            if (ok && pending >= 0 && mbar_wait(aimg_ready, pending & 1, abort_flag)) issue_composite(pending);
             mma_commit(drain);  // every MMA issued above has completed once this phase lands
             mbar_wait_drain(drain, 0);
         }
@@ -296,27 +260,48 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         const int row = quad * 32 + lane;          // TMEM lane = matrix row
         const int ncc = half ? 3 : 4;              // 16-column chunks in this half
         const int col0 = half * 64;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         // prep mapping: token r, quarter qq (panel qq>>1, chunks (qq&1)*4..+3)
         const int r = mt >> 2, qq = mt & 3;
         const uint32_t prep_off = (qq >> 1) * kTSPanel + r * kRowB;
-        float Creg[64], Hreg[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            Creg[j] = (row == col0 + j) ? 1.f : 0.f;
-            Hreg[j] = 0.f;
-        }
         const size_t FN = (size_t)p.F * p.N;
-        int it = 0;
+        int it = 0, grp_phase = 0;
         bool ok = true;
 
-        auto prep_stage = [&](int fl, int st) {
-            const int s = it & 1;
-            if (!(ok = mbar_wait_warp(&st_full[s], (it >> 1) & 1, abort_flag))) return;
-            uint8_t *stg = sm + s * kStageBytes;
+        // composites start at C = I, H = 0 (rows 112..127 stay zero)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            if (cc < ncc) {
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    uint32_t wc[8], wz[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        wc[j] = (row == col0 + cc * 16 + g8 * 8 + j) ? __float_as_uint(1.f) : 0u;
+                        wz[j] = 0u;
+                    }
+                    tmem_st8(tmem + lane_off + kTmC + col0 + cc * 16 + g8 * 8, wc);
+                    tmem_st8(tmem + lane_off + kTmH + col0 + cc * 16 + g8 * 8, wz);
+                }
+            }
+        }
+        tmem_st_wait();
+
+        auto load_beta = [&](int fl, int st) -> float {
             const int n = st * kTS + r;
-            const int f = f_begin + fl;
-            float bt = 0.f;
-            if (n < p.N) bt = p.beta[((size_t)b * FN + (size_t)f * p.N + n) * p.H + h];
+            if (fl >= nf || n >= p.N) return 0.f;
+            return __ldg(p.beta + ((size_t)b * FN + (size_t)(f_begin + fl) * p.N + n) * p.H + h);
+        };
+        float bt_next = load_beta(0, 0);
+        float g_frame[2] = {0.f, 0.f};  // gamma of frames with parity 0 / 1
+
+        auto prep_stage = [&](int fl, int st) {
+            const int s = it % kK1Stages, use = it / kK1Stages;
+            const float bt = bt_next;
+            bt_next = (st + 1 < n_st) ? load_beta(fl, st + 1) : load_beta(fl + 1, 0);
+            if (st == 0) g_frame[fl & 1] = __ldg(p.gamma + ((size_t)b * p.F + f_begin + fl) * p.H + h);
+            if (!(ok = mbar_wait_warp(&st_full[s], use & 1, abort_flag))) return;
+            uint8_t *stg = sm + s * kStageBytes;
             float kf[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -356,24 +341,27 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         const int img_rows = quad == 3 ? kD - 96 : 32;
         const uint32_t img_off = half * kAimgPanel + quad * 32 * kRowB;
 
+        // Frame epilogue: read A_f and U_f out of TMEM, write them to the workspace,
+        // scale the composites by gamma (+U_f into H) and stage -bf16(C), -bf16(H)
+        // as the composite MMAs' A operands.
         auto epilogue = [&](int fe) {
-            const int buf = fe & 1;
             const int f = f_begin + fe;
-            const uint32_t acc_a = tmem + buf * 256 + col0, acc_u = acc_a + 128;
-            const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
             // this warp's previous A_f bulk store must have finished reading its slice
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            if (!(ok = mbar_wait_warp(&acc_full[buf], (fe >> 1) & 1, abort_flag))) return;
+            if (!(ok = mbar_wait_warp(acc_full, fe & 1, abort_flag))) return;
             tc_fence_after();
             uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
             float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
+            const float g = g_frame[fe & 1];
+            // pass 1: A_f -> bf16 image (shared memory), U_f -> workspace
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 if (cc < ncc) {
+                    const uint32_t col = col0 + cc * 16;
                     uint32_t ra[16], ru[16];
-                    tmem_ld16(acc_a + lane_off + cc * 16, ra);
-                    tmem_ld16(acc_u + lane_off + cc * 16, ru);
+                    tmem_ld16(tmem + lane_off + kTmAccA + col, ra);
+                    tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
                     tmem_ld_wait();
                     if (row < kD) {
                         float a[16];
@@ -382,7 +370,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                         uint8_t *dst = sm + kK1OffAimg + half * kAimgPanel;
                         *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc)) = f32x8_to_bf16(a);
                         *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(a + 8);
-                        float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col0 + cc * 16);
+                        float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             u4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
@@ -390,75 +378,87 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                     }
                 }
             }
+            // every math warp has read acc_A before any warp writes the composite
+            // images over those columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(grp);
+            if (!(ok = mbar_wait_warp(grp, grp_phase & 1, abort_flag))) return;
+            ++grp_phase;
+            tc_fence_after();
+            // pass 2: H <- gamma H + U_f, C <- gamma C; A operands -bf16(H_prev), -bf16(C_prev)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < ncc) {
+                    const uint32_t col = col0 + cc * 16;
+                    uint32_t ru[16], rh[16], rc[16];
+                    tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
+                    tmem_ld16(tmem + lane_off + kTmH + col, rh);
+                    tmem_ld16(tmem + lane_off + kTmC + col, rc);
+                    tmem_ld_wait();
+                    uint32_t hn0[8], hn1[8], cn0[8], cn1[8], ih[8], ic[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        hn0[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[j]), __uint_as_float(ru[j])));
+                        hn1[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[8 + j]), __uint_as_float(ru[8 + j])));
+                        cn0[j] = __float_as_uint(g * __uint_as_float(rc[j]));
+                        cn1[j] = __float_as_uint(g * __uint_as_float(rc[8 + j]));
+                        ih[j] = pack_bf16x2(-__uint_as_float(rh[2 * j]), -__uint_as_float(rh[2 * j + 1]));
+                        ic[j] = pack_bf16x2(-__uint_as_float(rc[2 * j]), -__uint_as_float(rc[2 * j + 1]));
+                    }
+                    tmem_st8(tmem + lane_off + kTmH + col, hn0);
+                    tmem_st8(tmem + lane_off + kTmH + col + 8, hn1);
+                    tmem_st8(tmem + lane_off + kTmC + col, cn0);
+                    tmem_st8(tmem + lane_off + kTmC + col + 8, cn1);
+                    tmem_st8(tmem + lane_off + kTmImgH + col / 2, ih);
+                    tmem_st8(tmem + lane_off + kTmImgC + col / 2, ic);
+                }
+            }
             if (half == 1 && row < kD) {  // key columns 112..127 of the image: zero
                 uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(aimg_ready);
+                mbar_arrive(comp_ready);
                 bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
                 bulk_commit();
             }
-            // composite: C <- gamma C + acc_C (= -C A_f), H <- gamma H + acc_H (= U_f - H A_f)
-            if (!(ok = mbar_wait_warp(&comp_full[buf], (fe >> 1) & 1, abort_flag))) return;
-            tc_fence_after();
-            const float g = p.gamma[((size_t)b * p.F + f) * p.H + h];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                if (cc < ncc) {
-                    uint32_t rc[16], rh[16];
-                    tmem_ld16(acc_a + lane_off + cc * 16, rc);
-                    tmem_ld16(acc_u + lane_off + cc * 16, rh);
-                    tmem_ld_wait();
-                    float cn[16], hn[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        Creg[cc * 16 + j] = fmaf(g, Creg[cc * 16 + j], __uint_as_float(rc[j]));
-                        Hreg[cc * 16 + j] = fmaf(g, Hreg[cc * 16 + j], __uint_as_float(rh[j]));
-                        cn[j] = -Creg[cc * 16 + j];
-                        hn[j] = -Hreg[cc * 16 + j];
-                    }
-                    if (row < kD) {
-                        uint8_t *dc = sm + kK1OffCimg + half * kImgPanel;
-                        uint8_t *dh = sm + kK1OffHimg + half * kImgPanel;
-                        *reinterpret_cast<uint4 *>(dc + sw128_off(row, 2 * cc)) = f32x8_to_bf16(cn);
-                        *reinterpret_cast<uint4 *>(dc + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(cn + 8);
-                        *reinterpret_cast<uint4 *>(dh + sw128_off(row, 2 * cc)) = f32x8_to_bf16(hn);
-                        *reinterpret_cast<uint4 *>(dh + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(hn + 8);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_free[buf]);
         };
 
         for (int fl = 0; fl < nf && ok; ++fl) {
             for (int st = 0; st < n_st && ok; ++st) {
                 prep_stage(fl, st);
-                if (ok && fl >= 1 && st == min(1, n_st - 1)) epilogue(fl - 1);
+                if (ok && fl >= 1 && st == 0) epilogue(fl - 1);
             }
         }
         if (ok) epilogue(nf - 1);
-        if (ok && row < kD) {
+        // chunk composites out: wait for the last frame's composite MMAs
+        if (ok && (ok = mbar_wait_warp(comp_done, (nf - 1) & 1, abort_flag))) {
+            tc_fence_after();
             float *comp = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 if (cc < ncc) {
+                    const uint32_t col = col0 + cc * 16;
+                    uint32_t rc[16], rh[16];
+                    tmem_ld16(tmem + lane_off + kTmC + col, rc);
+                    tmem_ld16(tmem + lane_off + kTmH + col, rh);
+                    tmem_ld_wait();
+                    if (row < kD) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const int col = col0 + cc * 16 + j;
-                        *reinterpret_cast<float4 *>(comp + row * kD + col) =
-                            make_float4(Creg[cc * 16 + j], Creg[cc * 16 + j + 1], Creg[cc * 16 + j + 2],
-                                        Creg[cc * 16 + j + 3]);
-                        *reinterpret_cast<float4 *>(comp + kStateFloats + row * kD + col) =
-                            make_float4(Hreg[cc * 16 + j], Hreg[cc * 16 + j + 1], Hreg[cc * 16 + j + 2],
-                                        Hreg[cc * 16 + j + 3]);
+                        for (int j = 0; j < 16; j += 4) {
+                            *reinterpret_cast<float4 *>(comp + row * kD + col + j) =
+                                make_float4(__uint_as_float(rc[j]), __uint_as_float(rc[j + 1]),
+                                            __uint_as_float(rc[j + 2]), __uint_as_float(rc[j + 3]));
+                            *reinterpret_cast<float4 *>(comp + kStateFloats + row * kD + col + j) =
+                                make_float4(__uint_as_float(rh[j]), __uint_as_float(rh[j + 1]),
+                                            __uint_as_float(rh[j + 2]), __uint_as_float(rh[j + 3]));
+                        }
                     }
                 }
             }
@@ -702,11 +702,14 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             if (lane == 0) mbar_arrive(s_ready);
         };
         write_images();
+        const float *gam = p.gamma + ((size_t)b * p.F + f_begin) * p.H + h;
+        float g_next = __ldg(gam);
         for (int it = 0; it < nf; ++it) {
+            const float g = g_next;
+            if (it + 1 < nf) g_next = __ldg(gam + (size_t)(it + 1) * p.H);
             if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
             if (!mbar_wait_warp(u_full, it & 1, abort_flag)) break;
             tc_fence_after();
-            const float g = p.gamma[((size_t)b * p.F + f_begin + it) * p.H + h];
             const float *U = reinterpret_cast<const float *>(sm + kK2OffU) + (row < kD ? row : 0) * kUStride;
 #pragma unroll
             for (int cc = 0; cc < 7; ++cc) {

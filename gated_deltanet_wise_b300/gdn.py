@@ -128,7 +128,12 @@ def gdn_device_status(stream=None) -> int:
 def gdn_frame_fwd_profiled(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
                            workspace_bytes, events, stream=None) -> int:
     """``events``: 4 torch.cuda.Event(enable_timing=True) recorded around the internal launches."""
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events]) if events else None
+    arr = None
+    if events:
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+                e.record(torch.cuda.current_stream() if stream is None else stream)
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     return int(lib().gdn_frame_fwd_profiled(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
                                             B, H, F, N, D, float(key_scale), _p(workspace), int(workspace_bytes),
                                             _stream(stream), arr))

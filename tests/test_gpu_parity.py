@@ -204,3 +204,36 @@ def test_device_status_clean():
     x = make_inputs(1, 1, 2, 10, 112, dtype="bf16", seed=1, device=DEV)
     gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma)
     assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def test_profiled_entry_records_stage_events():
+    x = make_inputs(1, 4, 6, 300, 112, dtype="bf16", seed=4, device=DEV, s0_std=0.1)
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o = torch.empty_like(x.q)
+    S = torch.empty_like(S_ref)
+    nb = gdn.gdn_frame_fwd_workspace_size(B, H, F, N, D)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    st = gdn.gdn_frame_fwd_profiled(x.q, x.k, x.v, x.beta, x.gamma, x.S0, S, o, B, H, F, N, D, 0.0, ws, nb, ev)
+    assert st == gdn.GDN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(S, S_ref)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(t > 0 for t in times)
+
+
+def test_host_buffer_entry_matches_device_entry():
+    """gdn_frame_fwd_host: pinned host buffers in and out, copies and compute on one stream."""
+    x = make_inputs(1, 3, 5, 200, 112, dtype="bf16", seed=6, device=DEV, s0_std=0.1)
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    hq, hk, hv, hb, hg, hs = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.beta, x.gamma, x.S0))
+    ho = torch.empty_like(hq).pin_memory()
+    hS = torch.empty(B, H, D, D).pin_memory()
+    nb = gdn.gdn_frame_fwd_host_buffer_size(B, H, F, N, D)
+    dbuf = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    st = gdn.gdn_frame_fwd_host(hq, hk, hv, hb, hg, hs, hS, ho, B, H, F, N, D, 0.0, dbuf, nb)
+    assert st == gdn.GDN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(ho, o_ref.cpu()) and torch.equal(hS, S_ref.cpu())
