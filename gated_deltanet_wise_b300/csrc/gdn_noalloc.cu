@@ -1,0 +1,70 @@
+// gdn_noalloc.cu — a streaming step that allocates nothing and needs no
+// caller-supplied scratch.
+//
+// gdn_frame_step needs a device workspace from its caller.  Some callers
+// cannot call cudaMalloc (or any allocating routine) at the point where they
+// run a frame: a host that has handed the whole device memory budget to its
+// own pool and gives plug-ins only input/output pointers, a per-frame
+// real-time loop that must not take the allocator's locks or its latency, or
+// code running inside a stream capture in which allocation calls are
+// prohibited.  For them the step's scratch lives in the fixed array below,
+// which every GPU that loads this library holds until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+namespace {
+
+// Maximum scratch of the no-alloc step: 16 MiB per device.  At D = 112 one
+// chain (batch x head) of a step needs about 226 KiB, so up to 72 chains fit
+// (for example B = 2, H = 20).
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+
+static __device__ __align__(256) unsigned char g_step_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices];
+
+// Device address of g_step_scratch on the current device.  Host code only sees
+// a stand-in for the array's name, so the address is looked up once per device
+// (with that device current) and cached.
+void *scratch_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_step_scratch) != cudaSuccess || !p) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+size_t gdn_frame_step_noalloc_limit_bytes(void) { return gdn::kNoAllocScratchBytes; }
+
+gdn_status_t gdn_frame_step_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                                    const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int N,
+                                    int D, float key_scale, gdn_stream_t stream)
+{
+    const size_t need = gdn_frame_step_workspace_size(B, H, N, D);
+    if (need == (size_t)-1) return D > 0 && D != 112 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
+    if (need > gdn::kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
+    if (need == 0)  // degenerate sizes use no scratch
+        return gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, nullptr, 0, stream);
+    void *scratch = gdn::scratch_address();
+    if (!scratch) return GDN_ERR_CUDA;
+    return gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, scratch,
+                          gdn::kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"

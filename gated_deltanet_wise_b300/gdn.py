@@ -30,6 +30,7 @@ EXPORTED = [
     "gdn_version", "gdn_status_string", "gdn_frame_fwd_workspace_size", "gdn_frame_fwd",
     "gdn_frame_step_workspace_size", "gdn_frame_step", "gdn_frame_fwd_f32", "gdn_device_status",
     "gdn_frame_fwd_profiled", "gdn_frame_fwd_host_buffer_size", "gdn_frame_fwd_host",
+    "gdn_frame_step_noalloc_limit_bytes", "gdn_frame_step_noalloc",
 ]
 
 _lib = None
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_fwd_host_buffer_size.argtypes = [I] * 5
         L.gdn_frame_fwd_host.restype = I
         L.gdn_frame_fwd_host.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
+        L.gdn_frame_step_noalloc_limit_bytes.restype = Z
+        L.gdn_frame_step_noalloc_limit_bytes.argtypes = []
+        L.gdn_frame_step_noalloc.restype = I
+        L.gdn_frame_step_noalloc.argtypes = [P] * 8 + [I] * 4 + [F, P]
         _lib = L
     return _lib
 
@@ -149,6 +154,16 @@ def gdn_frame_fwd_host(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_
     return int(lib().gdn_frame_fwd_host(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
                                         B, H, F, N, D, float(key_scale), _p(device_buffer),
                                         int(device_buffer_bytes), _stream(stream)))
+
+
+def gdn_frame_step_noalloc_limit_bytes() -> int:
+    return int(lib().gdn_frame_step_noalloc_limit_bytes())
+
+
+def gdn_frame_step_noalloc(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, stream=None) -> int:
+    """Streaming step whose scratch is the library's fixed device array (no workspace argument)."""
+    return int(lib().gdn_frame_step_noalloc(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                            B, H, N, D, float(key_scale), _stream(stream)))
 
 
 # ---------------------------------------------------------------- conveniences

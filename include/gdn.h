@@ -156,6 +156,38 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,
                                 gdn_stream_t stream);
 
 /*
+ * Streaming step without caller-supplied scratch.  The paper has no
+ * counterpart: this is a library convenience.  Same arguments, layouts and
+ * results as gdn_frame_step, minus the workspace.
+ *
+ * It is for callers that cannot allocate device memory where they run a
+ * frame.  Examples: a host that owns the whole device memory budget and hands
+ * plug-ins only input and output pointers; a per-frame real-time loop that
+ * must not take the allocator's locks or latency; code inside a stream capture
+ * in which allocation calls are prohibited.  The step's scratch is a fixed
+ * 16 MiB device array inside the library (gdn_frame_step_noalloc_limit_bytes()).
+ * Every GPU that loads the library holds it until the process exits.
+ *   - Limit: gdn_frame_step_workspace_size(B, H, N, D) must not exceed the
+ *     array (about 226 KiB per chain at D = 112, so B*H <= 72).  Larger
+ *     requests return GDN_ERR_WORKSPACE before anything is enqueued.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first call
+ *     before any stream capture.
+ *   - Sharing: all calls on a device share the one array, which keeps the last
+ *     call's contents.  No part of it needs to start at zero, because every
+ *     byte a call reads is written earlier in the same call.  Calls that
+ *     overlap on the GPU (other streams, other host threads) race on it and
+ *     corrupt each other's results: serialise them.
+ */
+size_t gdn_frame_step_noalloc_limit_bytes(void);
+gdn_status_t gdn_frame_step_noalloc(const void *q, const void *k, const void *v,
+                                    const float *beta, const float *gamma,
+                                    const float *S_in, float *S_out, void *o,
+                                    int B, int H, int N, int D, float key_scale,
+                                    gdn_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GDN_OK, or GDN_ERR_TIMEOUT if a kernel's bounded wait expired since the
  * last call (that launch's outputs are then undefined).
