@@ -13,9 +13,10 @@
 //
 // Three launches:
 //   K1 (frame statistics), one CTA per (chunk, chain): streams K and V through
-//      shared memory in 64-token stages; CUDA cores turn each token into the
-//      MMA operands X = beta c^2/r^2 k, Y = beta c/r v (Y as bf16 hi + lo);
-//      tcgen05 accumulates A_f = X^T K and U_f = Y^T K in TMEM.  It writes
+//      shared memory in 32-token stages; CUDA cores turn each key into the MMA
+//      operands k^ = c/r k (in place) and B = beta c/r k (as bf16 hi + lo);
+//      tcgen05 accumulates A_f = K^^T B_hi and U_f = V^T (B_hi + B_lo) in
+//      TMEM, with the raw V tile as an operand.  It writes
 //      A_f (bf16, as the MMA-ready image) and U_f (fp32) to the workspace and
 //      folds the chunk composite (C, H), held in TMEM, with two more MMAs per
 //      frame whose A operands (-bf16 C, -bf16 H) are staged in TMEM as well.
@@ -25,12 +26,12 @@
 //      on tcgen05, and computes O = Q (S_hi + S_lo)^T for 128-token tiles of Q
 //      (TMA in, TMA out), scaling each row by 1/||q|| in the epilogue.
 //
-// Precision: raw bf16 k, v, q are exact MMA operands; the per-token fp32
-// weights are folded into X and Y; U (the part of S that matters) uses a
-// hi/lo bf16 split of Y, and O uses a hi/lo split of S, so the only
-// unavoidable rounding is the bf16 output.  A_f itself is ~1/D in norm, so a
-// single bf16 rounding of A_f and of C/H in the composite products stays at
-// ~u/D relative.
+// Precision: raw bf16 v and q are exact MMA operands; the per-token fp32
+// weight beta c/r is folded into the key operand B; U (the part of S that
+// matters) uses a hi/lo bf16 split of B, and O uses a hi/lo split of S, so
+// the only unavoidable rounding is the bf16 output.  A_f itself is ~1/D in
+// norm, so bf16 roundings of its operands, of A_f and of C/H in the composite
+// products stay at ~u/D relative.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -58,12 +59,12 @@ constexpr uint32_t kStateFloats = kD * kD;           // 12544
 constexpr size_t kStateBytes = kStateFloats * 4;     // 50176
 
 // K1
-constexpr int kTS = 64;                               // tokens per stage
-constexpr uint32_t kTSPanel = kTS * kRowB;            // 8192
-constexpr uint32_t kStageBytes = 8 * kTSPanel;        // K, V->Y_hi, Y_lo, X (2 panels each) = 65536
-constexpr uint32_t kOffK = 0, kOffY = 2 * kTSPanel, kOffYlo = 4 * kTSPanel, kOffX = 6 * kTSPanel;
-constexpr int kK1Stages = 3;
-constexpr int kK1Threads = 320;                       // producer, MMA, 8 math warps
+constexpr int kTS = 32;                               // tokens per stage
+constexpr uint32_t kTSPanel = kTS * kRowB;            // 4096: one 64-column panel of a stage
+constexpr uint32_t kStageBytes = 8 * kTSPanel;        // K->K^, V, B_hi, B_lo (2 panels each) = 32768
+constexpr uint32_t kOffK = 0, kOffV = 2 * kTSPanel, kOffBhi = 4 * kTSPanel, kOffBlo = 6 * kTSPanel;
+constexpr int kK1Stages = 6;
+constexpr int kK1Threads = 448;                       // producer, MMA, 2 x 4 prep warps, 4 epilogue warps
 constexpr uint32_t kK1OffAimg = kK1Stages * kStageBytes;   // 196608
 constexpr uint32_t kK1OffBar = kK1OffAimg + kAimgBytes;    // 225280
 constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
@@ -165,14 +166,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kK1Stages; ++i) {
             mbar_init(&st_full[i], 1);
-            mbar_init(&st_prep[i], 8);
+            mbar_init(&st_prep[i], 4);
             mbar_init(&st_empty[i], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(comp_ready, 8);
+        mbar_init(comp_ready, 4);
         mbar_init(comp_done, 1);
         mbar_init(drain, 1);
-        mbar_init(grp, 8);
+        mbar_init(grp, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int it = 0, issued[kK1Stages] = {};
+            int it = 0;
             bool ok = true;
             for (int fl = 0; fl < nf && ok; ++fl) {
                 const int bf = b * p.F + f_begin + fl;
@@ -201,14 +202,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                     mbar_arrive_expect_tx(&st_full[s], 4 * kTSPanel);
                     tma_load_4d(stg + kOffK, &mapK, &st_full[s], 0, h, st * kTS, bf, pol);
                     tma_load_4d(stg + kOffK + kTSPanel, &mapK, &st_full[s], 64, h, st * kTS, bf, pol);
-                    tma_load_4d(stg + kOffY, &mapV, &st_full[s], 0, h, st * kTS, bf, pol);
-                    tma_load_4d(stg + kOffY + kTSPanel, &mapV, &st_full[s], 64, h, st * kTS, bf, pol);
-                    ++issued[s];
+                    tma_load_4d(stg + kOffV, &mapV, &st_full[s], 0, h, st * kTS, bf, pol);
+                    tma_load_4d(stg + kOffV + kTSPanel, &mapV, &st_full[s], 64, h, st * kTS, bf, pol);
                 }
             }
             if (*abort_flag)  // let loads already in flight land before the CTA exits
-                for (int s = 0; s < kK1Stages; ++s)
-                    if (issued[s]) mbar_wait_drain(&st_full[s], (issued[s] - 1) & 1);
+                for (int s = 0; s < kK1Stages && s < it; ++s)
+                    mbar_wait_drain(&st_full[s], ((it - 1 - s) / kK1Stages) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -227,11 +227,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 #pragma unroll
                     for (int ks = 0; ks < kTS / 16; ++ks) {
                         const uint32_t o = ks * 2048;
-                        const uint64_t bk = sdesc_sw128(stg + kOffK + o, kTSPanel, 1024);
+                        const uint64_t bhi = sdesc_sw128(stg + kOffBhi + o, kTSPanel, 1024);
+                        const uint64_t blo = sdesc_sw128(stg + kOffBlo + o, kTSPanel, 1024);
+                        const uint64_t av = sdesc_sw128(stg + kOffV + o, kTSPanel, 1024);
                         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
-                        mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffX + o, kTSPanel, 1024), bk, kIdescMN, acc);
-                        mma_bf16(tmem + kTmAccU, sdesc_sw128(stg + kOffY + o, kTSPanel, 1024), bk, kIdescMN, acc);
-                        mma_bf16(tmem + kTmAccU, sdesc_sw128(stg + kOffYlo + o, kTSPanel, 1024), bk, kIdescMN, 1u);
+                        mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffK + o, kTSPanel, 1024), bhi, kIdescMN, acc);
+                        mma_bf16(tmem + kTmAccU, av, bhi, kIdescMN, acc);
+                        mma_bf16(tmem + kTmAccU, av, blo, kIdescMN, 1u);
                     }
                     mma_commit(&st_empty[s]);
                 }
@@ -252,172 +254,163 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             mma_commit(drain);  // every MMA issued above has completed once this phase lands
             mbar_wait_drain(drain, 0);
         }
-    } else {
-        // ------------------------------------------ math warps (prep + epilogue)
-        const int mt = threadIdx.x - 64;          // 0..255
-        const int quad = warp & 3;                 // TMEM lane quadrant
-        const int half = (warp - 2) >> 2;          // column half: 0 -> cols 0..63, 1 -> 64..111
-        const int row = quad * 32 + lane;          // TMEM lane = matrix row
-        const int ncc = half ? 3 : 4;              // 16-column chunks in this half
-        const int col0 = half * 64;
-        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        // prep mapping: token r, quarter qq (panel qq>>1, chunks (qq&1)*4..+3)
-        const int r = mt >> 2, qq = mt & 3;
+    } else if (warp < 10) {
+        // ------------------------------------------------------ prep warps
+        // Two groups of four warps take alternate stages, so two stages are
+        // prepared at once.  Thread (token r, quarter qq) handles panel qq>>1,
+        // chunks 4*(qq&1).. of its token; the eight threads of a quarter-warp
+        // phase touch eight different bank groups.
+        const int grpi = (warp - 2) >> 2;          // 0: even stages, 1: odd stages
+        const int t = threadIdx.x - 64 - 128 * grpi;  // 0..127
+        const int r = t >> 2, qq = t & 3;
         const uint32_t prep_off = (qq >> 1) * kTSPanel + r * kRowB;
         const size_t FN = (size_t)p.F * p.N;
-        int it = 0, grp_phase = 0;
-        bool ok = true;
-
-        // composites start at C = I, H = 0 (rows 112..127 stay zero)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            if (cc < ncc) {
-#pragma unroll
-                for (int g8 = 0; g8 < 2; ++g8) {
-                    uint32_t wc[8], wz[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        wc[j] = (row == col0 + cc * 16 + g8 * 8 + j) ? __float_as_uint(1.f) : 0u;
-                        wz[j] = 0u;
-                    }
-                    tmem_st8(tmem + lane_off + kTmC + col0 + cc * 16 + g8 * 8, wc);
-                    tmem_st8(tmem + lane_off + kTmH + col0 + cc * 16 + g8 * 8, wz);
-                }
-            }
-        }
-        tmem_st_wait();
-
-        auto load_beta = [&](int fl, int st) -> float {
-            const int n = st * kTS + r;
-            if (fl >= nf || n >= p.N) return 0.f;
+        const int total = nf * n_st;
+        auto load_beta = [&](int itx) -> float {
+            if (itx >= total) return 0.f;
+            const int fl = itx / n_st, n = (itx - fl * n_st) * kTS + r;
+            if (n >= p.N) return 0.f;
             return __ldg(p.beta + ((size_t)b * FN + (size_t)(f_begin + fl) * p.N + n) * p.H + h);
         };
-        float bt_next = load_beta(0, 0);
-        float g_frame[2] = {0.f, 0.f};  // gamma of frames with parity 0 / 1
-
-        auto prep_stage = [&](int fl, int st) {
+        float bt_next = load_beta(grpi);
+        for (int it = grpi; it < total; it += 2) {
             const int s = it % kK1Stages, use = it / kK1Stages;
             const float bt = bt_next;
-            bt_next = (st + 1 < n_st) ? load_beta(fl, st + 1) : load_beta(fl + 1, 0);
-            if (st == 0) g_frame[fl & 1] = __ldg(p.gamma + ((size_t)b * p.F + f_begin + fl) * p.H + h);
-            if (!(ok = mbar_wait_warp(&st_full[s], use & 1, abort_flag))) return;
-            uint8_t *stg = sm + s * kStageBytes;
+            bt_next = load_beta(it + 2);
+            if (!mbar_wait_warp(&st_full[s], use & 1, abort_flag)) break;
+            uint8_t *stg = sm + s * kStageBytes + prep_off;
             float kf[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stg + kOffK + prep_off + pos), kf + 8 * i);
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stg + kOffK + pos), kf + 8 * i);
             }
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) ss = fmaf(kf[i], kf[i], ss);
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-            const float inv = p.c * rsqrtf(ss + kEps);
-            const float wx = bt * inv * inv, wy = bt * inv;
+            const float inv = p.c * rsqrtf(ss + kEps);   // c / ||k||
+            const float wb = bt * inv;                   // beta c / ||k||
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
-                float x[8], vf[8];
+                float kh[8], y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = wx * kf[8 * i + e];
-                *reinterpret_cast<uint4 *>(stg + kOffX + prep_off + pos) = f32x8_to_bf16(x);
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stg + kOffY + prep_off + pos), vf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vf[e] *= wy;
+                for (int e = 0; e < 8; ++e) {
+                    kh[e] = inv * kf[8 * i + e];
+                    y[e] = wb * kf[8 * i + e];
+                }
                 uint4 hi, lo;
-                split_bf16x8(vf, hi, lo);
-                *reinterpret_cast<uint4 *>(stg + kOffY + prep_off + pos) = hi;
-                *reinterpret_cast<uint4 *>(stg + kOffYlo + prep_off + pos) = lo;
+                split_bf16x8(y, hi, lo);
+                *reinterpret_cast<uint4 *>(stg + kOffK + pos) = f32x8_to_bf16(kh);
+                *reinterpret_cast<uint4 *>(stg + kOffBhi + pos) = hi;
+                *reinterpret_cast<uint4 *>(stg + kOffBlo + pos) = lo;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st_prep[s]);
-            ++it;
-        };
-
-        // This warp's slice of the A_f image: rows 32*quad.. of panel `half`
-        // (contiguous in shared memory and in the workspace image).
+        }
+    } else {
+        // ------------------------------------------------- epilogue warps
+        // One warp per TMEM lane quadrant; thread = matrix row, all 112 columns.
+        // Per frame: A_f and U_f out of TMEM into the workspace, the composites
+        // scaled by gamma (+U_f into H), and -bf16(C), -bf16(H) staged as the
+        // composite MMAs' A operands.
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int grp_phase = 0;
+        bool ok = true;
+        // composites start at C = I, H = 0 (rows 112..127 stay zero)
+#pragma unroll
+        for (int c8 = 0; c8 < kD / 8; ++c8) {
+            uint32_t wc[8], wz[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                wc[j] = (row == c8 * 8 + j) ? __float_as_uint(1.f) : 0u;
+                wz[j] = 0u;
+            }
+            tmem_st8(tmem + lane_off + kTmC + c8 * 8, wc);
+            tmem_st8(tmem + lane_off + kTmH + c8 * 8, wz);
+        }
+        tmem_st_wait();
+        // this warp's rows of the A_f image: rows 32*quad.. of each panel
         const int img_rows = quad == 3 ? kD - 96 : 32;
-        const uint32_t img_off = half * kAimgPanel + quad * 32 * kRowB;
-
-        // Frame epilogue: read A_f and U_f out of TMEM, write them to the workspace,
-        // scale the composites by gamma (+U_f into H) and stage -bf16(C), -bf16(H)
-        // as the composite MMAs' A operands.
-        auto epilogue = [&](int fe) {
+        const uint32_t img_off = quad * 32 * kRowB;
+        const float *gam = p.gamma + ((size_t)b * p.F + f_begin) * p.H + h;
+        float g_next = __ldg(gam);
+        for (int fe = 0; fe < nf && ok; ++fe) {
             const int f = f_begin + fe;
-            // this warp's previous A_f bulk store must have finished reading its slice
+            const float g = g_next;
+            if (fe + 1 < nf) g_next = __ldg(gam + (size_t)(fe + 1) * p.H);
+            // this warp's previous A_f bulk stores must have finished reading
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            if (!(ok = mbar_wait_warp(acc_full, fe & 1, abort_flag))) return;
+            if (!(ok = mbar_wait_warp(acc_full, fe & 1, abort_flag))) break;
             tc_fence_after();
             uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
             float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
-            const float g = g_frame[fe & 1];
             // pass 1: A_f -> bf16 image (shared memory), U_f -> workspace
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                if (cc < ncc) {
-                    const uint32_t col = col0 + cc * 16;
-                    uint32_t ra[16], ru[16];
-                    tmem_ld16(tmem + lane_off + kTmAccA + col, ra);
-                    tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
-                    tmem_ld_wait();
-                    if (row < kD) {
-                        float a[16];
+            for (int cc = 0; cc < 7; ++cc) {
+                const uint32_t col = cc * 16;
+                uint32_t ra[16], ru[16];
+                tmem_ld16(tmem + lane_off + kTmAccA + col, ra);
+                tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
+                tmem_ld_wait();
+                if (row < kD) {
+                    float a[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) a[j] = __uint_as_float(ra[j]);
-                        uint8_t *dst = sm + kK1OffAimg + half * kAimgPanel;
-                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc)) = f32x8_to_bf16(a);
-                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * cc + 1)) = f32x8_to_bf16(a + 8);
-                        float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col);
+                    for (int j = 0; j < 16; ++j) a[j] = __uint_as_float(ra[j]);
+                    uint8_t *dst = sm + kK1OffAimg + (cc >> 2) * kAimgPanel;
+                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3))) = f32x8_to_bf16(a);
+                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3) + 1)) = f32x8_to_bf16(a + 8);
+                    float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            u4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
-                                                __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
-                    }
+                    for (int j = 0; j < 4; ++j)
+                        u4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                            __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
                 }
             }
-            // every math warp has read acc_A before any warp writes the composite
+            if (row < kD) {  // key columns 112..127 of the image: zero
+                uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
+                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
+            }
+            // all four warps have read acc_A before any writes the composite
             // images over those columns
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(grp);
-            if (!(ok = mbar_wait_warp(grp, grp_phase & 1, abort_flag))) return;
+            if (!(ok = mbar_wait_warp(grp, grp_phase & 1, abort_flag))) break;
             ++grp_phase;
             tc_fence_after();
             // pass 2: H <- gamma H + U_f, C <- gamma C; A operands -bf16(H_prev), -bf16(C_prev)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                if (cc < ncc) {
-                    const uint32_t col = col0 + cc * 16;
-                    uint32_t ru[16], rh[16], rc[16];
-                    tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
-                    tmem_ld16(tmem + lane_off + kTmH + col, rh);
-                    tmem_ld16(tmem + lane_off + kTmC + col, rc);
-                    tmem_ld_wait();
-                    uint32_t hn0[8], hn1[8], cn0[8], cn1[8], ih[8], ic[8];
+            for (int cc = 0; cc < 7; ++cc) {
+                const uint32_t col = cc * 16;
+                uint32_t ru[16], rh[16], rc[16];
+                tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
+                tmem_ld16(tmem + lane_off + kTmH + col, rh);
+                tmem_ld16(tmem + lane_off + kTmC + col, rc);
+                tmem_ld_wait();
+                uint32_t hn0[8], hn1[8], cn0[8], cn1[8], ih[8], ic[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        hn0[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[j]), __uint_as_float(ru[j])));
-                        hn1[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[8 + j]), __uint_as_float(ru[8 + j])));
-                        cn0[j] = __float_as_uint(g * __uint_as_float(rc[j]));
-                        cn1[j] = __float_as_uint(g * __uint_as_float(rc[8 + j]));
-                        ih[j] = pack_bf16x2(-__uint_as_float(rh[2 * j]), -__uint_as_float(rh[2 * j + 1]));
-                        ic[j] = pack_bf16x2(-__uint_as_float(rc[2 * j]), -__uint_as_float(rc[2 * j + 1]));
-                    }
-                    tmem_st8(tmem + lane_off + kTmH + col, hn0);
-                    tmem_st8(tmem + lane_off + kTmH + col + 8, hn1);
-                    tmem_st8(tmem + lane_off + kTmC + col, cn0);
-                    tmem_st8(tmem + lane_off + kTmC + col + 8, cn1);
-                    tmem_st8(tmem + lane_off + kTmImgH + col / 2, ih);
-                    tmem_st8(tmem + lane_off + kTmImgC + col / 2, ic);
+                for (int j = 0; j < 8; ++j) {
+                    hn0[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[j]), __uint_as_float(ru[j])));
+                    hn1[j] = __float_as_uint(fmaf(g, __uint_as_float(rh[8 + j]), __uint_as_float(ru[8 + j])));
+                    cn0[j] = __float_as_uint(g * __uint_as_float(rc[j]));
+                    cn1[j] = __float_as_uint(g * __uint_as_float(rc[8 + j]));
+                    ih[j] = pack_bf16x2(-__uint_as_float(rh[2 * j]), -__uint_as_float(rh[2 * j + 1]));
+                    ic[j] = pack_bf16x2(-__uint_as_float(rc[2 * j]), -__uint_as_float(rc[2 * j + 1]));
                 }
-            }
-            if (half == 1 && row < kD) {  // key columns 112..127 of the image: zero
-                uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
-                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
+                tmem_st8(tmem + lane_off + kTmH + col, hn0);
+                tmem_st8(tmem + lane_off + kTmH + col + 8, hn1);
+                tmem_st8(tmem + lane_off + kTmC + col, cn0);
+                tmem_st8(tmem + lane_off + kTmC + col + 8, cn1);
+                tmem_st8(tmem + lane_off + kTmImgH + col / 2, ih);
+                tmem_st8(tmem + lane_off + kTmImgC + col / 2, ic);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -426,39 +419,30 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             if (lane == 0) {
                 mbar_arrive(comp_ready);
                 bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
+                bulk_s2g(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off, img_rows * kRowB);
                 bulk_commit();
             }
-        };
-
-        for (int fl = 0; fl < nf && ok; ++fl) {
-            for (int st = 0; st < n_st && ok; ++st) {
-                prep_stage(fl, st);
-                if (ok && fl >= 1 && st == 0) epilogue(fl - 1);
-            }
         }
-        if (ok) epilogue(nf - 1);
         // chunk composites out: wait for the last frame's composite MMAs
         if (ok && (ok = mbar_wait_warp(comp_done, (nf - 1) & 1, abort_flag))) {
             tc_fence_after();
             float *comp = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                if (cc < ncc) {
-                    const uint32_t col = col0 + cc * 16;
-                    uint32_t rc[16], rh[16];
-                    tmem_ld16(tmem + lane_off + kTmC + col, rc);
-                    tmem_ld16(tmem + lane_off + kTmH + col, rh);
-                    tmem_ld_wait();
-                    if (row < kD) {
+            for (int cc = 0; cc < 7; ++cc) {
+                const uint32_t col = cc * 16;
+                uint32_t rc[16], rh[16];
+                tmem_ld16(tmem + lane_off + kTmC + col, rc);
+                tmem_ld16(tmem + lane_off + kTmH + col, rh);
+                tmem_ld_wait();
+                if (row < kD) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            *reinterpret_cast<float4 *>(comp + row * kD + col + j) =
-                                make_float4(__uint_as_float(rc[j]), __uint_as_float(rc[j + 1]),
-                                            __uint_as_float(rc[j + 2]), __uint_as_float(rc[j + 3]));
-                            *reinterpret_cast<float4 *>(comp + kStateFloats + row * kD + col + j) =
-                                make_float4(__uint_as_float(rh[j]), __uint_as_float(rh[j + 1]),
-                                            __uint_as_float(rh[j + 2]), __uint_as_float(rh[j + 3]));
-                        }
+                    for (int j = 0; j < 16; j += 4) {
+                        *reinterpret_cast<float4 *>(comp + row * kD + col + j) =
+                            make_float4(__uint_as_float(rc[j]), __uint_as_float(rc[j + 1]),
+                                        __uint_as_float(rc[j + 2]), __uint_as_float(rc[j + 3]));
+                        *reinterpret_cast<float4 *>(comp + kStateFloats + row * kD + col + j) =
+                            make_float4(__uint_as_float(rh[j]), __uint_as_float(rh[j + 1]),
+                                        __uint_as_float(rh[j + 2]), __uint_as_float(rh[j + 3]));
                     }
                 }
             }
