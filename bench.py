@@ -83,14 +83,17 @@ def ncu_traffic(kernel):
 class ClockSampler:
     """Samples SM clocks and clock-event reasons (read-only) while the timed region runs.
 
-    NVML is polled every ~2 ms on a thread (the device is found by PCI bus id,
-    since NVML numbers every GPU of the machine); if NVML is unavailable the
-    recipe's nvidia-smi query runs as a subprocess instead.
+    NVML (the driver's libnvidia-ml.so.1, through ctypes) is polled every ~2 ms
+    on a thread; the device is found by PCI bus id, since NVML numbers every GPU
+    of the machine.  If NVML cannot be loaded, ``nvidia-smi`` runs as a
+    subprocess instead, and the sampler waits for its first sample before the
+    timed region starts.  Nothing here changes a GPU setting.
     """
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    NVML_CLOCK_SM = 1
 
     def __init__(self, device):
         import torch
@@ -106,43 +109,52 @@ class ClockSampler:
             self.error = f"pci id: {e}"
         self.nv = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus.encode()) if self.bus else \
-                pynvml.nvmlDeviceGetHandleByIndex(0)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-            self.nv, self.h = pynvml, h
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if self.bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(self.bus.encode(), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML handle for this device")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self._ct = nv, h, ctypes
         except Exception as e:
             self.error = f"nvml: {e}"
 
     def _run(self):
-        nv = self.nv
+        ct, nv = self._ct, self.nv
+        clk, rsn = ct.c_uint(), ct.c_ulonglong()
         while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-            except Exception as e:
-                self.error = f"nvml poll: {e}"
-                break
+            if nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self._reason_fn(self.h, ct.byref(rsn)) == 0:
+                self.reasons |= rsn.value
             time.sleep(0.002)
 
     def __enter__(self):
         if self.nv:
             self._th = threading.Thread(target=self._run, daemon=True)
             self._th.start()
-        else:
-            import subprocess
-            import tempfile
-            self._log = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-            cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "20"]
-            if self.bus:
-                cmd += ["-i", self.bus]
-            try:
-                self._proc = subprocess.Popen(cmd, stdout=self._log, stderr=subprocess.DEVNULL)
-            except Exception as e:
-                self.error = f"nvidia-smi: {e}"
+            return self
+        import subprocess
+        import tempfile
+        self._log = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "20"]
+        if self.bus:
+            cmd += ["-i", self.bus]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=self._log, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and os.path.getsize(self._log.name) == 0:
+                time.sleep(0.01)
+        except Exception as e:
+            self.error = f"nvidia-smi: {e}"
         return self
 
     def __exit__(self, *a):
@@ -153,7 +165,7 @@ class ClockSampler:
             self._proc.terminate()
             self._proc.wait()
             self._log.seek(0)
-            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20, "sw_power_cap": 0x4}
             for line in self._log.read().splitlines():
                 f = [x.strip() for x in line.split(",")]
                 if len(f) < 6:
@@ -163,10 +175,9 @@ class ClockSampler:
                     self.max_mhz = float(f[1])
                 except ValueError:
                     continue
-                for n, v in zip(names, f[2:6]):
+                for n, v in zip(bits, f[2:6]):
                     if v.lower() == "active":
-                        self.reasons |= {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40,
-                                         "sw_thermal_slowdown": 0x20, "sw_power_cap": 0x4}[n]
+                        self.reasons |= bits[n]
 
     def summary(self):
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
