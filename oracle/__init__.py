@@ -46,6 +46,8 @@ def _load():
         lib.oracle_gdn_frame_fwd.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_fwd_tokacc.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_transitions.argtypes = [P] * 4 + [I] * 5 + [Dbl, P, P]
+        lib.oracle_gdn_frame_fwd_product.argtypes = [P] * 6 + [I] * 5 + [Dbl, I, P, P]
+        lib.oracle_gdn_frame_transitions_product.argtypes = [P] * 4 + [I] * 5 + [Dbl, I, P, P]
         lib.oracle_gdn_composite.argtypes = [P, P, I, I, P, P]
         lib.oracle_gdn_compose.argtypes = [P, P, P, P, I, P, P]
         lib.oracle_num_threads.restype = I
@@ -70,13 +72,19 @@ def _shapes(q):
     return B, FN, H, D
 
 
-def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulation="recurrence"):
+def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulation="recurrence",
+              mode="sum", sub=64):
     """Frame-wise GDN forward in fp64.
 
     Shapes: q, k, v [B, F*N, H, D]; beta [B, F*N, H]; gamma [B, F, H];
     S_in [B, H, D, D] or None.  Returns (o [B, F*N, H, D] fp64, S_out [B, H, D, D] fp64).
-    ``formulation`` picks the printed recurrence ("recurrence", module 2 of the
-    method-details section) or the token-accumulation rewrite ("tokacc").
+    ``mode="sum"`` is the transition as printed in module 2 of the
+    method-details section, M_f = gamma_f I - sum_n beta_n k^_n k^_n^T; there
+    ``formulation`` picks the printed recurrence ("recurrence") or the
+    token-accumulation rewrite ("tokacc").  ``mode="product"`` is the
+    token-ordered reading M_f = gamma_f I - (I - prod_n (I - beta_n k^_n k^_n^T))
+    with the frame's tokens applied in order from zero for U_f, computed through
+    the UT transform over sub-chunks of ``sub`` tokens.
     """
     q, k, v, beta, gamma, S_in = (_f32(x) for x in (q, k, v, beta, gamma, S_in))
     B, FN, H, D = _shapes(q)
@@ -88,6 +96,11 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
         assert S_in.shape == (B, H, D, D)
     o = np.zeros((B, FN, H, D), np.float64)
     S_out = np.zeros((B, H, D, D), np.float64)
+    if mode == "product":
+        _load().oracle_gdn_frame_fwd_product(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(S_in),
+                                             B, H, F, N, D, float(key_scale), int(sub), _ptr(o), _ptr(S_out))
+        return o, S_out
+    assert mode == "sum", mode
     fn = {"recurrence": _load().oracle_gdn_frame_fwd,
           "tokacc": _load().oracle_gdn_frame_fwd_tokacc}[formulation]
     fn(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(S_in),
@@ -95,14 +108,22 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
     return o, S_out
 
 
-def frame_transitions(k, v, beta, gamma, key_scale=0.0):
-    """Per-frame (M_f, U_f), each [B, H, F, D, D] fp64 (module 2: M_t = gamma_t I - K^ beta K^T)."""
+def frame_transitions(k, v, beta, gamma, key_scale=0.0, mode="sum", sub=64):
+    """Per-frame (M_f, U_f), each [B, H, F, D, D] fp64 (module 2: M_t = gamma_t I - K^ beta K^T).
+
+    ``mode`` as in ``frame_fwd``; ``sub`` is the UT-transform sub-chunk of the product reading.
+    """
     k, v, beta, gamma = (_f32(x) for x in (k, v, beta, gamma))
     B, FN, H, D = _shapes(k)
     F = gamma.shape[1]
     N = FN // F
     M = np.zeros((B, H, F, D, D), np.float64)
     U = np.zeros((B, H, F, D, D), np.float64)
+    if mode == "product":
+        _load().oracle_gdn_frame_transitions_product(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),
+                                                     B, H, F, N, D, float(key_scale), int(sub), _ptr(M), _ptr(U))
+        return M, U
+    assert mode == "sum", mode
     _load().oracle_gdn_frame_transitions(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),
                                          B, H, F, N, D, float(key_scale), _ptr(M), _ptr(U))
     return M, U

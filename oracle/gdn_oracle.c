@@ -271,6 +271,152 @@ void oracle_gdn_compose(const double *C1, const double *H1, const double *C2,
     free(T);
 }
 
+/*
+ * Token-ordered ("product") reading of the frame transition.
+ *
+ * The page writes the frame's transition as gamma_t I - K^_t beta_t K^_t^T with
+ * beta_t between K^_t and K^_t^T.  Read with beta_t = diag(beta) this is the sum
+ * form above.  The token-wise Gated DeltaNet that the frame-wise one
+ * generalises (novelty section) instead applies the frame's tokens one after
+ * another, S <- S (I - beta_n k^_n k^_n^T) + beta_n v_n k^_n^T.  Over a run of
+ * tokens that product has the WY form
+ *     prod_n (I - beta_n k^_n k^_n^T) = I - K^ T K^^T,  state input V T K^^T,
+ * with the UT transform T = (I + StrictLower(diag(beta) K^^T K^))^-1 diag(beta)
+ * (the same printed shape with beta_t replaced by the matrix T).  This reading
+ * keeps the frame's decay where the printed formula puts it:
+ *     M_f = gamma_f I - (I - prod_n (I - beta_n k^_n k^_n^T)),
+ *     U_f = state reached from zero by the frame's tokens in order.
+ * The product is accumulated over sub-chunks of `sub` tokens.  Each sub-chunk
+ * forms its T explicitly (forward substitution of the unit lower-triangular
+ * matrix), then updates the pair (Abar = I - P, W) of the frame so far:
+ *     Abar <- Abar + (K_c - Abar K_c) T_c^T K_c^T,   W <- W + (V_c - W K_c) T_c^T K_c^T,
+ * the delta rule applied to the pair with the keys themselves as Abar's values.
+ */
+static void frame_transition_product(const float *k, const float *v, const float *beta,
+                                     const float *gamma, int b, int h, int f,
+                                     int H, int F, int N, int D, double c, int sub,
+                                     double *M, double *U)
+{
+    if (sub < 1) sub = 1;
+    double *Ab = calloc((size_t)D * D, sizeof(double));       /* Abar = I - P */
+    double *Kc = malloc(sizeof(double) * sub * D);              /* sub-chunk keys k^ */
+    double *Bc = malloc(sizeof(double) * sub);
+    double *L = malloc(sizeof(double) * sub * sub);             /* I + StrictLower(diag(b) G) */
+    double *T = malloc(sizeof(double) * sub * sub);             /* L^-1 diag(b) */
+    double *Ra = malloc(sizeof(double) * sub * D);              /* rows: k_n - Abar k_n */
+    double *Rw = malloc(sizeof(double) * sub * D);              /* rows: v_n - W k_n */
+    double *Xa = malloc(sizeof(double) * sub * D);              /* T (K - Abar K)^T rows */
+    double *Xw = malloc(sizeof(double) * sub * D);
+    memset(U, 0, sizeof(double) * D * D);                       /* W */
+    for (int n0 = 0; n0 < N; n0 += sub) {
+        int m = N - n0 < sub ? N - n0 : sub;
+        for (int a = 0; a < m; ++a) {
+            normalise(k + tok_index(b, f, n0 + a, h, 0, F, N, H, D), D, c, Kc + (size_t)a * D);
+            Bc[a] = beta[beta_index(b, f, n0 + a, h, F, N, H)];
+        }
+        /* L = I + StrictLower(diag(beta) K^T K) */
+        for (int a = 0; a < m; ++a)
+            for (int e = 0; e < m; ++e) {
+                double g = 0.0;
+                if (e < a)
+                    for (int d = 0; d < D; ++d) g += Kc[(size_t)a * D + d] * Kc[(size_t)e * D + d];
+                L[a * sub + e] = (a == e) ? 1.0 : (e < a ? Bc[a] * g : 0.0);
+            }
+        /* T = L^-1 diag(beta): column e solves L t = beta_e e_e by forward substitution */
+        for (int e = 0; e < m; ++e)
+            for (int a = 0; a < m; ++a) {
+                double s = (a == e) ? Bc[e] : 0.0;
+                for (int r = 0; r < a; ++r) s -= L[a * sub + r] * T[r * sub + e];
+                T[a * sub + e] = s;
+            }
+        /* residual rows against the pair's sub-chunk-start values */
+        for (int a = 0; a < m; ++a) {
+            const float *vn = v + tok_index(b, f, n0 + a, h, 0, F, N, H, D);
+            const double *ka = Kc + (size_t)a * D;
+            for (int i = 0; i < D; ++i) {
+                double sa = 0.0, sw = 0.0;
+                for (int j = 0; j < D; ++j) {
+                    sa += Ab[i * D + j] * ka[j];
+                    sw += U[i * D + j] * ka[j];
+                }
+                Ra[(size_t)a * D + i] = ka[i] - sa;
+                Rw[(size_t)a * D + i] = (double)vn[i] - sw;
+            }
+        }
+        /* new values X = T R (rows indexed by token) */
+        for (int a = 0; a < m; ++a)
+            for (int i = 0; i < D; ++i) {
+                double sa = 0.0, sw = 0.0;
+                for (int r = 0; r < m; ++r) {
+                    sa += T[a * sub + r] * Ra[(size_t)r * D + i];
+                    sw += T[a * sub + r] * Rw[(size_t)r * D + i];
+                }
+                Xa[(size_t)a * D + i] = sa;
+                Xw[(size_t)a * D + i] = sw;
+            }
+        /* pair += X^T K^ */
+        for (int a = 0; a < m; ++a) {
+            const double *ka = Kc + (size_t)a * D;
+            for (int i = 0; i < D; ++i)
+                for (int j = 0; j < D; ++j) {
+                    Ab[i * D + j] += Xa[(size_t)a * D + i] * ka[j];
+                    U[i * D + j] += Xw[(size_t)a * D + i] * ka[j];
+                }
+        }
+    }
+    double g = gamma[((size_t)b * F + f) * H + h];
+    for (int e = 0; e < D * D; ++e) M[e] = -Ab[e];
+    for (int i = 0; i < D; ++i) M[i * D + i] += g;
+    free(Ab); free(Kc); free(Bc); free(L); free(T); free(Ra); free(Rw); free(Xa); free(Xw);
+}
+
+/* (M_f, U_f) of the product reading for every (b, f, h): [B][H][F][D][D]. */
+void oracle_gdn_frame_transitions_product(const float *k, const float *v, const float *beta,
+                                          const float *gamma, int B, int H, int F, int N,
+                                          int D, double key_scale, int sub,
+                                          double *M_out, double *U_out)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bhf = 0; bhf < B * H * F; ++bhf) {
+        int b = bhf / (H * F), h = (bhf / F) % H, f = bhf % F;
+        size_t off = (size_t)bhf * D * D;
+        frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c, sub,
+                                 M_out + off, U_out + off);
+    }
+}
+
+/*
+ * Forward pass of the product reading: S_f = S_{f-1} M_f + U_f with the
+ * token-ordered (M_f, U_f) above, o = S_f q^ (output after the update, as in
+ * the sum form).
+ */
+void oracle_gdn_frame_fwd_product(const float *q, const float *k, const float *v,
+                                  const float *beta, const float *gamma, const float *S_in,
+                                  int B, int H, int F, int N, int D, double key_scale, int sub,
+                                  double *o, double *S_out)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        double *S = malloc(sizeof(double) * D * D);
+        double *Sn = malloc(sizeof(double) * D * D);
+        double *M = malloc(sizeof(double) * D * D);
+        double *U = malloc(sizeof(double) * D * D);
+        double *vec = malloc(sizeof(double) * D);
+        load_state(S_in, b, h, H, D, S);
+        for (int f = 0; f < F; ++f) {
+            frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c, sub, M, U);
+            matmul(S, M, Sn, D);
+            for (int e = 0; e < D * D; ++e) S[e] = Sn[e] + U[e];
+            if (o) frame_output(q, S, b, h, f, H, F, N, D, o, vec);
+        }
+        store_state(S_out, S, b, h, H, D);
+        free(S); free(Sn); free(M); free(U); free(vec);
+    }
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
