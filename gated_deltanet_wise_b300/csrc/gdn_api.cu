@@ -193,14 +193,37 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v, con
     return GDN_OK;
 }
 
-size_t gdn_frame_step_workspace_size(int B, int H, int N, int D) { return gdn_frame_fwd_workspace_size(B, H, 1, N, D); }
+size_t gdn_frame_step_workspace_size(int B, int H, int N, int D)
+{
+    if (B < 0 || H < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (B == 0 || H == 0 || N == 0) return 0;
+    if (D != 112) return (size_t)-1;
+    return 0;  // the fused step keeps its cross-CTA reduction on chip
+}
 
 gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                             const float *S_in, float *S_out, void *o, int B, int H, int N, int D, float key_scale,
-                            void *workspace, size_t workspace_bytes, gdn_stream_t stream)
+                            void * /*workspace*/, size_t /*workspace_bytes*/, gdn_stream_t stream)
 {
-    return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, workspace, workspace_bytes,
-                         stream);
+    if (B < 0 || H < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    if (!gamma || !aligned(gamma, 4)) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        if (!S_out) return GDN_OK;
+        return launch_decay_only(gamma, S_in, S_out, B, H, 1, D, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (!q || !k || !v || !o || !beta) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4))
+        return GDN_ERR_INVALID_ARG;
+    if ((long long)B * H > (1 << 20)) return GDN_ERR_UNSUPPORTED;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_frame_step_tc(q, k, v, beta, gamma, S_in, S_out, o, B, H, N,
+                                         default_key_scale(key_scale, D, N), status, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status_t gdn_frame_fwd_f32(const float *q, const float *k, const float *v, const float *beta,

@@ -2,6 +2,7 @@
 // (never installed, never seen by callers of include/gdn.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -19,6 +20,10 @@ cudaError_t launch_decay_only(const float *gamma, const float *S_in, float *S_ou
 // Address of the current device's status word (device memory), or nullptr.
 unsigned *device_status_word();
 
+// 4-D TMA view (D, H, N, B*F) of a bf16 [B][F*N][H][D] token tensor, 128-byte
+// swizzle, boxes of 64 head-dim elements x `rows` tokens (gdn_tc.cu).
+bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N, int rows);
+
 // tensor-core path (gdn_tc.cu); D == 112.
 struct TcPlan {
     int B, H, F, N;
@@ -32,5 +37,10 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
                                 const float *S_in, float *S_out, void *o, const TcPlan &plan, float c,
                                 void *workspace, unsigned *status, cudaStream_t stream,
                                 cudaEvent_t *events = nullptr);
+
+// fused single-frame step (gdn_step.cu); D == 112.
+cudaError_t launch_frame_step_tc(const void *q, const void *k, const void *v, const float *beta,
+                                 const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int N,
+                                 float c, unsigned *status, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,14 +1,16 @@
 // gdn_noalloc.cu — a streaming step that allocates nothing and needs no
 // caller-supplied scratch.
 //
-// gdn_frame_step needs a device workspace from its caller.  Some callers
+// The multi-frame kernels (gdn_frame_fwd) keep per-frame statistics and chunk
+// composites in a device workspace that their caller allocates.  Some callers
 // cannot call cudaMalloc (or any allocating routine) at the point where they
 // run a frame: a host that has handed the whole device memory budget to its
 // own pool and gives plug-ins only input/output pointers, a per-frame
 // real-time loop that must not take the allocator's locks or its latency, or
 // code running inside a stream capture in which allocation calls are
-// prohibited.  For them the step's scratch lives in the fixed array below,
-// which every GPU that loads this library holds until the process exits.
+// prohibited.  This entry runs one frame through those kernels with their
+// scratch in the fixed array below, which every GPU that loads this library
+// holds until the process exits.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -56,15 +58,17 @@ gdn_status_t gdn_frame_step_noalloc(const void *q, const void *k, const void *v,
                                     const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int N,
                                     int D, float key_scale, gdn_stream_t stream)
 {
-    const size_t need = gdn_frame_step_workspace_size(B, H, N, D);
+    // The frame runs through the multi-frame kernels with F = 1, whose
+    // frame statistics and chunk composites live in the scratch.
+    const size_t need = gdn_frame_fwd_workspace_size(B, H, 1, N, D);
     if (need == (size_t)-1) return D > 0 && D != 112 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
     if (need > gdn::kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
     if (need == 0)  // degenerate sizes use no scratch
-        return gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, nullptr, 0, stream);
+        return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, nullptr, 0, stream);
     void *scratch = gdn::scratch_address();
     if (!scratch) return GDN_ERR_CUDA;
-    return gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, scratch,
-                          gdn::kNoAllocScratchBytes, stream);
+    return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, scratch,
+                         gdn::kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"

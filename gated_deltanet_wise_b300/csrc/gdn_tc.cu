@@ -38,26 +38,11 @@
 #include <math.h>
 
 #include "gdn_internal.h"
-#include "gdn_ptx.cuh"
+#include "gdn_tile.cuh"
 
 namespace gdn {
 
 // ------------------------------------------------------------------ sizes
-constexpr int kD = 112;               // head size this path is built for
-constexpr int kSms = 148;             // B300 SM count: the chunk plan targets it
-constexpr float kEps = 1e-12f;        // ||x|| = sqrt(sum x^2 + eps)
-
-constexpr uint32_t kRowB = 128;                      // one swizzled row: 64 bf16
-constexpr uint32_t kAimgPanel = kD * kRowB;          // 14336: A_f image, 112 rows
-constexpr uint32_t kAimgBytes = 2 * kAimgPanel;      // 28672
-constexpr uint32_t kUStride = 116;                   // floats per U_f row (padded: conflict-free smem rows)
-constexpr uint32_t kUimgBytes = kD * kUStride * 4;   // 51968
-constexpr uint32_t kFrameWs = kAimgBytes + kUimgBytes;  // 80640 bytes per (chain, frame)
-constexpr uint32_t kImgPanel = 128 * kRowB;          // 16384: 128-row bf16 image panel
-constexpr uint32_t kImgBytes = 2 * kImgPanel;        // 32768
-constexpr uint32_t kStateFloats = kD * kD;           // 12544
-constexpr size_t kStateBytes = kStateFloats * 4;     // 50176
-
 // K1
 constexpr int kTS = 32;                               // tokens per stage
 constexpr uint32_t kTSPanel = kTS * kRowB;            // 4096: one 64-column panel of a stage
@@ -80,47 +65,7 @@ constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 179200
 constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 211968
 constexpr uint32_t kK2Smem = kK2OffBar + 256 + 1024;
 static_assert(kK2OffU + kUimgBytes <= kK2OffShi, "K2 smem layout");
-static_assert(kK1Smem <= 232448 && kK2Smem <= 232448, "shared memory budget");
-
-// instruction descriptors (M = 128, N = 112)
-constexpr uint32_t kIdescMN = idesc_bf16(128, kD, true, true);    // token-contraction GEMMs
-constexpr uint32_t kIdescK = idesc_bf16(128, kD, false, false);   // D-contraction GEMMs
-
-__device__ __forceinline__ void raise_status(unsigned *status)
-{
-    if (status) atomicOr(status, kStatusTimeout);
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float *f)
-{
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
-__device__ __forceinline__ uint4 f32x8_to_bf16(const float *f)
-{
-    uint4 u;
-    u.x = pack_bf16x2(f[0], f[1]);
-    u.y = pack_bf16x2(f[2], f[3]);
-    u.z = pack_bf16x2(f[4], f[5]);
-    u.w = pack_bf16x2(f[6], f[7]);
-    return u;
-}
-
-// hi = bf16(x), lo = bf16(x - hi) for 8 values.
-__device__ __forceinline__ void split_bf16x8(const float *x, uint4 &hi, uint4 &lo)
-{
-    float r[8];
-    hi = f32x8_to_bf16(x);
-    bf16x8_to_f32(hi, r);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = x[i] - r[i];
-    lo = f32x8_to_bf16(r);
-}
+static_assert(kK1Smem <= kMaxSmem && kK2Smem <= kMaxSmem, "shared memory budget");
 
 // ===================================================================== K1
 struct K1Params {
@@ -786,6 +731,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 // ================================================================= host side
 namespace {
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -799,6 +746,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     }
     return fn;
 }
+
+}  // namespace
 
 // 4-D view [B*F][N][H][D] of a bf16 [B][F*N][H][D] tensor, 128B swizzle,
 // boxes of 64 head-dim elements x `rows` tokens of one head of one frame.
@@ -814,10 +763,6 @@ bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-}  // namespace
 
 bool tc_plan(int B, int H, int F, int N, int /*num_sms*/, TcPlan *plan)
 {

@@ -95,11 +95,16 @@ gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v,
 
 /*
  * Streaming step: one latent frame (F = 1) per call, state carried by the
- * caller (chunk-causal / autoregressive generation; resume by passing the
- * previous call's S_out as S_in).  Same layouts with F = 1:
+ * caller (chunk-causal / autoregressive generation, the chunk-wise variant of
+ * the CSDN article's §六 stage 4; resume by passing the previous call's S_out
+ * as S_in).  Same layouts with F = 1:
  *   q, k, v, o : bf16 [B][N][H][D];  beta: fp32 [B][N][H];  gamma: fp32 [B][H]
- * Workspace: gdn_frame_step_workspace_size(B, H, N, D) bytes.
- * Output equals gdn_frame_fwd run frame by frame on the same S_in.
+ * One launch: a thread-block cluster per (b, h) chain splits the frame's
+ * tokens across its CTAs and sums their partial statistics on chip, so the
+ * step needs no scratch: gdn_frame_step_workspace_size() returns 0 for every
+ * size this build supports (D == 112) and `workspace` may be NULL.  S_out may
+ * alias S_in.  Output equals gdn_frame_fwd run frame by frame on the same
+ * S_in, within the tolerance stated there.
  */
 size_t gdn_frame_step_workspace_size(int B, int H, int N, int D);
 gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v,
@@ -164,10 +169,12 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,
  * frame.  Examples: a host that owns the whole device memory budget and hands
  * plug-ins only input and output pointers; a per-frame real-time loop that
  * must not take the allocator's locks or latency; code inside a stream capture
- * in which allocation calls are prohibited.  The step's scratch is a fixed
- * 16 MiB device array inside the library (gdn_frame_step_noalloc_limit_bytes()).
- * Every GPU that loads the library holds it until the process exits.
- *   - Limit: gdn_frame_step_workspace_size(B, H, N, D) must not exceed the
+ * in which allocation calls are prohibited.  It runs the frame through the
+ * multi-frame kernels of gdn_frame_fwd with F = 1, whose per-frame statistics
+ * and chunk composites need scratch; that scratch is a fixed 16 MiB device
+ * array inside the library (gdn_frame_step_noalloc_limit_bytes()).  Every GPU
+ * that loads the library holds it until the process exits.
+ *   - Limit: gdn_frame_fwd_workspace_size(B, H, 1, N, D) must not exceed the
  *     array (about 226 KiB per chain at D = 112, so B*H <= 72).  Larger
  *     requests return GDN_ERR_WORKSPACE before anything is enqueued.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.

@@ -50,7 +50,8 @@ def test_workspace_sizes(L):
     assert gdn.gdn_frame_fwd_workspace_size(1, 20, 4, 0, 112) == 0
     assert gdn.gdn_frame_fwd_workspace_size(-1, 20, 4, 8, 112) == SZ_ERR
     assert gdn.gdn_frame_fwd_workspace_size(1, 1, 4, 8, 64) == SZ_ERR   # bf16 path is D = 112
-    assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 112) == gdn.gdn_frame_fwd_workspace_size(1, 20, 1, 880, 112)
+    assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 112) == 0   # the fused step needs no scratch
+    assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 64) == 2 ** 64 - 1
     # the workspace grows linearly in frames (per-frame images dominate)
     a = gdn.gdn_frame_fwd_workspace_size(1, 4, 10, 880, 112)
     b = gdn.gdn_frame_fwd_workspace_size(1, 4, 20, 880, 112)
@@ -79,6 +80,19 @@ def test_host_side_validation_without_gpu(L):
     need = gdn.gdn_frame_fwd_workspace_size(1, 1, 2, 8, 112)
     assert fwd(1, 1, 2, 8, 112, ws=fake, nbytes=need - 16) == gdn.GDN_ERR_WORKSPACE
     assert fwd(1, 1, 2, 8, 112, ws=P(0x10008), nbytes=need) == gdn.GDN_ERR_INVALID_ARG
+    def step(B, H, N, D, **over):
+        a = dict(args, **over)
+        return L.gdn_frame_step(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"],
+                                B, H, N, D, 0.0, None, 0, None)
+
+    assert step(1, 1, 8, -3) == gdn.GDN_ERR_INVALID_ARG
+    assert step(1, -1, 8, 112) == gdn.GDN_ERR_INVALID_ARG
+    assert step(0, 20, 880, 112) == gdn.GDN_OK           # empty batch: no-op
+    assert step(1, 1, 8, 128) == gdn.GDN_ERR_UNSUPPORTED
+    assert step(1, 1, 8, 112, v=None) == gdn.GDN_ERR_INVALID_ARG
+    assert step(1, 1, 8, 112, gamma=None) == gdn.GDN_ERR_INVALID_ARG
+    assert step(1, 1, 8, 112, o=P(0x10002)) == gdn.GDN_ERR_INVALID_ARG   # misaligned
+    assert step(1, 1, 8, 112, S_in=P(0x10004)) == gdn.GDN_ERR_INVALID_ARG
     f32 = L.gdn_frame_fwd_f32
     assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, 1, 1, 1, 129, 0.0, None) == gdn.GDN_ERR_UNSUPPORTED
     assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, -1, 1, 1, 16, 0.0, None) == gdn.GDN_ERR_INVALID_ARG

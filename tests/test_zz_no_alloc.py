@@ -36,7 +36,7 @@ def _step_inputs(seed, B, H, N):
 
 def test_noalloc_step_matches_workspace_step_on_two_calls():
     B, H, N, D = 1, 20, 880, 112
-    assert gdn.gdn_frame_step_workspace_size(B, H, N, D) <= gdn.gdn_frame_step_noalloc_limit_bytes()
+    assert gdn.gdn_frame_fwd_workspace_size(B, H, 1, N, D) <= gdn.gdn_frame_step_noalloc_limit_bytes()
     for call, seed in enumerate((21, 22)):
         q, k, v, beta, gamma, S0 = _step_inputs(seed, B, H, N)
         o_ref, S_ref = gdn.frame_step(q, k, v, beta, gamma, S0)
@@ -53,7 +53,7 @@ def test_noalloc_step_matches_workspace_step_on_two_calls():
 def test_noalloc_step_rejects_requests_beyond_its_scratch():
     limit = gdn.gdn_frame_step_noalloc_limit_bytes()
     B, H = 4, 40   # 160 chains: beyond the fixed scratch
-    assert gdn.gdn_frame_step_workspace_size(B, H, 880, 112) > limit
+    assert gdn.gdn_frame_fwd_workspace_size(B, H, 1, 880, 112) > limit
     fake = torch.empty(16, dtype=torch.uint8, device="cuda")   # never touched: rejected on the host
     st = gdn.gdn_frame_step_noalloc(fake, fake, fake, fake, fake, None, fake, fake, B, H, 880, 112, 0.0)
     assert st == gdn.GDN_ERR_WORKSPACE
