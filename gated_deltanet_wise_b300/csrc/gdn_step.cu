@@ -12,24 +12,28 @@
 // in the frame's statistics, S_out = gamma S_in + sum_r (U_r - S_in A_r) over
 // the CTAs' partials (A_r, U_r), so each CTA applies its own partial and only
 // one D x D matrix per CTA crosses the cluster:
-//   1. S_in is loaded once as bf16 hi + lo MMA images while the first K/V
-//      tiles are in flight;
-//   2. each CTA streams its token slice through shared memory (TMA, 64-token
-//      stages), turns keys into the MMA operands k^ and beta c/r k (bf16 hi +
-//      lo) and accumulates A_r and U_r with tcgen05 into TMEM;
-//   3. A_r becomes a bf16 image, tcgen05 forms S_in A_r, and the CTA pushes
-//      its delta U_r - S_in A_r, row block by row block, into the shared memory
-//      of the CTA that owns those rows (distributed shared memory stores).  The
-//      receive buffers overlay the stage rings, so the pushes wait at a cluster
+//   1. each CTA streams its token slice through shared memory (TMA, a ring of
+//      three 64-token stages, all issued up front for slices of <= 192
+//      tokens), turns keys into the MMA operands k^ and beta c/r k (bf16 hi +
+//      lo) and accumulates A_r and U_r with tcgen05 into TMEM; S_in is loaded
+//      into registers meanwhile;
+//   2. S_in becomes bf16 hi/lo MMA images, A_r a bf16 image, and tcgen05 forms
+//      S_in A_r; the delta U_r - S_in A_r goes to a shared-memory staging
+//      matrix;
+//   3. each row block of the delta is sent with a bulk copy (the TMA engine,
+//      shared::cta -> shared::cluster) to the CTA that owns those rows of
+//      S_out; the copies complete on the owner's mbarrier.  The receive
+//      buffers overlay the stage rings, so the copies start after a cluster
 //      barrier that every CTA passes once its own ring is drained;
-//   4. after a cluster barrier each owner sums the deltas of its rows, adds
-//      gamma S_in, writes those rows of S_out to global memory and broadcasts
-//      them as bf16 hi/lo image rows into every CTA of the cluster;
-//   5. after a second cluster barrier every CTA computes O = Q (S_hi + S_lo)^T
-//      for its 128-token tiles of Q, scales rows by 1/||q|| and stores bf16
-//      with TMA.
+//   4. each owner sums the deltas of its rows, adds gamma S_in, writes those
+//      rows of S_out to global memory and bulk-copies them, as bf16 hi/lo
+//      image rows, into every CTA of the cluster;
+//   5. every CTA computes O = Q (S_hi + S_lo)^T for its 128-token tiles of Q,
+//      scales rows by 1/||q|| and stores bf16 with TMA.
 // The kernel needs no global scratch.  Every CTA reads S_in before the first
-// cluster barrier and S_out is written after it, so S_out may alias S_in.
+// cluster barrier and S_out is written after it, so S_out may alias S_in.  A
+// last cluster barrier keeps every CTA resident until no copy can still be
+// headed into its shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -45,24 +49,32 @@ constexpr int kSTS = 64;                                   // tokens per stats s
 constexpr uint32_t kSPanel = kSTS * kRowB;                 // 8192: one 64-column panel of a stage
 constexpr uint32_t kSStageBytes = 8 * kSPanel;             // K -> K^, V, B_hi, B_lo (2 panels each)
 constexpr uint32_t kSOffK = 0, kSOffV = 2 * kSPanel, kSOffBhi = 4 * kSPanel, kSOffBlo = 6 * kSPanel;
-constexpr int kSStages = 2;
+constexpr int kSStages = 3;
 constexpr int kSThreads = 320;                             // producer, MMA, 8 math warps
 constexpr int kTQ = 128;                                   // tokens per Q/O tile
 constexpr int kMaxCluster = 8;                             // portable cluster size limit
-// After the stats phase the stage ring [0, 128 KB) is reused for:
-constexpr uint32_t kSOffRecv = 0;                          // fp32 deltas for the owned rows, one block per source CTA
+// Shared memory.  During the stats phase: stages 0 and 1 at [0, 128 KB),
+// the Q tile at [128, 160 KB), stage 2 at [160, 224 KB).  Afterwards the
+// first 128 KB hold the receive buffer, the A_r image, the delta staging
+// matrix (over the image once it is consumed) and the |q|^2 partial sums,
+// and [160, 224 KB) holds the S images (S_in, then S_out).
+constexpr uint32_t kSOffQ = 131072;                        // Q tile of even tiles, O written over it
+constexpr uint32_t kSOffQ2 = 0;                            // Q tile of odd tiles (over the consumed receive buffer)
+constexpr uint32_t kSOffShi = 163840, kSOffSlo = 196608;   // 128-row bf16 images of S (hi, lo)
+constexpr uint32_t kSOffRecv = 0;                          // fp32 delta rows: one block per source CTA
 constexpr uint32_t kRecvBytes = (kD + kMaxCluster - 1) * kD * 4;  // >= cl * ceil(112 / cl) rows
-constexpr uint32_t kSOffAimg = 55296;                      // bf16 K-major image of A_r (112 rows)
-constexpr uint32_t kSOffQ = kSStages * kSStageBytes;       // 131072: Q tile, O written over it
-constexpr uint32_t kSOffShi = kSOffQ + kImgBytes;          // 128-row bf16 images of S (hi, lo)
-constexpr uint32_t kSOffSlo = kSOffShi + kImgBytes;
-constexpr uint32_t kSOffBar = kSOffSlo + kImgBytes;        // 229376
-constexpr uint32_t kSOffQss = 86016;                       // |q|^2 partial sums [2 buffers][2 groups][128]
+constexpr uint32_t kSOffAimg = 54272;                      // bf16 K-major image of A_r (112 rows)
+constexpr uint32_t kSOffDelta = kSOffAimg;                 // fp32 [112][112] delta staging
+constexpr uint32_t kSOffQss = kSOffDelta + (uint32_t)kStateBytes;  // [2 buffers][2 groups][128] |q|^2 parts
+constexpr uint32_t kSOffBar = 229376;
 constexpr uint32_t kSSmem = kSOffBar + 256 + 1024;
 static_assert(kSOffRecv + kRecvBytes <= kSOffAimg, "step smem layout");
-static_assert(kSOffAimg + kAimgBytes <= kSOffQss && kSOffQss + 2048 <= kSOffQ, "step smem layout");
+static_assert(kSOffQss + 2048 <= 2 * kSStageBytes, "step smem layout");
+static_assert(kSOffShi == kSOffQ + kImgBytes && kSOffSlo + kImgBytes == kSOffBar, "step smem layout");
 static_assert(kSSmem <= kMaxSmem, "step shared memory budget");
 static_assert(kSOffAimg % 1024 == 0 && kSOffQ % 1024 == 0 && kSOffShi % 1024 == 0, "swizzle alignment");
+
+__device__ __forceinline__ uint32_t stage_off(int s) { return s < 2 ? (uint32_t)s * kSStageBytes : kSOffShi; }
 
 // Tensor memory (512 columns): A_r, U_r, S_in A_r, O accumulators, 128 columns each.
 constexpr uint32_t kTmA = 0, kTmU = 128, kTmS = 256, kTmO = 384;
@@ -83,25 +95,16 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v)
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned ends) from this CTA's
+// shared memory into a cluster peer's; completes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                 uint32_t mbar_cluster)
 {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_dsmem_u4(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
-// Generic-proxy writes into any CTA's shared memory -> visible to the async
-// proxy (the MMA that reads the broadcast S_out images).
-__device__ __forceinline__ void fence_proxy_async_cluster()
-{
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
 }
 
 // Cluster-wide barrier, split in two so that a thread may arrive early and
@@ -110,19 +113,23 @@ __device__ __forceinline__ void fence_proxy_async_cluster()
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next grid on the stream be scheduled,
+// and wait until the previous grid has completed with its writes visible.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over the 8 math warps (ids 1.., 0 is __syncthreads).
 __device__ __forceinline__ void math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // fp32 [rows][112] staging matrices in shared memory: float4 c4 of row `row`
 // sits at position c4 ^ ((row >> 1) & 3) of the row, so that eight consecutive
 // rows (one shared-memory wavefront of float4 accesses) hit eight different
-// 16-byte bank groups although a row is 448 bytes long.
-__device__ __forceinline__ int f4_off(int row, int c4) { return row * kD + ((c4 ^ ((row >> 1) & 3)) << 2); }
-
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
+// 16-byte bank groups although a row is 448 bytes long.  Rows stay
+// contiguous, so row blocks can be bulk-copied as they are.
+__device__ __forceinline__ int f4_pos(int row, int c4) { return (c4 ^ ((row >> 1) & 3)) << 2; }
 
 struct StepParams {
     const float *beta;   // [B][N][H]
@@ -144,12 +151,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSOffBar);
-    uint64_t *st_full = bars + 0, *st_prep = bars + 2, *st_empty = bars + 4;
-    uint64_t *q_full = bars + 6, *q_empty = bars + 7, *stats_done = bars + 8, *simg_ready = bars + 9;
-    uint64_t *aimg_ready = bars + 10, *s_done = bars + 11, *o_full = bars + 12, *o_free = bars + 13;
-    uint64_t *drain = bars + 14;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+    uint64_t *st_full = bars + 0, *st_prep = bars + 3, *st_empty = bars + 6;
+    uint64_t *q_full = bars + 9, *q_empty = bars + 11, *stats_done = bars + 13, *simg_ready = bars + 14;
+    uint64_t *aimg_ready = bars + 15, *s_done = bars + 16, *o_full = bars + 17, *o_free = bars + 19;
+    uint64_t *recv_full = bars + 21, *sout_full = bars + 22, *drain = bars + 23, *recv_free = bars + 24;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 25);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 26);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -169,34 +176,39 @@ __global__ void __launch_bounds__(kSThreads, 1)
             mbar_init(&st_prep[i], 8);
             mbar_init(&st_empty[i], 1);
         }
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 8);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 8);
+        }
         mbar_init(stats_done, 1);
         mbar_init(simg_ready, 8);
         mbar_init(aimg_ready, 8);
         mbar_init(s_done, 1);
-        mbar_init(o_full, 1);
-        mbar_init(o_free, 8);
+        mbar_init(recv_full, 1);
+        mbar_init(sout_full, 9);
         mbar_init(drain, 1);
+        mbar_init(recv_free, 8);
         *abort_flag = 0;
         fence_mbar_init();
+        // bytes this CTA will receive: its rows of every peer's delta, and
+        // every other owner's S_out image rows (hi and lo, two panels each)
+        mbar_arrive_expect_tx(recv_full, (uint32_t)(p.cl * (r1 - r0) * kD * 4));
+        mbar_arrive_expect_tx(sout_full, (uint32_t)((kD - (r1 - r0)) * kRowB * 4));
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    // rows 112..127 of the S images are never written again: zero them
-    for (int e = threadIdx.x; e < 2 * 2 * 16 * 8; e += kSThreads) {
-        const int img = e >> 8, pan = (e >> 7) & 1, rr = 112 + ((e >> 3) & 15), ch = e & 7;
-        *reinterpret_cast<uint4 *>(sm + (img ? kSOffSlo : kSOffShi) + pan * kImgPanel + rr * kRowB + ch * 16) =
-            make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
+    // The next step on the stream may start (its stats phase reads only its own
+    // inputs); it waits for this grid before it touches the state or outputs.
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -205,9 +217,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
             for (int st = 0; st < n_st; ++st) {
-                const int s = st & 1, use = st >> 1;
-                if (st >= 2 && !(ok = mbar_wait(&st_empty[s], (use - 1) & 1, abort_flag))) break;
-                uint8_t *stg = sm + s * kSStageBytes;
+                const int s = st % kSStages, use = st / kSStages;
+                if (st == kSStages && my_tiles > 0) {  // the first Q tile, behind the first ring of K/V
+                    mbar_arrive_expect_tx(&q_full[0], kImgBytes);
+                    tma_load_4d(sm + kSOffQ, &mapQ, &q_full[0], 0, h, (int)rank * kTQ, b, pol);
+                    tma_load_4d(sm + kSOffQ + kImgPanel, &mapQ, &q_full[0], 64, h, (int)rank * kTQ, b, pol);
+                    ++q_issued;
+                }
+                if (st >= kSStages && !(ok = mbar_wait(&st_empty[s], (use - 1) & 1, abort_flag))) break;
+                uint8_t *stg = sm + stage_off(s);
                 const int row = tok0 + st * kSTS;
                 mbar_arrive_expect_tx(&st_full[s], 4 * kSPanel);
                 tma_load_4d(stg + kSOffK, &mapK, &st_full[s], 0, h, row, b, pol);
@@ -215,44 +233,42 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 tma_load_4d(stg + kSOffV, &mapV, &st_full[s], 0, h, row, b, pol);
                 tma_load_4d(stg + kSOffV + kSPanel, &mapV, &st_full[s], 64, h, row, b, pol);
                 ++st_issued;
-                if (st == 1 && my_tiles > 0) {  // the first Q tile, behind the first two K/V stages
-                    const int t = (int)rank;
-                    mbar_arrive_expect_tx(q_full, kImgBytes);
-                    tma_load_4d(sm + kSOffQ, &mapQ, q_full, 0, h, t * kTQ, b, pol);
-                    tma_load_4d(sm + kSOffQ + kImgPanel, &mapQ, q_full, 64, h, t * kTQ, b, pol);
-                    ++q_issued;
-                }
             }
             if (ok && !q_issued && my_tiles > 0) {
-                const int t = (int)rank;
-                mbar_arrive_expect_tx(q_full, kImgBytes);
-                tma_load_4d(sm + kSOffQ, &mapQ, q_full, 0, h, t * kTQ, b, pol);
-                tma_load_4d(sm + kSOffQ + kImgPanel, &mapQ, q_full, 64, h, t * kTQ, b, pol);
+                mbar_arrive_expect_tx(&q_full[0], kImgBytes);
+                tma_load_4d(sm + kSOffQ, &mapQ, &q_full[0], 0, h, (int)rank * kTQ, b, pol);
+                tma_load_4d(sm + kSOffQ + kImgPanel, &mapQ, &q_full[0], 64, h, (int)rank * kTQ, b, pol);
                 ++q_issued;
             }
         }
         __syncwarp();
         cluster_arrive();  // B0
         cluster_wait();
-        cluster_arrive();  // B1
-        cluster_wait();
-        cluster_arrive();  // B2
-        cluster_wait();
         if (lane == 0) {
+            // odd tiles go to the second Q buffer, over the receive buffer once the
+            // deltas in it are summed; later tiles wait for their buffer's epilogue
             for (int i = 1; ok && i < my_tiles; ++i) {
-                const int t = (int)rank + i * p.cl;
-                if (!(ok = mbar_wait(q_empty, (i - 1) & 1, abort_flag))) break;
-                mbar_arrive_expect_tx(q_full, kImgBytes);
-                tma_load_4d(sm + kSOffQ, &mapQ, q_full, 0, h, t * kTQ, b, pol);
-                tma_load_4d(sm + kSOffQ + kImgPanel, &mapQ, q_full, 64, h, t * kTQ, b, pol);
+                const int t = (int)rank + i * p.cl, qb = i & 1;
+                if (i == 1) ok = mbar_wait(recv_free, 0, abort_flag);
+                else ok = mbar_wait(&q_empty[qb], ((i >> 1) - 1) & 1, abort_flag);
+                if (!ok) break;
+                uint8_t *dst = sm + (qb ? kSOffQ2 : kSOffQ);
+                mbar_arrive_expect_tx(&q_full[qb], kImgBytes);
+                tma_load_4d(dst, &mapQ, &q_full[qb], 0, h, t * kTQ, b, pol);
+                tma_load_4d(dst + kImgPanel, &mapQ, &q_full[qb], 64, h, t * kTQ, b, pol);
                 ++q_issued;
             }
             if (*abort_flag) {  // let copies already in flight land before the CTA exits
                 for (int s = 0; s < kSStages && s < st_issued; ++s) {
                     const int last = ((st_issued - 1 - s) / kSStages) * kSStages + s;  // last stage index using s
-                    mbar_wait_drain(&st_full[s], (last >> 1) & 1);
+                    mbar_wait_drain(&st_full[s], (last / kSStages) & 1);
                 }
-                if (q_issued) mbar_wait_drain(q_full, (q_issued - 1) & 1);
+                for (int qb = 0; qb < 2 && qb < q_issued; ++qb) {  // last tile index using buffer qb
+                    const int last = ((q_issued - 1 - qb) / 2) * 2 + qb;
+                    mbar_wait_drain(&q_full[qb], (last >> 1) & 1);
+                }
+                mbar_wait_drain(recv_full, 0);
+                mbar_wait_drain(sout_full, 0);
             }
         }
         __syncwarp();
@@ -261,10 +277,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         bool ok = true;
         if (lane == 0) {
             for (int st = 0; st < n_st; ++st) {
-                const int s = st & 1, use = st >> 1;
+                const int s = st % kSStages, use = st / kSStages;
                 if (!(ok = mbar_wait(&st_prep[s], use & 1, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t stg = sbase + s * kSStageBytes;
+                const uint32_t stg = sbase + stage_off(s);
 #pragma unroll
                 for (int ks = 0; ks < kSTS / 16; ++ks) {
                     const uint32_t o = ks * 2048;
@@ -296,24 +312,27 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
         cluster_arrive();  // B0
         cluster_wait();
-        cluster_arrive();  // B1
-        cluster_wait();
-        cluster_arrive();  // B2: the S_out images are complete in every CTA
-        cluster_wait();
         if (lane == 0) {
-            fence_proxy_async_smem();
+            // every row of the S_out images is in place: this CTA's own (generic
+            // stores, fenced by their writers) and the other owners' (bulk copies)
+            if (ok) ok = mbar_wait(sout_full, 0, abort_flag);
+            tc_fence_after();
+            // tiles alternate between two Q buffers and two accumulators (the
+            // second over A_r's consumed columns)
             for (int i = 0; ok && i < my_tiles; ++i) {
-                if (!(ok = mbar_wait(q_full, i & 1, abort_flag))) break;
-                if (i >= 1 && !(ok = mbar_wait(o_free, (i - 1) & 1, abort_flag))) break;
+                const int qb = i & 1, use = i >> 1;
+                if (!(ok = mbar_wait(&q_full[qb], use & 1, abort_flag))) break;
+                if (i >= 2 && !(ok = mbar_wait(&o_free[qb], (use - 1) & 1, abort_flag))) break;
                 tc_fence_after();
+                const uint32_t qa = sbase + (qb ? kSOffQ2 : kSOffQ), acc = tmem + (qb ? kTmA : kTmO);
 #pragma unroll
                 for (int ks = 0; ks < 7; ++ks) {
                     const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(sbase + kSOffQ + koff, 16, 1024);
-                    mma_bf16(tmem + kTmO, ad, sdesc_sw128(sbase + kSOffShi + koff, 16, 1024), kIdescK, ks > 0);
-                    mma_bf16(tmem + kTmO, ad, sdesc_sw128(sbase + kSOffSlo + koff, 16, 1024), kIdescK, 1u);
+                    const uint64_t ad = sdesc_sw128(qa + koff, 16, 1024);
+                    mma_bf16(acc, ad, sdesc_sw128(sbase + kSOffShi + koff, 16, 1024), kIdescK, ks > 0);
+                    mma_bf16(acc, ad, sdesc_sw128(sbase + kSOffSlo + koff, 16, 1024), kIdescK, 1u);
                 }
-                mma_commit(o_full);
+                mma_commit(&o_full[qb]);
             }
             mma_commit(drain);  // every MMA issued above has completed once this phase lands
             mbar_wait_drain(drain, 0);
@@ -326,50 +345,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int cc0 = g == 0 ? 0 : 4, cc1 = g == 0 ? 4 : 7;  // 16-column groups: panel 0 or panel 1
+        const float *sin = p.S_in ? p.S_in + (size_t)bh * kStateFloats : nullptr;
         bool ok = true;
 
-        // 1. S_in as hi/lo bf16 images (the first K/V tiles are in flight meanwhile)
-        {
-            constexpr int kIt = (kD * 14 + 255) / 256;
-            const float *sin = p.S_in ? p.S_in + (size_t)bh * kStateFloats : nullptr;
-            float4 x0[kIt], x1[kIt];
-#pragma unroll
-            for (int it = 0; it < kIt; ++it) {
-                const int e = t + it * 256, rr = e / 14, c8 = e % 14;
-                x0[it] = x1[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (sin && e < kD * 14) {
-                    x0[it] = __ldg(reinterpret_cast<const float4 *>(sin + rr * kD + c8 * 8));
-                    x1[it] = __ldg(reinterpret_cast<const float4 *>(sin + rr * kD + c8 * 8 + 4));
-                }
-            }
-#pragma unroll
-            for (int it = 0; it < kIt; ++it) {
-                const int e = t + it * 256, rr = e / 14, c8 = e % 14;
-                if (e >= kD * 14) break;
-                const float x[8] = {x0[it].x, x0[it].y, x0[it].z, x0[it].w, x1[it].x, x1[it].y, x1[it].z, x1[it].w};
-                uint4 hi, lo;
-                split_bf16x8(x, hi, lo);
-                const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(rr, c8 & 7);
-                *reinterpret_cast<uint4 *>(sm + kSOffShi + off) = hi;
-                *reinterpret_cast<uint4 *>(sm + kSOffSlo + off) = lo;
-            }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(simg_ready);
-
-        // 2. prep: four threads per token, each a quarter of the token's 128
+        // 1. prep: four threads per token, each a quarter of the token's 128
         //    swizzled columns (panel qq>>1, chunks rotated to spread banks).
         //    Rows past this CTA's slice get beta = 0 and contribute nothing.
         {
             const int r = t >> 2, qq = t & 3;
             const uint32_t prep_off = (qq >> 1) * kSPanel + r * kRowB;
             for (int st = 0; st < n_st; ++st) {
-                const int s = st & 1, use = st >> 1;
+                const int s = st % kSStages, use = st / kSStages;
                 const int n = tok0 + st * kSTS + r;
                 const float bt = n < tok1 ? __ldg(p.beta + ((size_t)b * p.N + n) * p.H + h) : 0.f;
                 if (!(ok = mbar_wait_warp(&st_full[s], use & 1, abort_flag))) break;
-                uint8_t *stg = sm + s * kSStageBytes + prep_off;
+                uint8_t *stg = sm + stage_off(s) + prep_off;
                 float kf[32];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -404,12 +394,45 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
         }
 
-        // 3. A_r -> bf16 image (over the drained stage ring); the MMA forms S_in A_r
+        // 2b. the previous grid on the stream (e.g. the previous step, whose
+        //     S_out is this S_in) must be complete before the state is read or
+        //     any output written; then S_in goes into registers for its images
+        griddep_wait();
+        constexpr int kIt = (kD * 14 + 255) / 256;
+        float4 x0[kIt], x1[kIt];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = t + it * 256, rr = e / 14, c8 = e % 14;
+            x0[it] = x1[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sin && e < kD * 14) {
+                x0[it] = __ldg(reinterpret_cast<const float4 *>(sin + rr * kD + c8 * 8));
+                x1[it] = __ldg(reinterpret_cast<const float4 *>(sin + rr * kD + c8 * 8 + 4));
+            }
+        }
+
+        // 3. the ring is drained: S_in images over stage 2, A_r image over stage 0
         if (ok) ok = mbar_wait_warp(stats_done, 0, abort_flag);
         tc_fence_after();
-        // B0: this CTA's stage ring is drained, so the other CTAs may push into
-        // its receive buffer (which overlays the ring) once every CTA arrived
-        cluster_arrive();
+        cluster_arrive();  // B0: peers may copy into this CTA's receive buffer once all arrived
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = t + it * 256, rr = e / 14, c8 = e % 14;
+            if (e >= kD * 14) break;
+            const float x[8] = {x0[it].x, x0[it].y, x0[it].z, x0[it].w, x1[it].x, x1[it].y, x1[it].z, x1[it].w};
+            uint4 hi, lo;
+            split_bf16x8(x, hi, lo);
+            const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(rr, c8 & 7);
+            *reinterpret_cast<uint4 *>(sm + kSOffShi + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + kSOffSlo + off) = lo;
+        }
+        for (int e = t; e < 2 * 2 * 16 * 8; e += 256) {  // rows 112..127 of the S images: zero
+            const int img = e >> 8, pan = (e >> 7) & 1, rr = 112 + ((e >> 3) & 15), ch = e & 7;
+            *reinterpret_cast<uint4 *>(sm + (img ? kSOffSlo : kSOffShi) + pan * kImgPanel + rr * kRowB + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(simg_ready);
         if (ok && n_st > 0) {
             for (int cc = cc0; cc < cc1; ++cc) {
                 uint32_t ra[16];
@@ -430,19 +453,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(aimg_ready);
 
-        // 4. delta_r = U_r - S_in A_r, pushed row by row to the owning CTA's
-        //    receive buffer (block `rank` of the owner's rows)
+        // 4. delta_r = U_r - S_in A_r into the staging matrix (over the consumed
+        //    A_r image), then one bulk copy per owner of its row block
         if (ok && n_st > 0) ok = mbar_wait_warp(s_done, 0, abort_flag);
         tc_fence_after();
-        cluster_wait();  // B0
         {
-            // TMEM loads are warp-collective: every lane loads, rows >= 112 store nothing
-            const int owner = min(row, kD - 1) / rows_per, lr = min(row, kD - 1) - owner * rows_per;
-            const uint32_t base = dsmem_addr(sbase + kSOffRecv, owner);
-            const int rr = (int)rank * rows_per + lr;
+            float *dl = reinterpret_cast<float *>(sm + kSOffDelta);
             for (int cc = cc0; cc < cc1; ++cc) {
                 uint32_t ru[16], rs[16];
-                if (ok && n_st > 0) {
+                if (ok && n_st > 0) {  // TMEM loads are warp-collective: all lanes load
                     tmem_ld16(tmem + lane_off + kTmU + cc * 16, ru);
                     tmem_ld16(tmem + lane_off + kTmS + cc * 16, rs);
                     tmem_ld_wait();
@@ -453,22 +472,32 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 if (row < kD) {
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
-                        st_dsmem_f4(base + 4u * (uint32_t)f4_off(rr, cc * 4 + j / 4),
-                                    make_float4(__uint_as_float(ru[j]) - __uint_as_float(rs[j]),
-                                                __uint_as_float(ru[j + 1]) - __uint_as_float(rs[j + 1]),
-                                                __uint_as_float(ru[j + 2]) - __uint_as_float(rs[j + 2]),
-                                                __uint_as_float(ru[j + 3]) - __uint_as_float(rs[j + 3])));
+                        *reinterpret_cast<float4 *>(dl + row * kD + f4_pos(row, cc * 4 + j / 4)) =
+                            make_float4(__uint_as_float(ru[j]) - __uint_as_float(rs[j]),
+                                        __uint_as_float(ru[j + 1]) - __uint_as_float(rs[j + 1]),
+                                        __uint_as_float(ru[j + 2]) - __uint_as_float(rs[j + 2]),
+                                        __uint_as_float(ru[j + 3]) - __uint_as_float(rs[j + 3]));
                 }
             }
         }
-        cluster_arrive();  // B1: every delta is in its owner's shared memory
-        cluster_wait();
+        fence_proxy_async_smem();  // the bulk copies read the staging through the async proxy
+        math_sync();
+        cluster_wait();  // B0
+        if (t == 0) {
+            for (int q = 0; q < p.cl; ++q) {
+                const int q0 = min(kD, q * rows_per), q1 = min(kD, q0 + rows_per);
+                if (q1 <= q0) continue;
+                bulk_s2s_cluster(dsmem_addr(sbase + kSOffRecv + (uint32_t)((int)rank * rows_per * kD * 4), q),
+                                 sbase + kSOffDelta + (uint32_t)(q0 * kD * 4), (uint32_t)((q1 - q0) * kD * 4),
+                                 dsmem_addr(smem_u32(recv_full), q));
+            }
+        }
 
-        // 5. owned rows: S_out = gamma S_in + sum of the deltas; to global memory,
-        //    and as hi/lo image rows into every CTA of the cluster
+        // 5. owned rows: S_out = gamma S_in + the peers' deltas; to global memory,
+        //    and as hi/lo image rows into this CTA and, by bulk copies, the others
+        if (ok) ok = mbar_wait_warp(recv_full, 0, abort_flag);
         {
             const float gam = __ldg(p.gamma + (size_t)b * p.H + h);
-            const float *sin = p.S_in ? p.S_in + (size_t)bh * kStateFloats : nullptr;
             float *sout = p.S_out ? p.S_out + (size_t)bh * kStateFloats : nullptr;
             const float *recv = reinterpret_cast<const float *>(sm + kSOffRecv);
             const int n8 = (r1 - r0) * 14;
@@ -482,9 +511,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 float x[8] = {gam * a0.x, gam * a0.y, gam * a0.z, gam * a0.w,
                               gam * a1.x, gam * a1.y, gam * a1.z, gam * a1.w};
                 for (int src = 0; src < p.cl; ++src) {
-                    const int rr = src * rows_per + lr;
-                    const float4 d0 = *reinterpret_cast<const float4 *>(recv + f4_off(rr, 2 * c8));
-                    const float4 d1 = *reinterpret_cast<const float4 *>(recv + f4_off(rr, 2 * c8 + 1));
+                    const float *rrow = recv + (src * rows_per + lr) * kD;
+                    const float4 d0 = *reinterpret_cast<const float4 *>(rrow + f4_pos(rw, 2 * c8));
+                    const float4 d1 = *reinterpret_cast<const float4 *>(rrow + f4_pos(rw, 2 * c8 + 1));
                     x[0] += d0.x;
                     x[1] += d0.y;
                     x[2] += d0.z;
@@ -501,26 +530,41 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 uint4 hi, lo;
                 split_bf16x8(x, hi, lo);
                 const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(rw, c8 & 7);
-                for (int q = 0; q < p.cl; ++q) {
-                    st_dsmem_u4(dsmem_addr(sbase + kSOffShi + off, q), hi);
-                    st_dsmem_u4(dsmem_addr(sbase + kSOffSlo + off, q), lo);
+                *reinterpret_cast<uint4 *>(sm + kSOffShi + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + kSOffSlo + off) = lo;
+            }
+        }
+        fence_proxy_async_smem();
+        math_sync();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(sout_full);  // this CTA's own rows are in place
+            mbar_arrive(recv_free);  // the receive buffer may take the second Q tile
+        }
+        if (t == 0 && r1 > r0) {
+            const uint32_t bytes = (uint32_t)(r1 - r0) * kRowB;
+            for (int q = 0; q < p.cl; ++q) {
+                if (q == (int)rank) continue;
+                const uint32_t mb = dsmem_addr(smem_u32(sout_full), q);
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    const uint32_t off =
+                        (part >> 1 ? kSOffSlo : kSOffShi) + (part & 1) * kImgPanel + (uint32_t)r0 * kRowB;
+                    bulk_s2s_cluster(dsmem_addr(sbase + off, q), sbase + off, bytes, mb);
                 }
             }
         }
-        fence_proxy_async_cluster();
-        cluster_arrive();  // B2: the S_out images are complete in every CTA
-        cluster_wait();
 
         // 6. O = Q S_out^T per 128-token tile, rows scaled by 1/||q||, bf16 over
         //    the Q tile, TMA store.  Every math warp runs every iteration (work
         //    skipped after an abort), so the named barrier inside always sees
         //    all 256 threads.
         float *ssp = reinterpret_cast<float *>(sm + kSOffQss);  // [2 buffers][2 column groups][128 rows]
-        uint8_t *qs = sm + kSOffQ;
         for (int i = 0; i < my_tiles; ++i) {
-            const int tile = (int)rank + i * p.cl;
-            if (ok) ok = mbar_wait_warp(o_full, i & 1, abort_flag);
-            tc_fence_after();
+            const int tile = (int)rank + i * p.cl, qb = i & 1, use = i >> 1;
+            uint8_t *qs = sm + (qb ? kSOffQ2 : kSOffQ);
+            // |q|^2 of this thread's row from the Q tile, while the MMA runs
+            if (ok) ok = mbar_wait_warp(&q_full[qb], use & 1, abort_flag);
             float ss = 0.f;
             if (ok) {
 #pragma unroll
@@ -531,13 +575,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
                 }
             }
-            ssp[(i & 1) * 256 + g * 128 + row] = ss;
+            ssp[qb * 256 + g * 128 + row] = ss;
             math_sync();
+            if (ok) ok = mbar_wait_warp(&o_full[qb], use & 1, abort_flag);
+            tc_fence_after();
+            const float rq = rsqrtf(ssp[qb * 256 + row] + ssp[qb * 256 + 128 + row] + kEps);
             if (!ok) continue;
-            const float rq = rsqrtf(ssp[(i & 1) * 256 + row] + ssp[(i & 1) * 256 + 128 + row] + kEps);
+            const uint32_t acc = tmem + lane_off + (qb ? kTmA : kTmO);
             for (int cc = cc0; cc < cc1; ++cc) {
                 uint32_t ra[16];
-                tmem_ld16(tmem + lane_off + kTmO + cc * 16, ra);
+                tmem_ld16(acc + cc * 16, ra);
                 tmem_ld_wait();
                 float o[16];
 #pragma unroll
@@ -551,18 +598,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(o_free);
+                mbar_arrive(&o_free[qb]);
                 const int row0 = tile * kTQ + quad * 32;
                 if (row0 < p.N) {
                     tma_store_4d(&mapO, qs + g * kImgPanel + quad * 32 * kRowB, g * 64, h, row0, b);
                     bulk_commit();
                     bulk_wait_read_all();
                 }
-                mbar_arrive(q_empty);
+                mbar_arrive(&q_empty[qb]);
             }
         }
         if (lane == 0) bulk_wait_all();
     }
+    // No CTA leaves while a peer may still copy into its shared memory.
+    cluster_arrive();
+    cluster_wait();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusTimeout);
@@ -669,17 +719,19 @@ cudaError_t launch_frame_step_tc(const void *q, const void *k, const void *v, co
     p.tok_per_cta = per;
     p.c = c;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the previous step's tail
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(BH * cl));
     cfg.blockDim = dim3(kSThreads);
     cfg.dynamicSmemBytes = kSSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k4_frame_step_kernel, mk, mv, mq, mo, p);
 }
 
