@@ -42,6 +42,22 @@ unsigned *device_status_word()
 
 }  // namespace gdn
 
+namespace gdn {
+namespace {
+// Composite of frames without tokens: C = (prod_f gamma_f) I, H = 0.
+__global__ void composite_decay_kernel(const float *gamma, float *C, float *Hc, int H, int F, int D)
+{
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    float g = 1.f;
+    for (int f = 0; f < F; ++f) g *= gamma[((size_t)b * F + f) * H + h];
+    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+        if (C) C[(size_t)bh * D * D + e] = (e / D == e % D) ? g : 0.f;
+        if (Hc) Hc[(size_t)bh * D * D + e] = 0.f;
+    }
+}
+}  // namespace
+}  // namespace gdn
+
 using namespace gdn;
 
 extern "C" {
@@ -223,6 +239,60 @@ gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v, const f
     if (!status) return GDN_ERR_CUDA;
     cudaError_t e = launch_frame_step_tc(q, k, v, beta, gamma, S_in, S_out, o, B, H, N,
                                          default_key_scale(key_scale, D, N), status, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+size_t gdn_frame_composite_workspace_size(int B, int H, int F, int N, int D)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
+    if (D != 112) return (size_t)-1;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 1, &plan)) return (size_t)-1;
+    return plan.ws_bytes;
+}
+
+gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta, const float *gamma, float *C_out,
+                                 float *H_out, int B, int H, int F, int N, int D, float key_scale, void *workspace,
+                                 size_t workspace_bytes, gdn_stream_t stream)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((C_out && !aligned(C_out, 16)) || (H_out && !aligned(H_out, 16))) return GDN_ERR_INVALID_ARG;
+    if (F > 0 && (!gamma || !aligned(gamma, 4))) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (F == 0 || N == 0) {
+        if ((long long)B * H > (1 << 20)) return GDN_ERR_UNSUPPORTED;
+        composite_decay_kernel<<<B * H, 256, 0, st>>>(gamma, C_out, H_out, H, F, D);
+        return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (!k || !v || !beta) return GDN_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(beta, 4)) return GDN_ERR_INVALID_ARG;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 1, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_frame_composite_tc(k, v, beta, gamma, C_out, H_out, plan,
+                                              default_key_scale(key_scale, D, N), workspace, status, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_state_compose(const float *S, const float *C, const float *Hc, float *S_out, int BH, int D,
+                               gdn_stream_t stream)
+{
+    if (BH < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (BH == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if (BH > (1 << 20)) return GDN_ERR_UNSUPPORTED;
+    if (!C || !Hc || !S_out) return GDN_ERR_INVALID_ARG;
+    if (!aligned(C, 16) || !aligned(Hc, 16) || !aligned(S_out, 16) || (S && !aligned(S, 16)))
+        return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_state_compose_tc(S, C, Hc, S_out, BH, status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 8);
+            mbar_init(&q_empty[i], 1);
             mbar_init(&o_full[i], 1);
             mbar_init(&o_free[i], 8);
         }
@@ -580,31 +580,32 @@ __global__ void __launch_bounds__(kSThreads, 1)
             if (ok) ok = mbar_wait_warp(&o_full[qb], use & 1, abort_flag);
             tc_fence_after();
             const float rq = rsqrtf(ssp[qb * 256 + row] + ssp[qb * 256 + 128 + row] + kEps);
-            if (!ok) continue;
-            const uint32_t acc = tmem + lane_off + (qb ? kTmA : kTmO);
-            for (int cc = cc0; cc < cc1; ++cc) {
-                uint32_t ra[16];
-                tmem_ld16(acc + cc * 16, ra);
-                tmem_ld_wait();
-                float o[16];
+            if (ok) {
+                const uint32_t acc = tmem + lane_off + (qb ? kTmA : kTmO);
+                for (int cc = cc0; cc < cc1; ++cc) {
+                    uint32_t ra[16];
+                    tmem_ld16(acc + cc * 16, ra);
+                    tmem_ld_wait();
+                    float o[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
-                const int c8 = cc * 2;
-                *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7)) = f32x8_to_bf16(o);
-                *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(row, (c8 + 1) & 7)) =
-                    f32x8_to_bf16(o + 8);
+                    for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
+                    const int c8 = cc * 2;
+                    *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7)) =
+                        f32x8_to_bf16(o);
+                    *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(row, (c8 + 1) & 7)) =
+                        f32x8_to_bf16(o + 8);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&o_free[qb]);
-                const int row0 = tile * kTQ + quad * 32;
-                if (row0 < p.N) {
-                    tma_store_4d(&mapO, qs + g * kImgPanel + quad * 32 * kRowB, g * 64, h, row0, b);
-                    bulk_commit();
-                    bulk_wait_read_all();
-                }
+            if (lane == 0 && ok) mbar_arrive(&o_free[qb]);
+            math_sync();  // the whole tile is in shared memory: one thread stores it as two 128-row boxes
+            if (t == 0 && ok) {
+                tma_store_4d(&mapO, qs, 0, h, tile * kTQ, b);
+                tma_store_4d(&mapO, qs + kImgPanel, 64, h, tile * kTQ, b);
+                bulk_commit();
+                bulk_wait_read_all();
                 mbar_arrive(&q_empty[qb]);
             }
         }
@@ -705,7 +706,7 @@ cudaError_t launch_frame_step_tc(const void *q, const void *k, const void *v, co
     if (!step_plan(BH, N, dev, &cl, &per)) return cudaErrorInvalidConfiguration;
     CUtensorMap mk, mv, mq, mo;
     if (!make_token_map(&mk, k, B, H, 1, N, kSTS) || !make_token_map(&mv, v, B, H, 1, N, kSTS) ||
-        !make_token_map(&mq, q, B, H, 1, N, kTQ) || !make_token_map(&mo, o, B, H, 1, N, 32))
+        !make_token_map(&mq, q, B, H, 1, N, kTQ) || !make_token_map(&mo, o, B, H, 1, N, kTQ))
         return cudaErrorInvalidValue;
     StepParams p;
     p.beta = beta;

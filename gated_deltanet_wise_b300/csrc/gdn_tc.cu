@@ -56,15 +56,15 @@ constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
 
 // K2
 constexpr int kTQ = 128;                              // tokens per Q/O tile
-constexpr int kK2QStages = 2;
-constexpr int kK2Threads = 320;                       // producer, MMA, 4 state warps, 4 output warps
+constexpr int kK2QStages = 2;                         // Q tiles in flight
+constexpr int kK2Threads = 320;                       // producers, MMA, 4 state warps, 4 output warps
 constexpr uint32_t kK2OffA = kK2QStages * kImgBytes;       // 65536
 constexpr uint32_t kK2OffU = kK2OffA + kAimgBytes;         // 94208
 constexpr uint32_t kK2OffShi = 146432;                     // 1024-aligned after U
 constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 179200
 constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 211968
 constexpr uint32_t kK2Smem = kK2OffBar + 256 + 1024;
-static_assert(kK2OffU + kUimgBytes <= kK2OffShi, "K2 smem layout");
+static_assert(kK2OffU + kUimgBytes <= kK2OffShi && kK2OffShi % 1024 == 0, "K2 smem layout");
 static_assert(kK1Smem <= kMaxSmem && kK2Smem <= kMaxSmem, "shared memory budget");
 
 // ===================================================================== K1
@@ -405,37 +405,68 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 
 // ===================================================================== K1b
 // S_start(c) for every chunk, row-parallel fp32: rows [8*y, 8*y+8) of chain x.
+// The chain is sequential over chunks, S_start(c+1) = S_start(c) C_c + H_c, so
+// each step's composite C_c (50 KB) is bulk-copied into shared memory while
+// the previous step computes (two buffers, one mbarrier each).
 constexpr int kK1bRows = 8;
 constexpr int kK1bThreads = 224;
-constexpr uint32_t kK1bSmem = (kD * kD + kK1bRows * kD) * 4;
+constexpr uint32_t kK1bOffS = 2 * (uint32_t)kStateBytes;           // S rows [8][112]
+constexpr uint32_t kK1bOffBar = kK1bOffS + kK1bRows * kD * 4;      // 2 mbarriers + abort flag
+constexpr uint32_t kK1bSmem = kK1bOffBar + 64;
 
 __global__ void __launch_bounds__(kK1bThreads)
-    k1b_chunk_boundary_kernel(const float *__restrict__ ws_comp, float *__restrict__ ws_start, const float *S_in,
-                              float *S_out, int n_chunks)
+    k1b_chunk_boundary_kernel(const float *__restrict__ compC, const float *__restrict__ compH, size_t chain_stride,
+                              size_t chunk_stride, float *__restrict__ ws_start, const float *S_in, float *S_out,
+                              int n_chunks, unsigned *status)
 {
-    extern __shared__ __align__(16) float k1b_smem[];
-    float *Cs = k1b_smem;                                                   // [kD][kD]
-    float(*Srows)[kD] = reinterpret_cast<float(*)[kD]>(k1b_smem + kD * kD);  // [kK1bRows][kD]
+    extern __shared__ __align__(128) uint8_t k1b_smem[];
+    float *Cb0 = reinterpret_cast<float *>(k1b_smem);
+    float *Cb1 = reinterpret_cast<float *>(k1b_smem + kStateBytes);
+    float(*Srows)[kD] = reinterpret_cast<float(*)[kD]>(k1b_smem + kK1bOffS);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(k1b_smem + kK1bOffBar);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + 2);
     const int bh = blockIdx.x, r0 = blockIdx.y * kK1bRows;
     const int t = threadIdx.x, j = t % kD, rp = t / kD;  // rows r0 + 4*rp + 0..3
+    const float *cC = compC + (size_t)bh * chain_stride, *cH = compH + (size_t)bh * chain_stride;
+    if (t == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
     for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
         const int rr = e / kD, cc = e % kD;
         Srows[rr][cc] = S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
     }
     __syncthreads();
+    if (t == 0 && n_chunks > 0) {
+        mbar_arrive_expect_tx(&bar[0], (uint32_t)kStateBytes);
+        bulk_g2s(Cb0, cC, (uint32_t)kStateBytes, &bar[0]);
+    }
+    int issued = n_chunks > 0 ? 1 : 0;
     for (int c = 0; c < n_chunks; ++c) {
-        float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
-        for (int e = t; e < kK1bRows * kD; e += kK1bThreads) dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
-        const float *C = ws_comp + ((size_t)bh * n_chunks + c) * 2 * kStateFloats;
-        const float *Hc = C + kStateFloats;
-        for (int e = t * 4; e < kStateFloats; e += kK1bThreads * 4)
-            *reinterpret_cast<float4 *>(&Cs[e]) = *reinterpret_cast<const float4 *>(C + e);
-        __syncthreads();
+        if (ws_start) {
+            float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
+            for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
+                dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
+        }
+        // the other buffer was last read in step c-1 (closed by the barrier below): refill it
+        if (t == 0 && c + 1 < n_chunks) {
+            mbar_arrive_expect_tx(&bar[(c + 1) & 1], (uint32_t)kStateBytes);
+            bulk_g2s((c + 1) & 1 ? Cb1 : Cb0, cC + (size_t)(c + 1) * chunk_stride, (uint32_t)kStateBytes,
+                     &bar[(c + 1) & 1]);
+            ++issued;
+        }
+        const float *Hc = cH + (size_t)c * chunk_stride;
         float acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = Hc[(r0 + 4 * rp + q) * kD + j];
+        if (t == 0 && !mbar_wait(&bar[c & 1], (c >> 1) & 1, abort_flag)) *abort_flag = 1;
+        __syncthreads();
+        if (*abort_flag) break;
+        const float *C = (c & 1) ? Cb1 : Cb0;
         for (int l = 0; l < kD; ++l) {
-            const float cl = Cs[l * kD + j];
+            const float cl = C[l * kD + j];
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[q] = fmaf(Srows[4 * rp + q][l], cl, acc[q]);
         }
@@ -443,6 +474,13 @@ __global__ void __launch_bounds__(kK1bThreads)
 #pragma unroll
         for (int q = 0; q < 4; ++q) Srows[4 * rp + q][j] = acc[q];
         __syncthreads();
+    }
+    if (*abort_flag) {
+        if (t == 0) {
+            for (int i = 0; i < issued; ++i) mbar_wait_drain(&bar[i & 1], (i >> 1) & 1);
+            if (status) atomicOr(status, kStatusTimeout);
+        }
+        return;
     }
     if (S_out)
         for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
@@ -458,6 +496,9 @@ struct K2Params {
     int B, H, F, N, chunk, n_chunks;
 };
 
+// Named barrier over K2's four output warps (id 0 is __syncthreads).
+__device__ __forceinline__ void out_warps_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kK2Threads, 1)
     k2_scan_output_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO,
                           const K2Params p)
@@ -465,8 +506,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK2OffBar);
-    uint64_t *q_full = bars + 0, *q_empty = bars + 2;
-    uint64_t *a_full = bars + 4, *a_empty = bars + 5, *u_full = bars + 6, *u_empty = bars + 7;
+    uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages, *u_full = bars + 4, *u_empty = bars + 5;
+    uint64_t *a_full = bars + 6, *a_empty = bars + 7;
     uint64_t *s_ready = bars + 8, *accS_full = bars + 9, *o_done = bars + 10;
     uint64_t *o_full = bars + 11, *o_free = bars + 14, *drain = bars + 17;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
@@ -481,15 +522,15 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const int n_tiles = (p.N + kTQ - 1) / kTQ;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kK2QStages; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 4);
+            mbar_init(&q_empty[i], 1);
         }
         mbar_init(drain, 1);
-        mbar_init(a_full, 1);
-        mbar_init(a_empty, 1);
         mbar_init(u_full, 1);
         mbar_init(u_empty, 4);
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
         mbar_init(s_ready, 4);
         mbar_init(accS_full, 1);
         mbar_init(o_done, 1);
@@ -516,43 +557,47 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const uint8_t *ws_chain = p.ws_frames + ((size_t)bh * p.F + f_begin) * kFrameWs;
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------------ TMA producers
+        // Lane 0 streams the per-frame workspace (A_f image, U_f), lane 1 the Q
+        // tiles, so that neither stream waits behind the other's buffer reuse.
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int qc = 0, q_issued[2] = {0, 0}, a_issued = 0, u_issued = 0;
+            int a_issued = 0, u_issued = 0;
             bool ok = true;
-            for (int it = 0; it <= nf && ok; ++it) {
-                if (it < nf) {
-                    if (it >= 1 && !(ok = mbar_wait(a_empty, (it - 1) & 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(a_full, kAimgBytes);
-                    bulk_g2s(sm + kK2OffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
-                    ++a_issued;
-                }
-                if (it >= 1) {
-                    const int bf = b * p.F + f_begin + it - 1;
-                    for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
-                        const int s = qc & 1;
-                        if (qc >= 2 && !(ok = mbar_wait(&q_empty[s], ((qc >> 1) - 1) & 1, abort_flag))) break;
-                        mbar_arrive_expect_tx(&q_full[s], kImgBytes);
-                        uint8_t *dst = sm + s * kImgBytes;
-                        tma_load_4d(dst, &mapQ, &q_full[s], 0, h, t * kTQ, bf, pol);
-                        tma_load_4d(dst + kImgPanel, &mapQ, &q_full[s], 64, h, t * kTQ, bf, pol);
-                        ++q_issued[s];
-                    }
-                }
-                if (ok && it < nf) {
-                    if (it >= 1 && !(ok = mbar_wait(u_empty, (it - 1) & 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(u_full, kUimgBytes);
-                    bulk_g2s(sm + kK2OffU, ws_chain + (size_t)it * kFrameWs + kAimgBytes, kUimgBytes, u_full);
-                    ++u_issued;
-                }
+            for (int it = 0; it < nf && ok; ++it) {
+                if (it >= 1 && !(ok = mbar_wait(a_empty, (it - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(a_full, kAimgBytes);
+                bulk_g2s(sm + kK2OffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
+                ++a_issued;
+                if (it >= 1 && !(ok = mbar_wait(u_empty, (it - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(u_full, kUimgBytes);
+                bulk_g2s(sm + kK2OffU, ws_chain + (size_t)it * kFrameWs + kAimgBytes, kUimgBytes, u_full);
+                ++u_issued;
             }
             if (*abort_flag) {  // let copies already in flight land before the CTA exits
-                for (int s = 0; s < 2; ++s)
-                    if (q_issued[s]) mbar_wait_drain(&q_full[s], (q_issued[s] - 1) & 1);
                 if (a_issued) mbar_wait_drain(a_full, (a_issued - 1) & 1);
                 if (u_issued) mbar_wait_drain(u_full, (u_issued - 1) & 1);
             }
+        } else if (lane == 1) {
+            const uint64_t pol = policy_evict_first();
+            int qc = 0;
+            bool ok = true;
+            for (int it = 1; it <= nf && ok; ++it) {
+                const int bf = b * p.F + f_begin + it - 1;
+                for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
+                    const int s = qc % kK2QStages;
+                    if (qc >= kK2QStages && !(ok = mbar_wait(&q_empty[s], (qc / kK2QStages - 1) & 1, abort_flag)))
+                        break;
+                    mbar_arrive_expect_tx(&q_full[s], kImgBytes);
+                    uint8_t *dst = sm + s * kImgBytes;
+                    tma_load_4d(dst, &mapQ, &q_full[s], 0, h, t * kTQ, bf, pol);
+                    tma_load_4d(dst + kImgPanel, &mapQ, &q_full[s], 64, h, t * kTQ, bf, pol);
+                }
+            }
+            if (*abort_flag)
+                for (int s = 0; s < kK2QStages && s < qc; ++s) {  // last tile index using stage s
+                    const int last = ((qc - 1 - s) / kK2QStages) * kK2QStages + s;
+                    mbar_wait_drain(&q_full[s], (last / kK2QStages) & 1);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -578,8 +623,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 }
                 if (it >= 1) {
                     for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
-                        const int s = qc & 1, slot = qc % 3;
-                        if (!(ok = mbar_wait(&q_full[s], (qc >> 1) & 1, abort_flag))) break;
+                        const int s = qc % kK2QStages, slot = qc % 3;
+                        if (!(ok = mbar_wait(&q_full[s], (qc / kK2QStages) & 1, abort_flag))) break;
                         if (qc >= 3 && !(ok = mbar_wait(&o_free[slot], ((qc / 3) - 1) & 1, abort_flag))) break;
                         tc_fence_after();
                         const uint32_t acc = tmem + 128 * (slot + 1);
@@ -662,57 +707,66 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         }
     } else {
         // ------------------------------------------------ output warps (tokens)
-        // Each warp owns 32 token rows of a tile: it scales them, writes bf16 in
-        // place over its Q rows and stores its own 32-row boxes with TMA.
+        // Each warp owns 32 token rows of a tile: it scales them and writes bf16
+        // in place over its Q rows; once all four warps are done, one thread
+        // stores the tile as two 128-row boxes (tall boxes stream far better
+        // than 32-row ones).  Every warp runs every iteration (work skipped
+        // after an abort), so the named barrier always sees all 128 threads.
         const int quad = warp & 3, r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const bool leader = warp == 6 && lane == 0;
         int qc = 0;
         bool ok = true;
-        for (int it = 1; it <= nf && ok; ++it) {
+        for (int it = 1; it <= nf; ++it) {
             const int bf = b * p.F + f_begin + it - 1;
             for (int t = 0; t < n_tiles; ++t, ++qc) {
-                const int s = qc & 1, slot = qc % 3;
-                if (!(ok = mbar_wait_warp(&o_full[slot], (qc / 3) & 1, abort_flag))) break;
-                tc_fence_after();
+                const int s = qc % kK2QStages, slot = qc % 3;
                 uint8_t *qs = sm + s * kImgBytes;
-                float ss = 0.f;
+                // 1/||q|| of this thread's token from the Q tile while the MMA runs
+                if (ok) ok = mbar_wait_warp(&q_full[s], (qc / kK2QStages) & 1, abort_flag);
+                float rq = 0.f;
+                if (ok) {
+                    float ss = 0.f;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(qs + (c >> 3) * kImgPanel + r * kRowB +
-                                                                     (((c & 7) ^ (r & 7)) << 4));
-                    float f8[8];
-                    bf16x8_to_f32(u, f8);
+                    for (int c = 0; c < 16; ++c) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(qs + (c >> 3) * kImgPanel + r * kRowB +
+                                                                         (((c & 7) ^ (r & 7)) << 4));
+                        float f8[8];
+                        bf16x8_to_f32(u, f8);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
+                        for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
+                    }
+                    rq = rsqrtf(ss + kEps);
+                    ok = mbar_wait_warp(&o_full[slot], (qc / 3) & 1, abort_flag);
                 }
-                const float rq = rsqrtf(ss + kEps);
-                const uint32_t acc = tmem + 128 * (slot + 1) + lane_off;
+                tc_fence_after();
+                if (ok) {
+                    const uint32_t acc = tmem + 128 * (slot + 1) + lane_off;
 #pragma unroll
-                for (int cc = 0; cc < 7; ++cc) {
-                    uint32_t ra[16];
-                    tmem_ld16(acc + cc * 16, ra);
-                    tmem_ld_wait();
-                    float o[16];
+                    for (int cc = 0; cc < 7; ++cc) {
+                        uint32_t ra[16];
+                        tmem_ld16(acc + cc * 16, ra);
+                        tmem_ld_wait();
+                        float o[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
-                    const int c8 = cc * 2;
-                    *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
-                        f32x8_to_bf16(o);
-                    *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
-                        f32x8_to_bf16(o + 8);
+                        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
+                        const int c8 = cc * 2;
+                        *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
+                            f32x8_to_bf16(o);
+                        *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
+                            f32x8_to_bf16(o + 8);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&o_free[slot]);
-                    const int row0 = t * kTQ + quad * 32;
-                    if (row0 < p.N) {
-                        tma_store_4d(&mapO, qs + quad * 32 * kRowB, 0, h, row0, bf);
-                        tma_store_4d(&mapO, qs + kImgPanel + quad * 32 * kRowB, 64, h, row0, bf);
-                        bulk_commit();
-                        bulk_wait_read_all();
-                    }
+                if (lane == 0 && ok) mbar_arrive(&o_free[slot]);
+                out_warps_sync();
+                if (leader && ok) {
+                    tma_store_4d(&mapO, qs, 0, h, t * kTQ, bf);
+                    tma_store_4d(&mapO, qs + kImgPanel, 64, h, t * kTQ, bf);
+                    bulk_commit();
+                    bulk_wait_read_all();
                     mbar_arrive(&q_empty[s]);
                 }
             }
@@ -764,7 +818,7 @@ bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_plan(int B, int H, int F, int N, int /*num_sms*/, TcPlan *plan)
+bool tc_plan(int B, int H, int F, int N, int force_chunks, TcPlan *plan)
 {
     if (B <= 0 || H <= 0 || F <= 0 || N <= 0) return false;
     const long long BH = (long long)B * H;
@@ -773,7 +827,7 @@ bool tc_plan(int B, int H, int F, int N, int /*num_sms*/, TcPlan *plan)
     // plus a small charge for each sequential boundary step.
     int best_n = 1;
     double best = 1e300;
-    for (int n = 1; n <= F; ++n) {
+    for (int n = 1; n <= F && force_chunks <= 0; ++n) {
         const int L = (F + n - 1) / n;
         const int n_real = (F + L - 1) / L;
         if (n_real != n) continue;
@@ -789,37 +843,41 @@ bool tc_plan(int B, int H, int F, int N, int /*num_sms*/, TcPlan *plan)
     plan->H = H;
     plan->F = F;
     plan->N = N;
-    plan->n_chunks = best_n;
-    plan->chunk = (F + best_n - 1) / best_n;
+    if (force_chunks > F) return false;
+    const int n = force_chunks > 0 ? force_chunks : best_n;
+    plan->chunk = (F + n - 1) / n;
+    plan->n_chunks = (F + plan->chunk - 1) / plan->chunk;
     plan->off_frames = 0;
     plan->off_comp = align_up((size_t)BH * F * kFrameWs, 256);
-    plan->off_start = align_up(plan->off_comp + (size_t)BH * best_n * 2 * kStateBytes, 256);
-    plan->ws_bytes = align_up(plan->off_start + (size_t)BH * best_n * kStateBytes, 256);
+    plan->off_start = align_up(plan->off_comp + (size_t)BH * plan->n_chunks * 2 * kStateBytes, 256);
+    plan->ws_bytes = align_up(plan->off_start + (size_t)BH * plan->n_chunks * kStateBytes, 256);
     return true;
 }
 
-cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
-                                const float *S_in, float *S_out, void *o, const TcPlan &pl, float c, void *workspace,
-                                unsigned *status, cudaStream_t stream, cudaEvent_t *events)
+namespace {
+constexpr int kMaxDevTc = 64;
+bool g_tc_attrs[kMaxDevTc];
+
+// Opt the kernels into their shared-memory sizes, once per device.
+cudaError_t prepare_tc_kernels()
 {
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS) ||
-        !make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, 32))
-        return cudaErrorInvalidValue;
-    static bool attrs_done = false;
-    if (!attrs_done) {
-        cudaError_t e = cudaFuncSetAttribute(k1_frame_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kK1Smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k2_scan_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK2Smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k1b_chunk_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kK1bSmem);
-        if (e != cudaSuccess) return e;
-        attrs_done = true;
-    }
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int BH = pl.B * pl.H;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevTc) return cudaErrorInvalidDevice;
+    if (g_tc_attrs[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(k1_frame_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1Smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k2_scan_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK2Smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k1b_chunk_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1bSmem);
+    if (e != cudaSuccess) return e;
+    g_tc_attrs[dev] = true;
+    return cudaSuccess;
+}
+
+K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, float c, uint8_t *ws, unsigned *status)
+{
     K1Params p1;
     p1.beta = beta;
     p1.gamma = gamma;
@@ -833,14 +891,66 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     p1.chunk = pl.chunk;
     p1.n_chunks = pl.n_chunks;
     p1.c = c;
-    cudaError_t e;
+    return p1;
+}
+}  // namespace
+
+cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float *beta, const float *gamma,
+                                      float *C_out, float *H_out, const TcPlan &pl, float c, void *workspace,
+                                      unsigned *status, cudaStream_t stream)
+{
+    if (pl.n_chunks != 1) return cudaErrorInvalidValue;
+    CUtensorMap mk, mv;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS))
+        return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int BH = pl.B * pl.H;
+    const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
+    k1_frame_stats_kernel<<<BH, kK1Threads, kK1Smem, stream>>>(mk, mv, p1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the chain's composite is (C, H) back to back in the workspace
+    if (C_out && (e = cudaMemcpy2DAsync(C_out, kStateBytes, p1.ws_comp, 2 * kStateBytes, kStateBytes, BH,
+                                        cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+        return e;
+    if (H_out && (e = cudaMemcpy2DAsync(H_out, kStateBytes, p1.ws_comp + kStateFloats, 2 * kStateBytes, kStateBytes,
+                                        BH, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+        return e;
+    return cudaSuccess;
+}
+
+cudaError_t launch_state_compose_tc(const float *S, const float *C, const float *H, float *S_out, int BH,
+                                    unsigned *status, cudaStream_t stream)
+{
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    k1b_chunk_boundary_kernel<<<dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream>>>(
+        C, H, kStateFloats, 0, nullptr, S, S_out, 1, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o, const TcPlan &pl, float c, void *workspace,
+                                unsigned *status, cudaStream_t stream, cudaEvent_t *events)
+{
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS) ||
+        !make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
+        return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int BH = pl.B * pl.H;
+    const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
     if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
     k1_frame_stats_kernel<<<BH * pl.n_chunks, kK1Threads, kK1Smem, stream>>>(mk, mv, p1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     k1b_chunk_boundary_kernel<<<dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream>>>(
-        p1.ws_comp, reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks);
+        p1.ws_comp, p1.ws_comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats, 2 * kStateFloats,
+        reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;

@@ -31,6 +31,7 @@ EXPORTED = [
     "gdn_frame_step_workspace_size", "gdn_frame_step", "gdn_frame_fwd_f32", "gdn_device_status",
     "gdn_frame_fwd_profiled", "gdn_frame_fwd_host_buffer_size", "gdn_frame_fwd_host",
     "gdn_frame_step_noalloc_limit_bytes", "gdn_frame_step_noalloc",
+    "gdn_frame_composite_workspace_size", "gdn_frame_composite", "gdn_state_compose",
 ]
 
 _lib = None
@@ -75,6 +76,12 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_step_noalloc_limit_bytes.argtypes = []
         L.gdn_frame_step_noalloc.restype = I
         L.gdn_frame_step_noalloc.argtypes = [P] * 8 + [I] * 4 + [F, P]
+        L.gdn_frame_composite_workspace_size.restype = Z
+        L.gdn_frame_composite_workspace_size.argtypes = [I] * 5
+        L.gdn_frame_composite.restype = I
+        L.gdn_frame_composite.argtypes = [P] * 6 + [I] * 5 + [F, P, Z, P]
+        L.gdn_state_compose.restype = I
+        L.gdn_state_compose.argtypes = [P] * 4 + [I] * 2 + [P]
         _lib = L
     return _lib
 
@@ -166,6 +173,20 @@ def gdn_frame_step_noalloc(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key
                                             B, H, N, D, float(key_scale), _stream(stream)))
 
 
+def gdn_frame_composite_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
+    return int(lib().gdn_frame_composite_workspace_size(B, H, F, N, D))
+
+
+def gdn_frame_composite(k, v, beta, gamma, C_out, H_out, B, H, F, N, D, key_scale, workspace, workspace_bytes,
+                        stream=None) -> int:
+    return int(lib().gdn_frame_composite(_p(k), _p(v), _p(beta), _p(gamma), _p(C_out), _p(H_out), B, H, F, N, D,
+                                         float(key_scale), _p(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def gdn_state_compose(S, C, Hc, S_out, BH, D, stream=None) -> int:
+    return int(lib().gdn_state_compose(_p(S), _p(C), _p(Hc), _p(S_out), BH, D, _stream(stream)))
+
+
 # ---------------------------------------------------------------- conveniences
 def _shape(q: torch.Tensor, gamma: torch.Tensor) -> Tuple[int, int, int, int, int]:
     B, FN, H, D = q.shape
@@ -249,3 +270,30 @@ def frame_fwd_f32(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, st
     st = gdn_frame_fwd_f32(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, stream)
     _check_status(st, "gdn_frame_fwd_f32")
     return o, S_out
+
+
+def frame_composite(k, v, beta, gamma, *, key_scale: float = 0.0, workspace: Optional[Workspace] = None,
+                    stream=None):
+    """Per-chain composites (C, H) of the frames given, each [B, H, D, D] fp32."""
+    B, H, F, N, D = _shape(k, gamma)
+    for t, n in ((k, "k"), (v, "v")):
+        _check(t, torch.bfloat16, n)
+    C = torch.empty(B, H, D, D, dtype=torch.float32, device=k.device)
+    Hc = torch.empty_like(C)
+    nbytes = gdn_frame_composite_workspace_size(B, H, F, N, D)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_composite_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, k.device)
+    st = gdn_frame_composite(k, v, beta, gamma, C, Hc, B, H, F, N, D, key_scale, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_composite")
+    return C, Hc
+
+
+def state_compose(S, C, Hc, *, out=None, stream=None):
+    """S C + Hc per chain (S None: zero); tensors [..., D, D] fp32."""
+    D = C.shape[-1]
+    BH = C.numel() // (D * D)
+    out = torch.empty_like(C) if out is None else out
+    st = gdn_state_compose(S, C, Hc, out, BH, D, stream)
+    _check_status(st, "gdn_state_compose")
+    return out

@@ -115,6 +115,37 @@ gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v,
                             gdn_stream_t stream);
 
 /*
+ * Context-parallel building blocks (summary page, section 技术新颖性: a run of
+ * frames acts on the state as the affine map S -> S C + H, with the
+ * transition composite C = M_{f0} M_{f0+1} ... M_{f1-1} and the input
+ * composite H = the state the run reaches from S = 0; composing the runs'
+ * maps in frame order reproduces the single-device result exactly).  A rank
+ * that owns frames [f0, f1) computes its (C, H), all ranks exchange them, each
+ * composes the maps of the ranks before it onto S_in with gdn_state_compose to
+ * get its start state, and runs gdn_frame_fwd on its frames from there.
+ *
+ * gdn_frame_composite: per chain (b, h), (C, H) of the F frames given, same
+ * layouts and key_scale as gdn_frame_fwd (frames [0, F) of the arrays passed);
+ * C_out, H_out: fp32 [B][H][D][D] (either may be NULL).  Workspace:
+ * gdn_frame_composite_workspace_size() bytes (0 for F == 0 or N == 0, where
+ * C = (prod gamma) I and H = 0).  Same errors as gdn_frame_fwd.
+ */
+size_t gdn_frame_composite_workspace_size(int B, int H, int F, int N, int D);
+gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta,
+                                 const float *gamma, float *C_out, float *H_out,
+                                 int B, int H, int F, int N, int D, float key_scale,
+                                 void *workspace, size_t workspace_bytes,
+                                 gdn_stream_t stream);
+
+/*
+ * gdn_state_compose: S_out = S C + Hc for each of BH chains (fp32
+ * [BH][D][D], row = value index; S == NULL means S = 0).  S_out may alias S;
+ * it must not alias C or Hc.  D == 112 only.  No workspace.
+ */
+gdn_status_t gdn_state_compose(const float *S, const float *C, const float *Hc, float *S_out,
+                               int BH, int D, gdn_stream_t stream);
+
+/*
  * fp32 validation entry: the same operation with fp32 q/k/v/o, computed with
  * fp32 CUDA-core arithmetic (one CTA per chain).  Any 1 <= D <= 128.  Needs no
  * workspace.  Intended for numerical validation (relative error ~1e-6), not

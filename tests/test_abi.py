@@ -93,6 +93,19 @@ def test_host_side_validation_without_gpu(L):
     assert step(1, 1, 8, 112, gamma=None) == gdn.GDN_ERR_INVALID_ARG
     assert step(1, 1, 8, 112, o=P(0x10002)) == gdn.GDN_ERR_INVALID_ARG   # misaligned
     assert step(1, 1, 8, 112, S_in=P(0x10004)) == gdn.GDN_ERR_INVALID_ARG
+    comp = L.gdn_frame_composite
+    assert comp(fake, fake, fake, fake, fake, fake, 1, 1, 2, 8, 64, 0.0, None, 0, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert comp(fake, fake, fake, None, fake, fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert comp(fake, fake, fake, fake, fake, fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_WORKSPACE
+    assert comp(fake, fake, fake, fake, P(0x10004), fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_frame_composite_workspace_size(1, 20, 16, 880, 112) >= 20 * 16 * 80000
+    assert gdn.gdn_frame_composite_workspace_size(1, 20, 0, 880, 112) == 0
+    cmp_ = L.gdn_state_compose
+    assert cmp_(None, None, fake, fake, 4, 112, None) == gdn.GDN_ERR_INVALID_ARG
+    assert cmp_(None, fake, fake, fake, 4, 96, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert cmp_(None, fake, fake, fake, -1, 112, None) == gdn.GDN_ERR_INVALID_ARG
+    assert cmp_(None, fake, fake, fake, 0, 112, None) == gdn.GDN_OK
+    assert cmp_(P(0x10008), fake, fake, fake, 4, 112, None) == gdn.GDN_ERR_INVALID_ARG
     f32 = L.gdn_frame_fwd_f32
     assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, 1, 1, 1, 129, 0.0, None) == gdn.GDN_ERR_UNSUPPORTED
     assert f32(fake, fake, fake, fake, fake, None, fake, fake, 1, -1, 1, 1, 16, 0.0, None) == gdn.GDN_ERR_INVALID_ARG
