@@ -321,7 +321,8 @@ def measure_streaming(x, K, W, stream):
             "tokens_per_s_graph": round(B * F * N / (graph_ms * 1e-3), 1),
             "algorithmic_bytes_per_call": call_bytes,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic("k4_frame_step_kernel"),
+                         "kernel": "k4_frame_step_kernel",
                          "note": f"per call inside the graph (launch gaps included); peak {kind}"},
             "launches_per_pass": F}
 
