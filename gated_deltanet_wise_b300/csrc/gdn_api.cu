@@ -125,6 +125,44 @@ gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v, const fl
                           workspace_bytes, stream, nullptr);
 }
 
+size_t gdn_frame_fwd_product_workspace_size(int B, int H, int F, int N, int D)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
+    if (D != 112) return (size_t)-1;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 1, &plan)) return (size_t)-1;
+    return plan.ws_bytes;
+}
+
+gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v, const float *beta,
+                                   const float *gamma, const float *S_in, float *S_out, void *o, int B, int H,
+                                   int F, int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
+                                   gdn_stream_t stream)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if (F == 0 || N == 0)  // no tokens: both readings reduce to S_out = (prod gamma) S_in
+        return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+                              workspace_bytes, stream, nullptr);
+    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !beta || !gamma) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4) ||
+        !aligned(gamma, 4))
+        return GDN_ERR_INVALID_ARG;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 1, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_frame_fwd_product_tc(q, k, v, beta, gamma, S_in, S_out, o, plan,
+                                                default_key_scale(key_scale, D, N), workspace, status,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v, const float *beta,
                                     const float *gamma, const float *S_in, float *S_out, void *o, int B, int H,
                                     int F, int N, int D, float key_scale, void *workspace, size_t workspace_bytes,

@@ -47,6 +47,16 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
                                 void *workspace, unsigned *status, cudaStream_t stream,
                                 cudaEvent_t *events = nullptr);
 
+// token-ordered ("product") reading, D == 112: per-frame transitions by the
+// UT-transform kernel into the plan's frame workspace (gdn_product.cu), and the
+// whole forward with a one-chunk plan (gdn_tc.cu).
+cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *beta, const TcPlan &plan, float c,
+                                    void *workspace, unsigned *status, cudaStream_t stream);
+cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void *v, const float *beta,
+                                        const float *gamma, const float *S_in, float *S_out, void *o,
+                                        const TcPlan &plan, float c, void *workspace, unsigned *status,
+                                        cudaStream_t stream);
+
 // fused single-frame step (gdn_step.cu); D == 112.
 cudaError_t launch_frame_step_tc(const void *q, const void *k, const void *v, const float *beta,
                                  const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int N,

@@ -1,0 +1,494 @@
+// gdn_product.cu — frame transitions of the token-ordered ("product") reading
+// of the frame-wise GDN, head size D = 112, bf16 k/v, fp32 beta/state.
+//
+// Summary page "SANA-WM: Efficient Minute-Scale World Modeling with Hybrid
+// Linear Diffusion Transformer": the frame transition is printed as
+// gamma_t I - K^_t beta_t K^_t^T (section 方法步骤详情, module 2), and the layer
+// generalises token-wise Gated DeltaNet (section 技术新颖性).  Read with beta_t
+// as the UT-transform matrix, the frame's tokens act in order:
+//     M_f = gamma_f I - Abar_f,   Abar_f = I - prod_n (I - beta_n k^_n k^_n^T),
+//     U_f = W_f = the state the frame's tokens reach from zero,
+// and the pair (Abar, W) obeys the delta rule with the keys themselves as
+// Abar's values.  Over a sub-chunk of 64 tokens (rows K^, K, V):
+//     G   = K^ K^^T,  T = (I + StrictLower(diag(beta) G))^-1 diag(beta),
+//     R   = [K^ | V] - K^ [Abar ; W]^T                 (residual rows),
+//     X   = T R = diag(beta) R + T_off R                (T_off = T - diag(beta)),
+//     [Abar ; W] += X^T K^ = (X diag(c/r))^T K         (raw K: an exact operand).
+//
+// One CTA per (frame, chain), sub-chunks in order.  tcgen05 forms G, R~ (the
+// product K^ [Abar ; W]^T, N = 2 x 128), T_off R (accumulated on top of the
+// fp32 diag(beta) R stored into TMEM) and the pair update (fp32 TMEM
+// accumulators, X split hi + lo); CUDA cores solve the 64 x 64 unit-triangular
+// system for T (one column per thread, in registers).  Abar is accumulated
+// transposed, so the accumulator's lanes are Abar's columns: its bf16 image is
+// then directly the B operand the scan kernel multiplies S by, and the kernel
+// writes (Abar_f^T image, W_f) in the per-frame workspace format of the sum
+// reading's frame-statistics kernel.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "gdn_internal.h"
+#include "gdn_tile.cuh"
+
+namespace gdn {
+
+constexpr int kPC = 64;                                // tokens per sub-chunk
+constexpr uint32_t kPPanel = kPC * kRowB;              // 8192: a 64-column panel of a 64-row tile
+constexpr int kPThreads = 320;                         // producer, MMA, 8 math warps
+// shared memory (1024-aligned regions)
+constexpr uint32_t kPOffK = 0;                         // raw K tiles, two buffers of 16 KB
+constexpr uint32_t kPOffV = 32768;                     // raw V tiles, two buffers of 16 KB
+constexpr uint32_t kPOffKh = 65536;                    // K^ = c/r k (bf16), 64 rows x 2 panels
+constexpr uint32_t kPOffSA = 81920;                    // Abar^T image: rows = key j, 2 panels of 64 i (B, MN-major)
+constexpr uint32_t kPOffSW = 114688;                   // W image: rows = value i, 2 panels of 64 j (B, K-major)
+constexpr uint32_t kPSPanel = 128 * kRowB;             // 16384
+constexpr uint32_t kPOffT = 147456;                    // T_off image: 64 rows x 1 panel (+ slack: M = 128 reads)
+constexpr uint32_t kPOffR = 163840;                    // R_hi image, then X_hi: 64 rows x 4 panels
+constexpr uint32_t kPOffXlo = 196608;                  // G (fp32 64 x 64), then X_lo image
+constexpr uint32_t kPOffBar = 229376;
+constexpr uint32_t kPOffArr = kPOffBar + 256;          // c/r and beta per token (2 x 64 floats)
+constexpr uint32_t kPSmem = kPOffArr + 512 + 1024;
+static_assert(kPSmem <= kMaxSmem, "product kernel shared memory");
+
+// TMEM: Abar [0,128), W [128,256), G / R~ / X [256,512)
+constexpr uint32_t kPTmA = 0, kPTmW = 128, kPTmX = 256;
+
+constexpr uint32_t kIdG = idesc_bf16(128, 64, false, false);    // G = K^ K^^T
+constexpr uint32_t kIdRA = idesc_bf16(128, 128, false, true);   // R~_A = K^ Abar^T (B = Abar^T image)
+constexpr uint32_t kIdRW = idesc_bf16(128, 128, false, false);  // R~_W = K^ W^T
+constexpr uint32_t kIdX = idesc_bf16(128, 256, false, true);    // X += T_off R
+constexpr uint32_t kIdU = idesc_bf16(128, kD, true, true);      // pair += X'^T K
+
+__device__ __forceinline__ void p_math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+struct ProdParams {
+    const float *beta;
+    uint8_t *ws_frames;  // [BH][F] x kFrameWs
+    unsigned *status;
+    int B, H, F, N;
+    float c;
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    kp_frame_product_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                            const ProdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPOffBar);
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 2, *prep_done = bars + 4, *g_full = bars + 5;
+    uint64_t *g_read = bars + 6, *simg_ready = bars + 7, *rt_full = bars + 8, *r_ready = bars + 9;
+    uint64_t *x_full = bars + 10, *x_ready = bars + 11, *upd_done = bars + 12, *drain = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 15);
+    float *cr = reinterpret_cast<float *>(sm + kPOffArr);   // c / ||k|| per token
+    float *bt = cr + 64;                                     // beta per token (0 past the frame)
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p.B * p.H;
+    const int f = blockIdx.x / BH, bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int bf = b * p.F + f;
+    const int n_sc = (p.N + kPC - 1) / kPC;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        mbar_init(prep_done, 8);
+        mbar_init(g_full, 1);
+        mbar_init(g_read, 4);
+        mbar_init(simg_ready, 8);
+        mbar_init(rt_full, 1);
+        mbar_init(r_ready, 8);
+        mbar_init(x_full, 1);
+        mbar_init(x_ready, 4);
+        mbar_init(upd_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (int sc = 0; sc < n_sc; ++sc) {
+                const int kb = sc & 1;
+                if (sc >= 2 && !mbar_wait(&kv_empty[kb], ((sc >> 1) - 1) & 1, abort_flag)) break;
+                uint8_t *kd = sm + kPOffK + kb * 2 * kPPanel, *vd = sm + kPOffV + kb * 2 * kPPanel;
+                mbar_arrive_expect_tx(&kv_full[kb], 4 * kPPanel);
+                tma_load_4d(kd, &mapK, &kv_full[kb], 0, h, sc * kPC, bf, pol);
+                tma_load_4d(kd + kPPanel, &mapK, &kv_full[kb], 64, h, sc * kPC, bf, pol);
+                tma_load_4d(vd, &mapV, &kv_full[kb], 0, h, sc * kPC, bf, pol);
+                tma_load_4d(vd + kPPanel, &mapV, &kv_full[kb], 64, h, sc * kPC, bf, pol);
+                ++issued;
+            }
+            if (*abort_flag)  // let loads already in flight land before the CTA exits
+                for (int kb = 0; kb < 2 && kb < issued; ++kb) {
+                    const int last = ((issued - 1 - kb) / 2) * 2 + kb;
+                    mbar_wait_drain(&kv_full[kb], (last >> 1) & 1);
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            for (int sc = 0; sc < n_sc && ok; ++sc) {
+                const int kb = sc & 1, ph = sc & 1;
+                const uint32_t kraw = sbase + kPOffK + kb * 2 * kPPanel, kh = sbase + kPOffKh;
+                if (!(ok = mbar_wait(prep_done, ph, abort_flag))) break;
+                tc_fence_after();
+                // G = K^ K^^T (64 x 64, lanes = tokens)
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint32_t koff = (ks >> 2) * kPPanel + (ks & 3) * 32;
+                    mma_bf16(tmem + kPTmX, sdesc_sw128(kh + koff, 16, 1024), sdesc_sw128(kh + koff, 16, 1024), kIdG,
+                             ks > 0);
+                }
+                mma_commit(g_full);
+                // R~ = K^ [Abar ; W]^T once G is read out and the pair image is current
+                if (!(ok = mbar_wait(g_read, ph, abort_flag))) break;
+                if (!(ok = mbar_wait(simg_ready, ph, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint64_t ad = sdesc_sw128(kh + (ks >> 2) * kPPanel + (ks & 3) * 32, 16, 1024);
+                    mma_bf16(tmem + kPTmX, ad, sdesc_sw128(sbase + kPOffSA + ks * 2048, kPSPanel, 1024), kIdRA, ks > 0);
+                    mma_bf16(tmem + kPTmX + 128, ad,
+                             sdesc_sw128(sbase + kPOffSW + (ks >> 2) * kPSPanel + (ks & 3) * 32, 16, 1024), kIdRW, ks > 0);
+                }
+                mma_commit(rt_full);
+                // X = diag(beta) R (already in TMEM) + T_off R_hi
+                if (!(ok = mbar_wait(r_ready, ph, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kPC / 16; ++ks)
+                    mma_bf16(tmem + kPTmX, sdesc_sw128(sbase + kPOffT + ks * 32, 16, 1024),
+                             sdesc_sw128(sbase + kPOffR + ks * 2048, kPPanel, 1024), kIdX, 1u);
+                mma_commit(x_full);
+                // pair update (X' = X c/r as hi + lo; all operands token-row tiles, MN-major):
+                //   Abar^T += K^T X'_A  (lanes = key j),   W += X'_W^T K  (lanes = value i)
+                if (!(ok = mbar_wait(x_ready, ph, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kPC / 16; ++ks) {
+                    const uint64_t kd = sdesc_sw128(kraw + ks * 2048, kPPanel, 1024);
+                    const uint32_t acc = (sc > 0 || ks > 0) ? 1u : 0u;
+                    const uint32_t oa = ks * 2048, ow = 2 * kPPanel + ks * 2048;
+                    mma_bf16(tmem + kPTmA, kd, sdesc_sw128(sbase + kPOffR + oa, kPPanel, 1024), kIdU, acc);
+                    mma_bf16(tmem + kPTmA, kd, sdesc_sw128(sbase + kPOffXlo + oa, kPPanel, 1024), kIdU, 1u);
+                    mma_bf16(tmem + kPTmW, sdesc_sw128(sbase + kPOffR + ow, kPPanel, 1024), kd, kIdU, acc);
+                    mma_bf16(tmem + kPTmW, sdesc_sw128(sbase + kPOffXlo + ow, kPPanel, 1024), kd, kIdU, 1u);
+                }
+                mma_commit(upd_done);
+                mma_commit(&kv_empty[kb]);
+            }
+            mma_commit(drain);  // every MMA issued above has completed once this phase lands
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------- math warps
+        // G is kept column-major (Gs[c * 64 + a] = G[a][c]): lanes store
+        // consecutive words, and the solve reads a column as a broadcast row.
+        const int t = threadIdx.x - 64;                  // 0..255
+        const int quad = warp & 3, g = (warp - 2) >> 2;  // TMEM lane quadrant, column half
+        const int row = quad * 32 + lane;                // TMEM lane (token or pair row)
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const bool tok_warp = quad < 2;                  // lanes 0..63 hold the token-indexed results
+        float *Gs = reinterpret_cast<float *>(sm + kPOffXlo);
+        bool ok = true;
+
+        // the pair starts at zero: zero image
+        for (int e = t; e < (int)(4 * kPSPanel / 16); e += 256)
+            reinterpret_cast<uint4 *>(sm + kPOffSA)[e] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(simg_ready);
+
+        for (int sc = 0; sc < n_sc; ++sc) {
+            const int kb = sc & 1, ph = sc & 1;
+            const int m = min(kPC, p.N - sc * kPC);  // tokens of this sub-chunk
+            uint8_t *kraw = sm + kPOffK + kb * 2 * kPPanel, *vraw = sm + kPOffV + kb * 2 * kPPanel;
+
+            // (1) norms; K^ = c/r k as bf16; c/r and beta per token
+            {
+                const int r = t >> 2, qq = t & 3;
+                const uint32_t off = (qq >> 1) * kPPanel + r * kRowB;
+                const float bet = r < m ? __ldg(p.beta + ((size_t)bf * p.N + sc * kPC + r) * p.H + h) : 0.f;
+                if (ok) ok = mbar_wait_warp(&kv_full[kb], (sc >> 1) & 1, abort_flag);
+                if (ok) {
+                    float kf[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
+                        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(kraw + off + pos), kf + 8 * i);
+                    }
+                    float ss = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ss = fmaf(kf[i], kf[i], ss);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    const float inv = p.c * rsqrtf(ss + kEps);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t pos = (((i + qq + r) & 3) + 4 * (qq & 1)) << 4;
+                        float kh[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) kh[e] = inv * kf[8 * i + e];
+                        *reinterpret_cast<uint4 *>(sm + kPOffKh + off + pos) = f32x8_to_bf16(kh);
+                    }
+                    if (qq == 0) {
+                        cr[r] = r < m ? inv : 0.f;
+                        bt[r] = bet;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(prep_done);
+            }
+
+            // (2) G out of TMEM into shared memory (token warps), visible to all math warps
+            if (tok_warp) {
+                if (ok) ok = mbar_wait_warp(g_full, ph, abort_flag);
+                tc_fence_after();
+                if (ok) {
+                    uint32_t rg[16];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        tmem_ld16(tmem + lane_off + kPTmX + g * 32 + cc * 16, rg);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) Gs[(g * 32 + cc * 16 + j) * 64 + row] = __uint_as_float(rg[j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(g_read);
+            }
+            p_math_sync();
+
+            if (warp == 2 || warp == 3) {
+                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta), column e = t per thread,
+                //     by forward substitution in right-looking order: once t_r is known it is
+                //     added into every later row's sum (independent FMAs, broadcast reads of
+                //     column r of G); t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r.
+                //     The strictly lower part T_off goes to the bf16 image (row a, column e).
+                const int e = t;
+                const float be = bt[e];
+                float Tc[kPC];
+#pragma unroll
+                for (int a = 0; a < kPC; ++a) Tc[a] = 0.f;
+#pragma unroll
+                for (int r2 = 0; r2 < kPC; ++r2) {
+                    Tc[r2] = (r2 == e ? be : 0.f) - bt[r2] * Tc[r2];
+#pragma unroll
+                    for (int a4 = (r2 + 1) >> 2; a4 < kPC / 4; ++a4) {
+                        const float4 g4 = reinterpret_cast<const float4 *>(Gs + r2 * 64)[a4];
+                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (4 * a4 + j > r2) Tc[4 * a4 + j] = fmaf(gv[j], Tc[r2], Tc[4 * a4 + j]);
+                    }
+                }
+                __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + kPOffT);
+#pragma unroll
+                for (int a = 0; a < kPC; ++a) {
+                    const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
+                    timg[off >> 1] = __float2bfloat16_rn(a > e ? Tc[a] : 0.f);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(r_ready);
+            } else if (tok_warp) {
+                // (4) R = [K^ | V] - R~ (row = token): R_hi image for the MMA, and the exact
+                //     diag(beta) R written over R~ in TMEM as the start of X.  The key part
+                //     takes K^ from its bf16 image, the same values R~ was formed from, so
+                //     that R's rounding error scales with R rather than with K^.
+                if (ok) ok = mbar_wait_warp(rt_full, ph, abort_flag);
+                tc_fence_after();
+                if (ok) {
+                    const float btt = bt[row];
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int n0 = g * 128 + cc * 16;  // column of [Abar | W] (padded to 128 each)
+                        const int y0 = cc * 16;            // column inside K or V
+                        uint32_t rr[16];
+                        tmem_ld16(tmem + lane_off + kPTmX + n0, rr);
+                        tmem_ld_wait();
+                        float y[16];
+                        if (y0 < kD) {
+                            const uint8_t *src = g == 0 ? sm + kPOffKh : vraw;
+                            const uint32_t pb = (y0 >> 6) * kPPanel;
+                            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(src + pb + sw128_off(row, (y0 & 63) >> 3)), y);
+                            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(src + pb + sw128_off(row, ((y0 & 63) >> 3) + 1)),
+                                          y + 8);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) y[j] = 0.f;
+                        }
+                        float rv[16];
+                        uint32_t xd0[8], xd1[8];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) rv[j] = y[j] - __uint_as_float(rr[j]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            xd0[j] = __float_as_uint(btt * rv[j]);
+                            xd1[j] = __float_as_uint(btt * rv[8 + j]);
+                        }
+                        tmem_st8(tmem + lane_off + kPTmX + n0, xd0);
+                        tmem_st8(tmem + lane_off + kPTmX + n0 + 8, xd1);
+                        uint8_t *dst = sm + kPOffR + (n0 >> 6) * kPPanel;
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, (n0 & 63) >> 3)) = f32x8_to_bf16(rv);
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, ((n0 & 63) >> 3) + 1)) = f32x8_to_bf16(rv + 8);
+                    }
+                    tmem_st_wait();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(r_ready);
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(r_ready);
+            }
+
+            // (5) X' = X c/r as hi + lo MMA images (token warps)
+            if (tok_warp) {
+                if (ok) ok = mbar_wait_warp(x_full, ph, abort_flag);
+                tc_fence_after();
+                if (ok) {
+                    const float crt = cr[row];
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int n0 = g * 128 + cc * 16;
+                        uint32_t rx[16];
+                        tmem_ld16(tmem + lane_off + kPTmX + n0, rx);
+                        tmem_ld_wait();
+                        float xv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xv[j] = __uint_as_float(rx[j]) * crt;
+                        uint4 hi0, lo0, hi1, lo1;
+                        split_bf16x8(xv, hi0, lo0);
+                        split_bf16x8(xv + 8, hi1, lo1);
+                        const uint32_t pb = (n0 >> 6) * kPPanel;
+                        const uint32_t o0 = pb + sw128_off(row, (n0 & 63) >> 3), o1 = pb + sw128_off(row, ((n0 & 63) >> 3) + 1);
+                        *reinterpret_cast<uint4 *>(sm + kPOffR + o0) = hi0;
+                        *reinterpret_cast<uint4 *>(sm + kPOffR + o1) = hi1;
+                        *reinterpret_cast<uint4 *>(sm + kPOffXlo + o0) = lo0;
+                        *reinterpret_cast<uint4 *>(sm + kPOffXlo + o1) = lo1;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_ready);
+            }
+
+            // (6) after the update: refresh the pair images (Abar^T row j from lane j, W row i
+            //     from lane i), or after the last sub-chunk write the frame's Abar^T image
+            //     (bf16) and W_f (fp32) to the workspace
+            if (ok) ok = mbar_wait_warp(upd_done, ph, abort_flag);
+            tc_fence_after();
+            const bool last = sc + 1 == n_sc;
+            uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
+            float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
+            const int cc0 = g ? 4 : 0, cc1 = g ? 7 : 4;  // 16-column chunks: panel g
+            if (ok) {
+                for (int cc = cc0; cc < cc1; ++cc) {
+                    uint32_t ra[16], rw[16];
+                    tmem_ld16(tmem + lane_off + kPTmA + cc * 16, ra);
+                    tmem_ld16(tmem + lane_off + kPTmW + cc * 16, rw);
+                    tmem_ld_wait();
+                    if (row < kD) {
+                        float a[16], w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            a[j] = __uint_as_float(ra[j]);
+                            w[j] = __uint_as_float(rw[j]);
+                        }
+                        const int c8 = 2 * (cc & 3);
+                        if (!last) {
+                            uint8_t *da = sm + kPOffSA + (cc >> 2) * kPSPanel, *dw = sm + kPOffSW + (cc >> 2) * kPSPanel;
+                            *reinterpret_cast<uint4 *>(da + sw128_off(row, c8)) = f32x8_to_bf16(a);
+                            *reinterpret_cast<uint4 *>(da + sw128_off(row, c8 + 1)) = f32x8_to_bf16(a + 8);
+                            *reinterpret_cast<uint4 *>(dw + sw128_off(row, c8)) = f32x8_to_bf16(w);
+                            *reinterpret_cast<uint4 *>(dw + sw128_off(row, c8 + 1)) = f32x8_to_bf16(w + 8);
+                        } else {
+                            uint8_t *dst = ws + (cc >> 2) * kAimgPanel;
+                            *reinterpret_cast<uint4 *>(dst + sw128_off(row, c8)) = f32x8_to_bf16(a);
+                            *reinterpret_cast<uint4 *>(dst + sw128_off(row, c8 + 1)) = f32x8_to_bf16(a + 8);
+                            float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + cc * 16);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                u4[j] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        }
+                    }
+                }
+                if (last && g == 1 && row < kD) {  // key columns 112..127 of the image: zero
+                    *reinterpret_cast<uint4 *>(ws + kAimgPanel + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(ws + kAimgPanel + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (!last && lane == 0) mbar_arrive(simg_ready);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+namespace {
+constexpr int kMaxDevP = 64;
+bool g_p_attr[kMaxDevP];
+}  // namespace
+
+cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *beta, const TcPlan &pl, float c,
+                                    void *workspace, unsigned *status, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevP) return cudaErrorInvalidDevice;
+    if (!g_p_attr[dev]) {
+        e = cudaFuncSetAttribute(kp_frame_product_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+        if (e != cudaSuccess) return e;
+        g_p_attr[dev] = true;
+    }
+    CUtensorMap mk, mv;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kPC) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kPC))
+        return cudaErrorInvalidValue;
+    ProdParams p;
+    p.beta = beta;
+    p.ws_frames = static_cast<uint8_t *>(workspace) + pl.off_frames;
+    p.status = status;
+    p.B = pl.B;
+    p.H = pl.H;
+    p.F = pl.F;
+    p.N = pl.N;
+    p.c = c;
+    const long long grid = (long long)pl.B * pl.H * pl.F;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kp_frame_product_kernel<<<(unsigned)grid, kPThreads, kPSmem, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -492,6 +492,7 @@ struct K2Params {
     const float *gamma;
     const uint8_t *ws_frames;
     const float *ws_start;
+    float *S_out;  // non-null: the last chunk's CTAs write the chain's final state here
     unsigned *status;
     int B, H, F, N, chunk, n_chunks;
 };
@@ -704,6 +705,12 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             if (lane == 0) mbar_arrive(u_empty);
             if (it >= 1 && !mbar_wait_warp(o_done, (it - 1) & 1, abort_flag)) break;
             write_images();
+        }
+        if (p.S_out && chunk_idx + 1 == p.n_chunks && row < kD) {
+            float *dst = p.S_out + (size_t)bh * kStateFloats + row * kD;
+#pragma unroll
+            for (int j = 0; j < kD; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     } else {
         // ------------------------------------------------ output warps (tokens)
@@ -958,6 +965,7 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     p2.gamma = gamma;
     p2.ws_frames = ws + pl.off_frames;
     p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
+    p2.S_out = nullptr;  // the boundary kernel has written it
     p2.status = status;
     p2.B = pl.B;
     p2.H = pl.H;
@@ -970,6 +978,44 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
     return cudaSuccess;
+}
+
+// Token-ordered reading: per-frame transitions from the UT-transform kernel
+// (gdn_product.cu) in the workspace format K2 consumes, then K2 over one
+// chunk per chain, starting from S_in (or zero) and writing S_out itself.
+cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void *v, const float *beta,
+                                        const float *gamma, const float *S_in, float *S_out, void *o,
+                                        const TcPlan &pl, float c, void *workspace, unsigned *status,
+                                        cudaStream_t stream)
+{
+    if (pl.n_chunks != 1) return cudaErrorInvalidValue;
+    CUtensorMap mq, mo;
+    if (!make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
+        return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int BH = pl.B * pl.H;
+    if ((e = launch_frame_product_tc(k, v, beta, pl, c, workspace, status, stream)) != cudaSuccess) return e;
+    const float *start = S_in;
+    if (!start) {
+        if ((e = cudaMemsetAsync(ws + pl.off_start, 0, (size_t)BH * kStateBytes, stream)) != cudaSuccess) return e;
+        start = reinterpret_cast<const float *>(ws + pl.off_start);
+    }
+    K2Params p2;
+    p2.gamma = gamma;
+    p2.ws_frames = ws + pl.off_frames;
+    p2.ws_start = start;  // one chunk per chain: [B][H][D][D], the layout of S_in
+    p2.S_out = S_out;
+    p2.status = status;
+    p2.B = pl.B;
+    p2.H = pl.H;
+    p2.F = pl.F;
+    p2.N = pl.N;
+    p2.chunk = pl.chunk;
+    p2.n_chunks = 1;
+    k2_scan_output_kernel<<<BH, kK2Threads, kK2Smem, stream>>>(mq, mo, p2);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -94,6 +94,33 @@ gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v,
                            gdn_stream_t stream);
 
 /*
+ * Token-ordered ("product") reading of the same layer.  The summary page
+ * (section 方法步骤详情, module 2) prints the frame transition as
+ * M_f = gamma_f I - K^ beta K^^T and says the layer generalises token-wise
+ * Gated DeltaNet (section 技术新颖性).  gdn_frame_fwd reads beta as the
+ * diagonal of the frame's token weights (the first-order sum); this entry
+ * reads it as the UT-transform matrix, so the frame's tokens act in order:
+ *   M_f = gamma_f I - Abar_f,  I - Abar_f = prod_n (I - beta_n k^_n k^_n^T)
+ *   U_f = sum_n beta_n v_n k^_n^T (I - beta_{n+1} k^_{n+1} k^_{n+1}^T) ... (I - beta_N k^_N k^_N^T)
+ *   S_f = S_{f-1} M_f + U_f,   o = S_f q^ (as gdn_frame_fwd)
+ * i.e. within a frame the state follows the delta rule token by token from
+ * the frame's start state, and the decay gamma_f is applied once per frame.
+ * The two readings differ at order (c_k^2 ||k^||^2)^2 per token pair: at the
+ * default key_scale they agree to about 1e-8; with unit keys (key_scale = 1)
+ * they differ at first order.  Arguments, layouts, ownership and status codes
+ * are those of gdn_frame_fwd; the workspace size has its own query.  Results
+ * match the fp64 definition within 5e-3 relative Frobenius error on o and
+ * S_out for inputs drawn as in the tests, key_scale up to 1.
+ */
+size_t gdn_frame_fwd_product_workspace_size(int B, int H, int F, int N, int D);
+gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v,
+                                   const float *beta, const float *gamma,
+                                   const float *S_in, float *S_out, void *o,
+                                   int B, int H, int F, int N, int D, float key_scale,
+                                   void *workspace, size_t workspace_bytes,
+                                   gdn_stream_t stream);
+
+/*
  * Streaming step: one latent frame (F = 1) per call, state carried by the
  * caller (chunk-causal / autoregressive generation, the chunk-wise variant of
  * the CSDN article's §六 stage 4; resume by passing the previous call's S_out
