@@ -429,10 +429,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             uint8_t *dst = ws + (cc >> 2) * kAimgPanel;
                             *reinterpret_cast<uint4 *>(dst + sw128_off(row, c8)) = f32x8_to_bf16(a);
                             *reinterpret_cast<uint4 *>(dst + sw128_off(row, c8 + 1)) = f32x8_to_bf16(a + 8);
-                            float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + cc * 16);
+                            float4 *u4 = reinterpret_cast<float4 *>(wsU) + (cc * 4) * kD + row;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                u4[j] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                                u4[j * kD] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                         }
                     }
                 }

@@ -58,13 +58,13 @@ constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
 constexpr int kTQ = 128;                              // tokens per Q/O tile
 constexpr int kK2QStages = 2;                         // Q tiles in flight
 constexpr int kK2Threads = 320;                       // producers, MMA, 4 state warps, 4 output warps
-constexpr uint32_t kK2OffA = kK2QStages * kImgBytes;       // 65536
-constexpr uint32_t kK2OffU = kK2OffA + kAimgBytes;         // 94208
-constexpr uint32_t kK2OffShi = 146432;                     // 1024-aligned after U
-constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 179200
-constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 211968
+constexpr uint32_t kK2OffO = kK2QStages * kImgBytes;       // 65536: two output staging tiles
+constexpr uint32_t kK2OffA = kK2OffO + 2 * kImgBytes;      // 131072
+constexpr uint32_t kK2OffShi = kK2OffA + kAimgBytes;       // 159744
+constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 192512
+constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 225280
 constexpr uint32_t kK2Smem = kK2OffBar + 256 + 1024;
-static_assert(kK2OffU + kUimgBytes <= kK2OffShi && kK2OffShi % 1024 == 0, "K2 smem layout");
+static_assert(kK2OffShi % 1024 == 0 && kK2OffA % 1024 == 0, "K2 smem layout");
 static_assert(kK1Smem <= kMaxSmem && kK2Smem <= kMaxSmem, "shared memory budget");
 
 // ===================================================================== K1
@@ -311,11 +311,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                     uint8_t *dst = sm + kK1OffAimg + (cc >> 2) * kAimgPanel;
                     *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3))) = f32x8_to_bf16(a);
                     *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3) + 1)) = f32x8_to_bf16(a + 8);
-                    float4 *u4 = reinterpret_cast<float4 *>(wsU + row * kUStride + col);
+                    float4 *u4 = reinterpret_cast<float4 *>(wsU) + (col / 4) * kD + row;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        u4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
-                                            __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+                        u4[j * kD] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                                 __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
                 }
             }
             if (row < kD) {  // key columns 112..127 of the image: zero
@@ -507,12 +507,11 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK2OffBar);
-    uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages, *u_full = bars + 4, *u_empty = bars + 5;
-    uint64_t *a_full = bars + 6, *a_empty = bars + 7;
-    uint64_t *s_ready = bars + 8, *accS_full = bars + 9, *o_done = bars + 10;
-    uint64_t *o_full = bars + 11, *o_free = bars + 14, *drain = bars + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+    uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages, *a_full = bars + 4, *a_empty = bars + 5;
+    uint64_t *s_ready = bars + 6, *accS_full = bars + 7, *o_done = bars + 8;
+    uint64_t *o_full = bars + 9, *o_free = bars + 12, *drain = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = p.B * p.H;
@@ -525,11 +524,9 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kK2QStages; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 1);
+            mbar_init(&q_empty[i], 5);  // the tile's MMAs (commit) + the four output warps (norms read)
         }
         mbar_init(drain, 1);
-        mbar_init(u_full, 1);
-        mbar_init(u_empty, 4);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         mbar_init(s_ready, 4);
@@ -559,25 +556,21 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producers
-        // Lane 0 streams the per-frame workspace (A_f image, U_f), lane 1 the Q
-        // tiles, so that neither stream waits behind the other's buffer reuse.
+        // Lane 0 streams the per-frame A_f images (and prefetches U_f into L2
+        // for the state warps), lane 1 the Q tiles, so that neither stream
+        // waits behind the other's buffer reuse.
         if (lane == 0) {
-            int a_issued = 0, u_issued = 0;
-            bool ok = true;
-            for (int it = 0; it < nf && ok; ++it) {
-                if (it >= 1 && !(ok = mbar_wait(a_empty, (it - 1) & 1, abort_flag))) break;
+            int a_issued = 0;
+            bulk_prefetch_l2(ws_chain + kAimgBytes, kUBytes);
+            for (int it = 0; it < nf; ++it) {
+                if (it >= 1 && !mbar_wait(a_empty, (it - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(a_full, kAimgBytes);
                 bulk_g2s(sm + kK2OffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
+                if (it + 1 < nf) bulk_prefetch_l2(ws_chain + (size_t)(it + 1) * kFrameWs + kAimgBytes, kUBytes);
                 ++a_issued;
-                if (it >= 1 && !(ok = mbar_wait(u_empty, (it - 1) & 1, abort_flag))) break;
-                mbar_arrive_expect_tx(u_full, kUimgBytes);
-                bulk_g2s(sm + kK2OffU, ws_chain + (size_t)it * kFrameWs + kAimgBytes, kUimgBytes, u_full);
-                ++u_issued;
             }
-            if (*abort_flag) {  // let copies already in flight land before the CTA exits
-                if (a_issued) mbar_wait_drain(a_full, (a_issued - 1) & 1);
-                if (u_issued) mbar_wait_drain(u_full, (u_issued - 1) & 1);
-            }
+            if (*abort_flag && a_issued)  // let the copy in flight land before the CTA exits
+                mbar_wait_drain(a_full, (a_issued - 1) & 1);
         } else if (lane == 1) {
             const uint64_t pol = policy_evict_first();
             int qc = 0;
@@ -638,6 +631,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                             mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffSlo + koff, 16, 1024), kIdescK, 1);
                         }
                         mma_commit(&o_full[slot]);
+                        mma_commit(&q_empty[s]);
                     }
                     if (ok) mma_commit(o_done);
                 }
@@ -647,7 +641,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         }
     } else if (warp < 6) {
         // ------------------------------------------------- state warps (rows)
+        // Thread = row of S, held in fp32 registers.  As soon as S_f's images
+        // are written, S <- gamma_f S + U_f (U_f read from global memory, where
+        // it was prefetched into L2 a frame ahead, quad-major: a warp's lanes
+        // read 512 contiguous bytes), overlapping the S A_f GEMM; when that
+        // lands, S <- S - S_f A_f.
         const int quad = warp & 3, row = quad * 32 + lane;
+        const int urow = row < kD ? row : 0;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         float S[kD];
         const float *s0 = p.ws_start + ((size_t)bh * p.n_chunks + chunk_idx) * kStateFloats;
@@ -682,27 +682,38 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         for (int it = 0; it < nf; ++it) {
             const float g = g_next;
             if (it + 1 < nf) g_next = __ldg(gam + (size_t)(it + 1) * p.H);
+            const float4 *U4 = reinterpret_cast<const float4 *>(ws_chain + (size_t)it * kFrameWs + kAimgBytes) + urow;
+            float4 ub[2][4];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ub[c][j] = __ldg(U4 + (c * 4 + j) * kD);
+#pragma unroll
+            for (int cc = 0; cc < 7; ++cc) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 u4 = ub[cc & 1][j];
+                    const int c0 = cc * 16 + 4 * j;
+                    S[c0] = fmaf(g, S[c0], u4.x);
+                    S[c0 + 1] = fmaf(g, S[c0 + 1], u4.y);
+                    S[c0 + 2] = fmaf(g, S[c0 + 2], u4.z);
+                    S[c0 + 3] = fmaf(g, S[c0 + 3], u4.w);
+                }
+                if (cc + 2 < 7)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ub[cc & 1][j] = __ldg(U4 + ((cc + 2) * 4 + j) * kD);
+            }
             if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
-            if (!mbar_wait_warp(u_full, it & 1, abort_flag)) break;
             tc_fence_after();
-            const float *U = reinterpret_cast<const float *>(sm + kK2OffU) + (row < kD ? row : 0) * kUStride;
 #pragma unroll
             for (int cc = 0; cc < 7; ++cc) {
                 uint32_t ra[16];
                 tmem_ld16(tmem + lane_off + cc * 16, ra);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 u4 = *reinterpret_cast<const float4 *>(U + cc * 16 + j);
-                    S[cc * 16 + j] = fmaf(g, S[cc * 16 + j], u4.x - __uint_as_float(ra[j]));
-                    S[cc * 16 + j + 1] = fmaf(g, S[cc * 16 + j + 1], u4.y - __uint_as_float(ra[j + 1]));
-                    S[cc * 16 + j + 2] = fmaf(g, S[cc * 16 + j + 2], u4.z - __uint_as_float(ra[j + 2]));
-                    S[cc * 16 + j + 3] = fmaf(g, S[cc * 16 + j + 3], u4.w - __uint_as_float(ra[j + 3]));
-                }
+                for (int j = 0; j < 16; ++j) S[cc * 16 + j] -= __uint_as_float(ra[j]);
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(u_empty);
             if (it >= 1 && !mbar_wait_warp(o_done, (it - 1) & 1, abort_flag)) break;
             write_images();
         }
@@ -714,11 +725,15 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         }
     } else {
         // ------------------------------------------------ output warps (tokens)
-        // Each warp owns 32 token rows of a tile: it scales them and writes bf16
-        // in place over its Q rows; once all four warps are done, one thread
+        // Each warp owns 32 token rows of a tile.  It computes their 1/||q||
+        // from the Q tile (then releases the Q stage: the tile's MMAs release
+        // it too), scales the accumulator rows and writes bf16 into one of two
+        // output staging tiles; once all four warps are done, one thread
         // stores the tile as two 128-row boxes (tall boxes stream far better
-        // than 32-row ones).  Every warp runs every iteration (work skipped
-        // after an abort), so the named barrier always sees all 128 threads.
+        // than 32-row ones).  Before a staging tile is rewritten, that thread
+        // has seen the store issued from it two tiles earlier finish reading.
+        // Every warp runs every iteration (work skipped after an abort), so the
+        // named barriers always see all 128 threads.
         const int quad = warp & 3, r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const bool leader = warp == 6 && lane == 0;
@@ -728,8 +743,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             const int bf = b * p.F + f_begin + it - 1;
             for (int t = 0; t < n_tiles; ++t, ++qc) {
                 const int s = qc % kK2QStages, slot = qc % 3;
-                uint8_t *qs = sm + s * kImgBytes;
-                // 1/||q|| of this thread's token from the Q tile while the MMA runs
+                const uint8_t *qs = sm + s * kImgBytes;
+                uint8_t *os = sm + kK2OffO + (qc & 1) * kImgBytes;
                 if (ok) ok = mbar_wait_warp(&q_full[s], (qc / kK2QStages) & 1, abort_flag);
                 float rq = 0.f;
                 if (ok) {
@@ -744,9 +759,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                         for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
                     }
                     rq = rsqrtf(ss + kEps);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&q_empty[s]);
                     ok = mbar_wait_warp(&o_full[slot], (qc / 3) & 1, abort_flag);
                 }
                 tc_fence_after();
+                if (leader) bulk_wait_read_le1();  // the store from this staging tile (two tiles ago) has read it
+                out_warps_sync();
                 if (ok) {
                     const uint32_t acc = tmem + 128 * (slot + 1) + lane_off;
 #pragma unroll
@@ -758,9 +777,9 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
                         const int c8 = cc * 2;
-                        *reinterpret_cast<uint4 *>(qs + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
+                        *reinterpret_cast<uint4 *>(os + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
                             f32x8_to_bf16(o);
-                        *reinterpret_cast<uint4 *>(qs + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
+                        *reinterpret_cast<uint4 *>(os + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
                             f32x8_to_bf16(o + 8);
                     }
                 }
@@ -770,11 +789,9 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 if (lane == 0 && ok) mbar_arrive(&o_free[slot]);
                 out_warps_sync();
                 if (leader && ok) {
-                    tma_store_4d(&mapO, qs, 0, h, t * kTQ, bf);
-                    tma_store_4d(&mapO, qs + kImgPanel, 64, h, t * kTQ, bf);
+                    tma_store_4d(&mapO, os, 0, h, t * kTQ, bf);
+                    tma_store_4d(&mapO, os + kImgPanel, 64, h, t * kTQ, bf);
                     bulk_commit();
-                    bulk_wait_read_all();
-                    mbar_arrive(&q_empty[s]);
                 }
             }
         }

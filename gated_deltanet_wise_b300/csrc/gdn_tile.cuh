@@ -15,9 +15,11 @@ constexpr float kEps = 1e-12f;        // ||x|| = sqrt(sum x^2 + eps)
 constexpr uint32_t kRowB = 128;                      // one swizzled row: 64 bf16
 constexpr uint32_t kAimgPanel = kD * kRowB;          // 14336: A_f image, 112 rows
 constexpr uint32_t kAimgBytes = 2 * kAimgPanel;      // 28672
-constexpr uint32_t kUStride = 116;                   // floats per U_f row (padded: conflict-free smem rows)
-constexpr uint32_t kUimgBytes = kD * kUStride * 4;   // 51968
-constexpr uint32_t kFrameWs = kAimgBytes + kUimgBytes;  // 80640 bytes per (chain, frame)
+// U_f in the frame workspace: fp32, stored as float4 column quads, quad-major:
+// float4 index (c4 * kD + i) holds U[i][4 c4 .. 4 c4 + 3].  A warp whose lanes
+// are consecutive rows reads or writes 512 contiguous bytes per access.
+constexpr uint32_t kUBytes = kD * kD * 4;            // 50176
+constexpr uint32_t kFrameWs = kAimgBytes + kUBytes;  // 78848 bytes per (chain, frame)
 constexpr uint32_t kImgPanel = 128 * kRowB;          // 16384: 128-row bf16 image panel
 constexpr uint32_t kImgBytes = 2 * kImgPanel;        // 32768
 constexpr uint32_t kStateFloats = kD * kD;           // 12544
