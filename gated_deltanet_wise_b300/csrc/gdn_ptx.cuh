@@ -114,6 +114,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
     return true;
 }
 
+// Programmatic dependent launch: let the next grid on the stream be scheduled,
+// and wait until the previous grid has completed with its writes visible.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA / bulk
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1, int c2,
                                             int c3, uint64_t policy)

@@ -113,14 +113,6 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, uint32_t 
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
-// Programmatic dependent launch: let the next grid on the stream be scheduled,
-// and wait until the previous grid has completed with its writes visible.
-__device__ __forceinline__ void griddep_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Named barrier over the 8 math warps (ids 1.., 0 is __syncthreads).
 __device__ __forceinline__ void math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 

@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Programmatic dependent launch: the next kernel may be scheduled now; no
+    // global memory is touched before the previous kernel has completed.
+    griddep_launch_dependents();
+    griddep_wait();
     const uint32_t sbase = smem_u32(sm);
 
     if (warp == 0) {
@@ -434,6 +438,8 @@ __global__ void __launch_bounds__(kK1bThreads)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    griddep_launch_dependents();
+    griddep_wait();  // composites and S_in come from earlier kernels on the stream
     for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
         const int rr = e / kD, cc = e % kD;
         Srows[rr][cc] = S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
@@ -552,6 +558,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
+    griddep_launch_dependents();
+    griddep_wait();
     const uint8_t *ws_chain = p.ws_frames + ((size_t)bh * p.F + f_begin) * kFrameWs;
 
     if (warp == 0) {
@@ -879,6 +887,26 @@ bool tc_plan(int B, int H, int F, int N, int force_chunks, TcPlan *plan)
 }
 
 namespace {
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it calls griddepcontrol.wait
+// before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t stream,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kMaxDevTc = 64;
 bool g_tc_attrs[kMaxDevTc];
 
@@ -932,8 +960,8 @@ cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = pl.B * pl.H;
     const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
-    k1_frame_stats_kernel<<<BH, kK1Threads, kK1Smem, stream>>>(mk, mv, p1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(k1_frame_stats_kernel, dim3(BH), kK1Threads, kK1Smem, stream, mk, mv, p1)) != cudaSuccess)
+        return e;
     // the chain's composite is (C, H) back to back in the workspace
     if (C_out && (e = cudaMemcpy2DAsync(C_out, kStateBytes, p1.ws_comp, 2 * kStateBytes, kStateBytes, BH,
                                         cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
@@ -949,9 +977,8 @@ cudaError_t launch_state_compose_tc(const float *S, const float *C, const float 
 {
     cudaError_t e = prepare_tc_kernels();
     if (e != cudaSuccess) return e;
-    k1b_chunk_boundary_kernel<<<dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream>>>(
-        C, H, kStateFloats, 0, nullptr, S, S_out, 1, status);
-    return cudaGetLastError();
+    return launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream, C, H,
+                      (size_t)kStateFloats, (size_t)0, (float *)nullptr, S, S_out, 1, status);
 }
 
 cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
@@ -968,14 +995,13 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     const int BH = pl.B * pl.H;
     const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
     if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
-    k1_frame_stats_kernel<<<BH * pl.n_chunks, kK1Threads, kK1Smem, stream>>>(mk, mv, p1);
-    e = cudaGetLastError();
+    e = launch_pdl(k1_frame_stats_kernel, dim3(BH * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
-    k1b_chunk_boundary_kernel<<<dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream>>>(
-        p1.ws_comp, p1.ws_comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats, 2 * kStateFloats,
-        reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks, status);
-    e = cudaGetLastError();
+    e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
+                   (const float *)p1.ws_comp, (const float *)(p1.ws_comp + kStateFloats),
+                   (size_t)pl.n_chunks * 2 * kStateFloats, (size_t)2 * kStateFloats,
+                   reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks, status);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
     K2Params p2;
@@ -990,8 +1016,7 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     p2.N = pl.N;
     p2.chunk = pl.chunk;
     p2.n_chunks = pl.n_chunks;
-    k2_scan_output_kernel<<<BH * pl.n_chunks, kK2Threads, kK2Smem, stream>>>(mq, mo, p2);
-    e = cudaGetLastError();
+    e = launch_pdl(k2_scan_output_kernel, dim3(BH * pl.n_chunks), kK2Threads, kK2Smem, stream, mq, mo, p2);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -1031,8 +1056,7 @@ cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void
     p2.N = pl.N;
     p2.chunk = pl.chunk;
     p2.n_chunks = 1;
-    k2_scan_output_kernel<<<BH, kK2Threads, kK2Smem, stream>>>(mq, mo, p2);
-    return cudaGetLastError();
+    return launch_pdl(k2_scan_output_kernel, dim3(BH), kK2Threads, kK2Smem, stream, mq, mo, p2);
 }
 
 }  // namespace gdn
