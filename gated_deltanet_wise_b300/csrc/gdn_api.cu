@@ -77,9 +77,10 @@ const char *gdn_status_string(gdn_status_t s)
     return "unknown status";
 }
 
-size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D)
+static size_t fwd_workspace_size(int B, int H, int F, int N, int D, unsigned flags)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE)) return (size_t)-1;
     if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
     if (D != 112) return (size_t)-1;
     TcPlan plan;
@@ -87,17 +88,30 @@ size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D)
     return plan.ws_bytes;
 }
 
+size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D) { return fwd_workspace_size(B, H, F, N, D, 0); }
+
+size_t gdn_frame_fwd_product_workspace_size(int B, int H, int F, int N, int D)
+{
+    return fwd_workspace_size(B, H, F, N, D, GDN_FWD_PRODUCT);
+}
+
+size_t gdn_frame_fwd_ex_workspace_size(int B, int H, int F, int N, int D, unsigned flags)
+{
+    return fwd_workspace_size(B, H, F, N, D, flags);
+}
+
 static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, const float *beta,
                                    const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int F,
-                                   int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
-                                   gdn_stream_t stream, void **events)
+                                   int N, int D, float key_scale, unsigned flags, void *workspace,
+                                   size_t workspace_bytes, gdn_stream_t stream, void **events)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE)) return GDN_ERR_INVALID_ARG;
     if (B == 0 || H == 0) return GDN_OK;
     if (D != 112) return GDN_ERR_UNSUPPORTED;
     if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (F == 0 || N == 0) {
+    if (F == 0 || N == 0) {  // no tokens: every reading and direction gives S_out = (prod gamma) S_in
         if (F > 0 && (!gamma || !aligned(gamma, 4))) return GDN_ERR_INVALID_ARG;
         if (!S_out) return GDN_OK;
         return launch_decay_only(gamma, S_in, S_out, B, H, F, D, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -106,14 +120,19 @@ static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, 
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4) ||
         !aligned(gamma, 4))
         return GDN_ERR_INVALID_ARG;
+    const bool product = (flags & GDN_FWD_PRODUCT) != 0;
+    const int reverse = (flags & GDN_FWD_REVERSE) ? 1 : 0;
     TcPlan plan;
     if (!tc_plan(B, H, F, N, 0, &plan)) return GDN_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
     unsigned *status = device_status_word();
     if (!status) return GDN_ERR_CUDA;
-    cudaError_t e = launch_frame_fwd_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, default_key_scale(key_scale, D, N),
-                                        workspace, status, st, reinterpret_cast<cudaEvent_t *>(events));
+    const float c = default_key_scale(key_scale, D, N);
+    cudaError_t e = product ? launch_frame_fwd_product_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse,
+                                                          workspace, status, st)
+                            : launch_frame_fwd_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse, workspace,
+                                                  status, st, reinterpret_cast<cudaEvent_t *>(events));
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -121,18 +140,8 @@ gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v, const fl
                            const float *S_in, float *S_out, void *o, int B, int H, int F, int N, int D,
                            float key_scale, void *workspace, size_t workspace_bytes, gdn_stream_t stream)
 {
-    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, 0, workspace,
                           workspace_bytes, stream, nullptr);
-}
-
-size_t gdn_frame_fwd_product_workspace_size(int B, int H, int F, int N, int D)
-{
-    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
-    if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
-    if (D != 112) return (size_t)-1;
-    TcPlan plan;
-    if (!tc_plan(B, H, F, N, 1, &plan)) return (size_t)-1;
-    return plan.ws_bytes;
 }
 
 gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v, const float *beta,
@@ -140,27 +149,17 @@ gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v, 
                                    int F, int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
                                    gdn_stream_t stream)
 {
-    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
-    if (B == 0 || H == 0) return GDN_OK;
-    if (D != 112) return GDN_ERR_UNSUPPORTED;
-    if (F == 0 || N == 0)  // no tokens: both readings reduce to S_out = (prod gamma) S_in
-        return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
-                              workspace_bytes, stream, nullptr);
-    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
-    if (!q || !k || !v || !o || !beta || !gamma) return GDN_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4) ||
-        !aligned(gamma, 4))
-        return GDN_ERR_INVALID_ARG;
-    TcPlan plan;
-    if (!tc_plan(B, H, F, N, 1, &plan)) return GDN_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
-    if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
-    unsigned *status = device_status_word();
-    if (!status) return GDN_ERR_CUDA;
-    cudaError_t e = launch_frame_fwd_product_tc(q, k, v, beta, gamma, S_in, S_out, o, plan,
-                                                default_key_scale(key_scale, D, N), workspace, status,
-                                                static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, GDN_FWD_PRODUCT,
+                          workspace, workspace_bytes, stream, nullptr);
+}
+
+gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                              const float *S_in, float *S_out, void *o, int B, int H, int F, int N, int D,
+                              float key_scale, unsigned flags, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream)
+{
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, flags, workspace,
+                          workspace_bytes, stream, nullptr);
 }
 
 gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v, const float *beta,
@@ -168,7 +167,7 @@ gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v,
                                     int F, int N, int D, float key_scale, void *workspace, size_t workspace_bytes,
                                     gdn_stream_t stream, void **events)
 {
-    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, 0, workspace,
                           workspace_bytes, stream, events);
 }
 
@@ -239,7 +238,7 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v, con
     gdn_status_t s = frame_fwd_impl(d + L.off_q, d + L.off_k, d + L.off_v, reinterpret_cast<float *>(d + L.off_beta),
                                     reinterpret_cast<float *>(d + L.off_gamma),
                                     S_in ? reinterpret_cast<float *>(d + L.off_sin) : nullptr,
-                                    reinterpret_cast<float *>(d + L.off_sout), d + L.off_o, B, H, F, N, D, key_scale,
+                                    reinterpret_cast<float *>(d + L.off_sout), d + L.off_o, B, H, F, N, D, key_scale, 0,
                                     L.ws ? d + L.off_ws : nullptr, L.ws, stream, nullptr);
     if (s != GDN_OK) return s;
     if (has_tokens && o && !d2h(o, L.off_o, L.tok)) return GDN_ERR_CUDA;

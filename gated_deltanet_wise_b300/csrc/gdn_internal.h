@@ -42,19 +42,22 @@ cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float 
 // S_out = S C + H per chain (S may be null: zero), fp32.
 cudaError_t launch_state_compose_tc(const float *S, const float *C, const float *H, float *S_out, int BH,
                                     unsigned *status, cudaStream_t stream);
+// reverse = 1 visits the frames from the last to the first (reverse-direction scan).
 cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
-                                const float *S_in, float *S_out, void *o, const TcPlan &plan, float c,
+                                const float *S_in, float *S_out, void *o, const TcPlan &plan, float c, int reverse,
                                 void *workspace, unsigned *status, cudaStream_t stream,
                                 cudaEvent_t *events = nullptr);
 
 // token-ordered ("product") reading, D == 112: per-frame transitions by the
-// UT-transform kernel into the plan's frame workspace (gdn_product.cu), and the
-// whole forward with a one-chunk plan (gdn_tc.cu).
+// UT-transform kernel into the plan's frame workspace and their chunk
+// composites (gdn_product.cu), and the whole forward (gdn_tc.cu).
 cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *beta, const TcPlan &plan, float c,
-                                    void *workspace, unsigned *status, cudaStream_t stream);
+                                    int reverse, void *workspace, unsigned *status, cudaStream_t stream);
+cudaError_t launch_chunk_composite_tc(const float *gamma, const TcPlan &plan, int reverse, void *workspace,
+                                      unsigned *status, cudaStream_t stream);
 cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void *v, const float *beta,
                                         const float *gamma, const float *S_in, float *S_out, void *o,
-                                        const TcPlan &plan, float c, void *workspace, unsigned *status,
+                                        const TcPlan &plan, float c, int reverse, void *workspace, unsigned *status,
                                         cudaStream_t stream);
 
 // fused single-frame step (gdn_step.cu); D == 112.

@@ -65,10 +65,11 @@ __device__ __forceinline__ void p_math_sync() { asm volatile("bar.sync 1, 256;" 
 
 struct ProdParams {
     const float *beta;
-    uint8_t *ws_frames;  // [BH][F] x kFrameWs
+    uint8_t *ws_frames;  // [BH][F] x kFrameWs, by processing position
     unsigned *status;
     int B, H, F, N;
     float c;
+    int reverse;  // 1: processing position f holds frame F - 1 - f
 };
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int BH = p.B * p.H;
     const int f = blockIdx.x / BH, bh = blockIdx.x % BH;
     const int b = bh / p.H, h = bh % p.H;
-    const int bf = b * p.F + f;
+    const int bf = b * p.F + frame_at(f, p.F, p.reverse);  // the frame's tokens; workspace slot f
     const int n_sc = (p.N + kPC - 1) / kPC;
 
     if (threadIdx.x == 0) {
@@ -456,13 +457,203 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
+// ===================================================================== K1c
+// Chunk composites of the product reading, from the per-frame workspace:
+// per (chunk, chain) C = M_{f0} ... M_{f1-1} and H = the state the chunk's
+// frames reach from zero, i.e. C <- gamma_f C - C Abar_f, H <- gamma_f H -
+// H Abar_f + U_f over the chunk's frames (summary page, section 技术新颖性:
+// the C_p / H_p composites).  In the sum reading the frame-statistics kernel
+// forms them while it builds A_f; here A_f = Abar_f is not small, so C and H
+// enter the GEMM as hi + lo bf16 images (fp32-accurate), against the bf16
+// Abar_f^T image the scan kernel also uses.  Four warps hold C's rows and four
+// H's rows in fp32 registers.
+constexpr int kCThreads = 320;                          // producer, MMA, 4 C warps, 4 H warps
+constexpr uint32_t kCOffA = 0;                          // Abar_f^T image (K2 layout)
+constexpr uint32_t kCOffImg = 32768;                    // C_hi, C_lo, H_hi, H_lo: 128-row images
+constexpr uint32_t kCOffBar = kCOffImg + 4 * kImgBytes; // 163840
+constexpr uint32_t kCSmem = kCOffBar + 256 + 1024;
+
+struct CompParams {
+    const float *gamma;
+    const uint8_t *ws_frames;  // [BH][F] x kFrameWs, by processing position
+    float *ws_comp;            // [BH][n_chunks] x (C, H) fp32
+    unsigned *status;
+    int B, H, F, chunk, n_chunks, reverse;
+};
+
+__global__ void __launch_bounds__(kCThreads, 1) kc_chunk_composite_kernel(const CompParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kCOffBar);
+    uint64_t *a_full = bars + 0, *a_empty = bars + 1, *s_ready = bars + 2, *acc_full = bars + 3, *drain = bars + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 6);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p.B * p.H;
+    const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int f_begin = chunk_idx * p.chunk;
+    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        mbar_init(s_ready, 8);
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
+    }
+    // zero the images (rows 112..127 and key columns 112..127 stay zero)
+    for (int o = threadIdx.x * 16; o < 4 * (int)kImgBytes; o += kCThreads * 16)
+        *reinterpret_cast<uint4 *>(sm + kCOffImg + o) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+    const uint8_t *ws_chain = p.ws_frames + ((size_t)bh * p.F + f_begin) * kFrameWs;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            bulk_prefetch_l2(ws_chain + kAimgBytes, kUBytes);
+            for (int it = 0; it < nf; ++it) {
+                if (it >= 1 && !mbar_wait(a_empty, (it - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(a_full, kAimgBytes);
+                bulk_g2s(sm + kCOffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
+                if (it + 1 < nf) bulk_prefetch_l2(ws_chain + (size_t)(it + 1) * kFrameWs + kAimgBytes, kUBytes);
+                ++issued;
+            }
+            if (*abort_flag && issued) mbar_wait_drain(a_full, (issued - 1) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int it = 0; it < nf && ok; ++it) {
+                if (!(ok = mbar_wait(s_ready, it & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(a_full, it & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                    const uint64_t bd = sdesc_sw128(sbase + kCOffA + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {  // m = 0: C, 1: H
+                        const uint32_t img = sbase + kCOffImg + m * 2 * kImgBytes + koff;
+                        mma_bf16(tmem + 128 * m, sdesc_sw128(img, 16, 1024), bd, kIdescK, ks > 0);
+                        mma_bf16(tmem + 128 * m, sdesc_sw128(img + kImgBytes, 16, 1024), bd, kIdescK, 1);
+                    }
+                }
+                mma_commit(acc_full);
+                mma_commit(a_empty);
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        const int m = (warp - 2) >> 2;  // 0: C rows, 1: H rows
+        const int quad = warp & 3, row = quad * 32 + lane;
+        const int urow = row < kD ? row : 0;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        uint8_t *img_hi = sm + kCOffImg + m * 2 * kImgBytes, *img_lo = img_hi + kImgBytes;
+        float S[kD];
+#pragma unroll
+        for (int j = 0; j < kD; ++j) S[j] = (m == 0 && row == j) ? 1.f : 0.f;
+        auto write_images = [&]() {
+            if (row < kD) {
+#pragma unroll
+                for (int c8 = 0; c8 < kD / 8; ++c8) {
+                    uint4 hi, lo;
+                    split_bf16x8(S + 8 * c8, hi, lo);
+                    const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
+                    *reinterpret_cast<uint4 *>(img_hi + off) = hi;
+                    *reinterpret_cast<uint4 *>(img_lo + off) = lo;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_ready);
+        };
+        write_images();
+        const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
+        bool ok = true;
+        for (int it = 0; it < nf && ok; ++it) {
+            const float g = __ldg(gam + (size_t)frame_at(f_begin + it, p.F, p.reverse) * p.H);
+            // S <- gamma S (+ U_f for H) while the GEMM runs, then S <- S - S Abar_f
+            if (m == 1) {
+                const float4 *U4 =
+                    reinterpret_cast<const float4 *>(ws_chain + (size_t)it * kFrameWs + kAimgBytes) + urow;
+                float4 ub[2][4];  // 16-column chunks, loaded two ahead of their use
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ub[c][j] = __ldg(U4 + (c * 4 + j) * kD);
+#pragma unroll
+                for (int cc = 0; cc < 7; ++cc) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 u4 = ub[cc & 1][j];
+                        const int c0 = cc * 16 + 4 * j;
+                        S[c0] = fmaf(g, S[c0], u4.x);
+                        S[c0 + 1] = fmaf(g, S[c0 + 1], u4.y);
+                        S[c0 + 2] = fmaf(g, S[c0 + 2], u4.z);
+                        S[c0 + 3] = fmaf(g, S[c0 + 3], u4.w);
+                    }
+                    if (cc + 2 < 7)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) ub[cc & 1][j] = __ldg(U4 + ((cc + 2) * 4 + j) * kD);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kD; ++j) S[j] *= g;
+            }
+            if (!(ok = mbar_wait_warp(acc_full, it & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 7; ++cc) {
+                uint32_t ra[16];
+                tmem_ld16(tmem + 128 * m + lane_off + cc * 16, ra);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) S[cc * 16 + j] -= __uint_as_float(ra[j]);
+            }
+            tc_fence_before();
+            if (it + 1 < nf) write_images();
+        }
+        if (ok && row < kD) {
+            float *dst = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats +
+                         (size_t)m * kStateFloats + row * kD;
+#pragma unroll
+            for (int j = 0; j < kD; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
 namespace {
 constexpr int kMaxDevP = 64;
 bool g_p_attr[kMaxDevP];
+bool g_c_attr[kMaxDevP];
 }  // namespace
 
 cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *beta, const TcPlan &pl, float c,
-                                    void *workspace, unsigned *status, cudaStream_t stream)
+                                    int reverse, void *workspace, unsigned *status, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -485,9 +676,39 @@ cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *b
     p.F = pl.F;
     p.N = pl.N;
     p.c = c;
+    p.reverse = reverse;
     const long long grid = (long long)pl.B * pl.H * pl.F;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kp_frame_product_kernel<<<(unsigned)grid, kPThreads, kPSmem, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+
+cudaError_t launch_chunk_composite_tc(const float *gamma, const TcPlan &pl, int reverse, void *workspace,
+                                      unsigned *status, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevP) return cudaErrorInvalidDevice;
+    if (!g_c_attr[dev]) {
+        e = cudaFuncSetAttribute(kc_chunk_composite_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem);
+        if (e != cudaSuccess) return e;
+        g_c_attr[dev] = true;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    CompParams p;
+    p.gamma = gamma;
+    p.ws_frames = ws + pl.off_frames;
+    p.ws_comp = reinterpret_cast<float *>(ws + pl.off_comp);
+    p.status = status;
+    p.B = pl.B;
+    p.H = pl.H;
+    p.F = pl.F;
+    p.chunk = pl.chunk;
+    p.n_chunks = pl.n_chunks;
+    p.reverse = reverse;
+    kc_chunk_composite_kernel<<<pl.B * pl.H * pl.n_chunks, kCThreads, kCSmem, stream>>>(p);
     return cudaGetLastError();
 }
 

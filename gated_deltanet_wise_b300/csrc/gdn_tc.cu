@@ -76,6 +76,7 @@ struct K1Params {
     unsigned *status;
     int B, H, F, N, chunk, n_chunks;
     float c;
+    int reverse;  // 1: frames are visited from the last to the first
 };
 
 // Tensor memory of K1 (512 columns, fp32 unless noted):
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             int it = 0;
             bool ok = true;
             for (int fl = 0; fl < nf && ok; ++fl) {
-                const int bf = b * p.F + f_begin + fl;
+                const int bf = b * p.F + frame_at(f_begin + fl, p.F, p.reverse);
                 for (int st = 0; st < n_st; ++st, ++it) {
                     const int s = it % kK1Stages, use = it / kK1Stages;
                     if (use >= 1 && !(ok = mbar_wait(&st_empty[s], (use - 1) & 1, abort_flag))) break;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             if (itx >= total) return 0.f;
             const int fl = itx / n_st, n = (itx - fl * n_st) * kTS + r;
             if (n >= p.N) return 0.f;
-            return __ldg(p.beta + ((size_t)b * FN + (size_t)(f_begin + fl) * p.N + n) * p.H + h);
+            return __ldg(p.beta + ((size_t)b * FN + (size_t)frame_at(f_begin + fl, p.F, p.reverse) * p.N + n) * p.H + h);
         };
         float bt_next = load_beta(grpi);
         for (int it = grpi; it < total; it += 2) {
@@ -287,12 +288,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // this warp's rows of the A_f image: rows 32*quad.. of each panel
         const int img_rows = quad == 3 ? kD - 96 : 32;
         const uint32_t img_off = quad * 32 * kRowB;
-        const float *gam = p.gamma + ((size_t)b * p.F + f_begin) * p.H + h;
-        float g_next = __ldg(gam);
+        const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
+        float g_next = __ldg(gam + (size_t)frame_at(f_begin, p.F, p.reverse) * p.H);
         for (int fe = 0; fe < nf && ok; ++fe) {
             const int f = f_begin + fe;
             const float g = g_next;
-            if (fe + 1 < nf) g_next = __ldg(gam + (size_t)(fe + 1) * p.H);
+            if (fe + 1 < nf) g_next = __ldg(gam + (size_t)frame_at(f + 1, p.F, p.reverse) * p.H);
             // this warp's previous A_f bulk stores must have finished reading
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -445,19 +446,22 @@ __global__ void __launch_bounds__(kK1bThreads)
         Srows[rr][cc] = S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
     }
     __syncthreads();
-    if (t == 0 && n_chunks > 0) {
+    // composite steps to apply: without S_out the state after the last chunk is not needed
+    const int steps = S_out ? n_chunks : n_chunks - 1;
+    if (t == 0 && steps > 0) {
         mbar_arrive_expect_tx(&bar[0], (uint32_t)kStateBytes);
         bulk_g2s(Cb0, cC, (uint32_t)kStateBytes, &bar[0]);
     }
-    int issued = n_chunks > 0 ? 1 : 0;
+    int issued = steps > 0 ? 1 : 0;
     for (int c = 0; c < n_chunks; ++c) {
         if (ws_start) {
             float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
             for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
                 dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
         }
+        if (c >= steps) break;
         // the other buffer was last read in step c-1 (closed by the barrier below): refill it
-        if (t == 0 && c + 1 < n_chunks) {
+        if (t == 0 && c + 1 < steps) {
             mbar_arrive_expect_tx(&bar[(c + 1) & 1], (uint32_t)kStateBytes);
             bulk_g2s((c + 1) & 1 ? Cb1 : Cb0, cC + (size_t)(c + 1) * chunk_stride, (uint32_t)kStateBytes,
                      &bar[(c + 1) & 1]);
@@ -501,6 +505,7 @@ struct K2Params {
     float *S_out;  // non-null: the last chunk's CTAs write the chain's final state here
     unsigned *status;
     int B, H, F, N, chunk, n_chunks;
+    int reverse;  // 1: frames are visited from the last to the first
 };
 
 // Named barrier over K2's four output warps (id 0 is __syncthreads).
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             int qc = 0;
             bool ok = true;
             for (int it = 1; it <= nf && ok; ++it) {
-                const int bf = b * p.F + f_begin + it - 1;
+                const int bf = b * p.F + frame_at(f_begin + it - 1, p.F, p.reverse);
                 for (int t = 0; t < n_tiles && ok; ++t, ++qc) {
                     const int s = qc % kK2QStages;
                     if (qc >= kK2QStages && !(ok = mbar_wait(&q_empty[s], (qc / kK2QStages - 1) & 1, abort_flag)))
@@ -685,13 +690,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             if (lane == 0) mbar_arrive(s_ready);
         };
         write_images();
-        const float *gam = p.gamma + ((size_t)b * p.F + f_begin) * p.H + h;
-        float g_next = __ldg(gam);
+        const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
+        float g_next = __ldg(gam + (size_t)frame_at(f_begin, p.F, p.reverse) * p.H);
         for (int it = 0; it < nf; ++it) {
             const float g = g_next;
-            if (it + 1 < nf) g_next = __ldg(gam + (size_t)(it + 1) * p.H);
+            if (it + 1 < nf) g_next = __ldg(gam + (size_t)frame_at(f_begin + it + 1, p.F, p.reverse) * p.H);
             const float4 *U4 = reinterpret_cast<const float4 *>(ws_chain + (size_t)it * kFrameWs + kAimgBytes) + urow;
-            float4 ub[2][4];
+            float4 ub[2][4];  // 16-column chunks of U_f, loaded two ahead of their use
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -748,7 +753,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         int qc = 0;
         bool ok = true;
         for (int it = 1; it <= nf; ++it) {
-            const int bf = b * p.F + f_begin + it - 1;
+            const int bf = b * p.F + frame_at(f_begin + it - 1, p.F, p.reverse);
             for (int t = 0; t < n_tiles; ++t, ++qc) {
                 const int s = qc % kK2QStages, slot = qc % 3;
                 const uint8_t *qs = sm + s * kImgBytes;
@@ -928,7 +933,8 @@ cudaError_t prepare_tc_kernels()
     return cudaSuccess;
 }
 
-K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, float c, uint8_t *ws, unsigned *status)
+K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, float c, int reverse, uint8_t *ws,
+                   unsigned *status)
 {
     K1Params p1;
     p1.beta = beta;
@@ -943,6 +949,7 @@ K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, floa
     p1.chunk = pl.chunk;
     p1.n_chunks = pl.n_chunks;
     p1.c = c;
+    p1.reverse = reverse;
     return p1;
 }
 }  // namespace
@@ -959,7 +966,7 @@ cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float 
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = pl.B * pl.H;
-    const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
+    const K1Params p1 = k1_params(beta, gamma, pl, c, 0, ws, status);
     if ((e = launch_pdl(k1_frame_stats_kernel, dim3(BH), kK1Threads, kK1Smem, stream, mk, mv, p1)) != cudaSuccess)
         return e;
     // the chain's composite is (C, H) back to back in the workspace
@@ -981,34 +988,28 @@ cudaError_t launch_state_compose_tc(const float *S, const float *C, const float 
                       (size_t)kStateFloats, (size_t)0, (float *)nullptr, S, S_out, 1, status);
 }
 
-cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
-                                const float *S_in, float *S_out, void *o, const TcPlan &pl, float c, void *workspace,
-                                unsigned *status, cudaStream_t stream, cudaEvent_t *events)
+// K1b + K2: chunk-boundary states from the chunk composites in the workspace,
+// then the scan/output kernel.  events (optional) get records [2] and [3].
+static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, const float *S_in, float *S_out, void *o,
+                                         const TcPlan &pl, int reverse, uint8_t *ws, unsigned *status,
+                                         cudaStream_t stream, cudaEvent_t *events)
 {
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS) ||
-        !make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
+    CUtensorMap mq, mo;
+    if (!make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
         return cudaErrorInvalidValue;
-    cudaError_t e = prepare_tc_kernels();
-    if (e != cudaSuccess) return e;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = pl.B * pl.H;
-    const K1Params p1 = k1_params(beta, gamma, pl, c, ws, status);
-    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
-    e = launch_pdl(k1_frame_stats_kernel, dim3(BH * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1);
-    if (e != cudaSuccess) return e;
-    if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
-    e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
-                   (const float *)p1.ws_comp, (const float *)(p1.ws_comp + kStateFloats),
-                   (size_t)pl.n_chunks * 2 * kStateFloats, (size_t)2 * kStateFloats,
-                   reinterpret_cast<float *>(ws + pl.off_start), S_in, S_out, pl.n_chunks, status);
+    const float *comp = reinterpret_cast<const float *>(ws + pl.off_comp);
+    cudaError_t e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
+                               comp, comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats,
+                               (size_t)2 * kStateFloats, reinterpret_cast<float *>(ws + pl.off_start), S_in,
+                               (float *)nullptr, pl.n_chunks, status);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
     K2Params p2;
     p2.gamma = gamma;
     p2.ws_frames = ws + pl.off_frames;
     p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
-    p2.S_out = nullptr;  // the boundary kernel has written it
+    p2.S_out = S_out;  // the last chunk's state after its last frame
     p2.status = status;
     p2.B = pl.B;
     p2.H = pl.H;
@@ -1016,47 +1017,45 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     p2.N = pl.N;
     p2.chunk = pl.chunk;
     p2.n_chunks = pl.n_chunks;
+    p2.reverse = reverse;
     e = launch_pdl(k2_scan_output_kernel, dim3(BH * pl.n_chunks), kK2Threads, kK2Smem, stream, mq, mo, p2);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
-// Token-ordered reading: per-frame transitions from the UT-transform kernel
-// (gdn_product.cu) in the workspace format K2 consumes, then K2 over one
-// chunk per chain, starting from S_in (or zero) and writing S_out itself.
-cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void *v, const float *beta,
-                                        const float *gamma, const float *S_in, float *S_out, void *o,
-                                        const TcPlan &pl, float c, void *workspace, unsigned *status,
-                                        cudaStream_t stream)
+cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                                const float *S_in, float *S_out, void *o, const TcPlan &pl, float c, int reverse,
+                                void *workspace, unsigned *status, cudaStream_t stream, cudaEvent_t *events)
 {
-    if (pl.n_chunks != 1) return cudaErrorInvalidValue;
-    CUtensorMap mq, mo;
-    if (!make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
+    CUtensorMap mk, mv;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS))
         return cudaErrorInvalidValue;
     cudaError_t e = prepare_tc_kernels();
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int BH = pl.B * pl.H;
-    if ((e = launch_frame_product_tc(k, v, beta, pl, c, workspace, status, stream)) != cudaSuccess) return e;
-    const float *start = S_in;
-    if (!start) {
-        if ((e = cudaMemsetAsync(ws + pl.off_start, 0, (size_t)BH * kStateBytes, stream)) != cudaSuccess) return e;
-        start = reinterpret_cast<const float *>(ws + pl.off_start);
-    }
-    K2Params p2;
-    p2.gamma = gamma;
-    p2.ws_frames = ws + pl.off_frames;
-    p2.ws_start = start;  // one chunk per chain: [B][H][D][D], the layout of S_in
-    p2.S_out = S_out;
-    p2.status = status;
-    p2.B = pl.B;
-    p2.H = pl.H;
-    p2.F = pl.F;
-    p2.N = pl.N;
-    p2.chunk = pl.chunk;
-    p2.n_chunks = 1;
-    return launch_pdl(k2_scan_output_kernel, dim3(BH), kK2Threads, kK2Smem, stream, mq, mo, p2);
+    const K1Params p1 = k1_params(beta, gamma, pl, c, reverse, ws, status);
+    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
+    e = launch_pdl(k1_frame_stats_kernel, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1);
+    if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
+    return launch_scan_output_tc(q, gamma, S_in, S_out, o, pl, reverse, ws, status, stream, events);
+}
+
+// Token-ordered reading: per-frame transitions from the UT-transform kernel
+// and their chunk composites (gdn_product.cu), in the workspace format the
+// sum reading's frame-statistics kernel produces; then K1b and K2 as there.
+cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void *v, const float *beta,
+                                        const float *gamma, const float *S_in, float *S_out, void *o,
+                                        const TcPlan &pl, float c, int reverse, void *workspace, unsigned *status,
+                                        cudaStream_t stream)
+{
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    if ((e = launch_frame_product_tc(k, v, beta, pl, c, reverse, workspace, status, stream)) != cudaSuccess) return e;
+    if ((e = launch_chunk_composite_tc(gamma, pl, reverse, workspace, status, stream)) != cudaSuccess) return e;
+    return launch_scan_output_tc(q, gamma, S_in, S_out, o, pl, reverse, static_cast<uint8_t *>(workspace), status,
+                                 stream, nullptr);
 }
 
 }  // namespace gdn

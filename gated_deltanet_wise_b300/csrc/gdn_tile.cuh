@@ -30,6 +30,11 @@ constexpr uint32_t kMaxSmem = 232448;                // dynamic shared memory a 
 constexpr uint32_t kIdescMN = idesc_bf16(128, kD, true, true);    // token-contraction GEMMs
 constexpr uint32_t kIdescK = idesc_bf16(128, kD, false, false);   // D-contraction GEMMs
 
+// Frame visited at processing position p: the scan runs over frames in
+// increasing order, or, for the reverse-direction scan, from the last frame
+// to the first.  Per-frame workspace slots are indexed by processing position.
+__host__ __device__ __forceinline__ int frame_at(int p, int F, int reverse) { return reverse ? F - 1 - p : p; }
+
 __device__ __forceinline__ void raise_status(unsigned *status)
 {
     if (status) atomicOr(status, kStatusTimeout);

@@ -33,7 +33,11 @@ EXPORTED = [
     "gdn_frame_step_noalloc_limit_bytes", "gdn_frame_step_noalloc",
     "gdn_frame_composite_workspace_size", "gdn_frame_composite", "gdn_state_compose",
     "gdn_frame_fwd_product_workspace_size", "gdn_frame_fwd_product",
+    "gdn_frame_fwd_ex_workspace_size", "gdn_frame_fwd_ex",
 ]
+
+GDN_FWD_PRODUCT = 1
+GDN_FWD_REVERSE = 2
 
 _lib = None
 
@@ -87,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_fwd_product_workspace_size.argtypes = [I] * 5
         L.gdn_frame_fwd_product.restype = I
         L.gdn_frame_fwd_product.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
+        L.gdn_frame_fwd_ex_workspace_size.restype = Z
+        L.gdn_frame_fwd_ex_workspace_size.argtypes = [I] * 5 + [ctypes.c_uint]
+        L.gdn_frame_fwd_ex.restype = I
+        L.gdn_frame_fwd_ex.argtypes = [P] * 8 + [I] * 5 + [F, ctypes.c_uint, P, Z, P]
         _lib = L
     return _lib
 
@@ -135,6 +143,17 @@ def gdn_frame_fwd_product(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, k
     return int(lib().gdn_frame_fwd_product(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
                                            B, H, F, N, D, float(key_scale), _p(workspace), int(workspace_bytes),
                                            _stream(stream)))
+
+
+def gdn_frame_fwd_ex_workspace_size(B: int, H: int, F: int, N: int, D: int, flags: int) -> int:
+    return int(lib().gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags))
+
+
+def gdn_frame_fwd_ex(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, flags, workspace,
+                     workspace_bytes, stream=None) -> int:
+    return int(lib().gdn_frame_fwd_ex(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
+                                      B, H, F, N, D, float(key_scale), int(flags), _p(workspace),
+                                      int(workspace_bytes), _stream(stream)))
 
 
 def gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, workspace, workspace_bytes,
@@ -279,6 +298,28 @@ def frame_fwd_product(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0
     ws = (workspace or _default_ws).get(nbytes, q.device)
     st = gdn_frame_fwd_product(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, ws, nbytes, stream)
     _check_status(st, "gdn_frame_fwd_product")
+    return o, S_out
+
+
+def frame_fwd_ex(q, k, v, beta, gamma, S_in=None, *, product: bool = False, reverse: bool = False,
+                 key_scale: float = 0.0, o=None, S_out=None, workspace: Optional[Workspace] = None, stream=None):
+    """gdn_frame_fwd_ex: the sum or product reading, forward or reverse frame order."""
+    B, H, F, N, D = _shape(q, gamma)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, torch.bfloat16, n)
+    _check(beta, torch.float32, "beta")
+    _check(gamma, torch.float32, "gamma")
+    if S_in is not None:
+        _check(S_in, torch.float32, "S_in")
+    flags = (GDN_FWD_PRODUCT if product else 0) | (GDN_FWD_REVERSE if reverse else 0)
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device) if S_out is None else S_out
+    nbytes = gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_fwd_ex_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, q.device)
+    st = gdn_frame_fwd_ex(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, flags, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_fwd_ex")
     return o, S_out
 
 

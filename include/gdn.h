@@ -121,6 +121,34 @@ gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v,
                                    gdn_stream_t stream);
 
 /*
+ * Forward with options.  `flags` is a bitwise OR of:
+ *   GDN_FWD_PRODUCT - the token-ordered reading (as gdn_frame_fwd_product);
+ *   GDN_FWD_REVERSE - reverse-direction scan for the bidirectional stage-1
+ *     model (summary page, section 局限与改进, compares the stage-1
+ *     bidirectional model with the chunk-causal one; the CSDN article's §六
+ *     stage 4 derives the streaming variant from the bidirectional model).
+ *     The frames are visited from the last to the
+ *     first: S_F' = S_in, S_f' = S_{f+1}' M_f + U_f for f = F-1 .. 0 (U_f,
+ *     M_f of the chosen reading), o of frame f = S_f' q^, and S_out = S_0'.
+ *     This equals gdn_frame_fwd on the frame-reversed sequence with its
+ *     outputs put back in frame order.  How the two directions' outputs are
+ *     combined is not stated on the pages and is left to the caller.
+ * flags == 0 is gdn_frame_fwd.  Unknown bits return GDN_ERR_INVALID_ARG (and
+ * (size_t)-1 from the size query).  Arguments, layouts, ownership and the
+ * other status codes are those of gdn_frame_fwd; the workspace must hold
+ * gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags) bytes.
+ */
+#define GDN_FWD_PRODUCT 1u
+#define GDN_FWD_REVERSE 2u
+size_t gdn_frame_fwd_ex_workspace_size(int B, int H, int F, int N, int D, unsigned flags);
+gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
+                              const float *beta, const float *gamma,
+                              const float *S_in, float *S_out, void *o,
+                              int B, int H, int F, int N, int D, float key_scale,
+                              unsigned flags, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream);
+
+/*
  * Streaming step: one latent frame (F = 1) per call, state carried by the
  * caller (chunk-causal / autoregressive generation, the chunk-wise variant of
  * the CSDN article's §六 stage 4; resume by passing the previous call's S_out

@@ -72,8 +72,14 @@ def _shapes(q):
     return B, FN, H, D
 
 
+def _flip_frames(x, F):
+    """Reverse the frame order of a [B, F*N, ...] token array (or [B, F, H] per-frame array)."""
+    B, FN = x.shape[:2]
+    return np.ascontiguousarray(x.reshape(B, F, FN // F, *x.shape[2:])[:, ::-1].reshape(x.shape))
+
+
 def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulation="recurrence",
-              mode="sum", sub=64):
+              mode="sum", sub=64, reverse=False):
     """Frame-wise GDN forward in fp64.
 
     Shapes: q, k, v [B, F*N, H, D]; beta [B, F*N, H]; gamma [B, F, H];
@@ -85,7 +91,20 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
     token-ordered reading M_f = gamma_f I - (I - prod_n (I - beta_n k^_n k^_n^T))
     with the frame's tokens applied in order from zero for U_f, computed through
     the UT transform over sub-chunks of ``sub`` tokens.
+
+    ``reverse=True`` is the reverse-direction scan of the bidirectional stage-1
+    model (summary page, section 局限与改进): the frames are visited from the
+    last to the first, starting from S_in, each frame's output read from the
+    state after its own update, and S_out is the state after frame 0.  It is
+    computed literally as the forward scan of the frame-reversed sequence,
+    with the outputs put back in frame order.
     """
+    if reverse:
+        q, k, v, beta, gamma = (_f32(x) for x in (q, k, v, beta, gamma))
+        F = gamma.shape[1]
+        o, S_out = frame_fwd(*(_flip_frames(x, F) for x in (q, k, v, beta, gamma)), S_in, N=N, key_scale=key_scale,
+                             formulation=formulation, mode=mode, sub=sub)
+        return _flip_frames(o, F), S_out
     q, k, v, beta, gamma, S_in = (_f32(x) for x in (q, k, v, beta, gamma, S_in))
     B, FN, H, D = _shapes(q)
     F = gamma.shape[1]

@@ -52,6 +52,14 @@ def test_workspace_sizes(L):
     assert gdn.gdn_frame_fwd_workspace_size(1, 1, 4, 8, 64) == SZ_ERR   # bf16 path is D = 112
     assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 112) == 0   # the fused step needs no scratch
     assert gdn.gdn_frame_step_workspace_size(1, 20, 880, 64) == 2 ** 64 - 1
+    # the options entry: the sum reading matches gdn_frame_fwd, unknown flags are refused
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 0) == \
+        gdn.gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112)
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, gdn.GDN_FWD_REVERSE) == \
+        gdn.gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112)
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, gdn.GDN_FWD_PRODUCT) == \
+        gdn.gdn_frame_fwd_product_workspace_size(1, 20, 121, 880, 112)
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 4) == SZ_ERR
     # the workspace grows linearly in frames (per-frame images dominate)
     a = gdn.gdn_frame_fwd_workspace_size(1, 4, 10, 880, 112)
     b = gdn.gdn_frame_fwd_workspace_size(1, 4, 20, 880, 112)
@@ -79,6 +87,10 @@ def test_host_side_validation_without_gpu(L):
     assert fwd(1, 1, 2, 8, 112, ws=None, nbytes=0) == gdn.GDN_ERR_WORKSPACE
     need = gdn.gdn_frame_fwd_workspace_size(1, 1, 2, 8, 112)
     assert fwd(1, 1, 2, 8, 112, ws=fake, nbytes=need - 16) == gdn.GDN_ERR_WORKSPACE
+    a = args
+    for flags in (4, 8, 0x80000000):
+        assert L.gdn_frame_fwd_ex(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"],
+                                  1, 1, 2, 8, 112, 0.0, flags, fake, need, None) == gdn.GDN_ERR_INVALID_ARG
     assert fwd(1, 1, 2, 8, 112, ws=P(0x10008), nbytes=need) == gdn.GDN_ERR_INVALID_ARG
     def step(B, H, N, D, **over):
         a = dict(args, **over)
