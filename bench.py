@@ -373,16 +373,19 @@ def run_ours(args):
     K, W = args.steps, args.warmup
 
     def step(events=None):
-        st = gdn.gdn_frame_fwd_profiled(x.q, x.k, x.v, x.beta, x.gamma, x.S0, S_out, o, B, H, F, N, D, 0.0,
-                                        ws, nbytes, events, stream)
+        if events is None:  # the public entry point, as a user calls it
+            st = gdn.gdn_frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0, S_out, o, B, H, F, N, D, 0.0,
+                                   ws, nbytes, stream)
+        else:  # same launches with CUDA events between the three kernels
+            st = gdn.gdn_frame_fwd_profiled(x.q, x.k, x.v, x.beta, x.gamma, x.S0, S_out, o, B, H, F, N, D, 0.0,
+                                            ws, nbytes, events, stream)
         if st != gdn.GDN_OK:
             raise gdn.GdnError(st, "gdn_frame_fwd")
 
     for _ in range(W):
         step()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for e in [t0, t1] + [e for row in ev for e in row]:
+    for e in (t0, t1):
         e.record(stream)  # creates the CUDA events outside the timed region
     torch.cuda.synchronize()
     barrier(world)
@@ -390,7 +393,7 @@ def run_ours(args):
     with ClockSampler(dev) as clk:
         t0.record(stream)
         for i in range(K):
-            step(ev[i])
+            step()
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -399,6 +402,17 @@ def run_ours(args):
         raise RuntimeError("device status reports a timed-out wait")
     ms = t0.elapsed_time(t1) / K
     ms_max = max_over_ranks(world, ms)
+    # per-kernel durations: a separate pass with events between the kernels (which
+    # also keeps each kernel from overlapping its neighbour's tail)
+    Kp = max(3, min(K, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kp)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(Kp):
+        step(ev[i])
+    torch.cuda.synchronize()
     stage_ms = [statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(3)]
 
     alg = algorithmic(B, H, F, N, D)
@@ -416,11 +430,13 @@ def run_ours(args):
                 "peak_source": f"{peaks_kind} STREAM-style copy (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": kbytes[dom],
                 "stage_ms": {n: round(t, 5) for n, t in zip(names, stage_ms)},
+                "stage_steps": Kp,
                 "path": {"achieved_gbs": round(alg["total"] / (ms * 1e-3) / 1e9, 1),
                          "frac": round(alg["total"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                          "tflops": round(alg["flops"] / (ms * 1e-3) / 1e12, 2),
                          "tensor_frac": round(alg["flops"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}}
 
+    variants = measure_variants(x, max(3, min(K, 30)), stream, alg, peaks)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(x, K, W, world)
@@ -441,12 +457,50 @@ def run_ours(args):
                            "l2": f"inputs {alg['total'] / 1e9:.2f} GB per step > 126 MB L2; no flush needed",
                            "parallelism": f"replica x{world} (independent chains per rank)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K,
-                "streaming": streaming,
+                "streaming": streaming, "variants": variants,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_variants(x, K, stream, alg, peaks):
+    """The same layer through gdn_frame_fwd_ex: the token-ordered (product) reading
+    and the reverse-direction scan, K back-to-back calls each after 3 warm-ups."""
+    import torch
+    from gated_deltanet_wise_b300 import gdn
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    o = torch.empty_like(x.q)
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=x.q.device)
+    out = {}
+    for name, flags, launches in (("product", gdn.GDN_FWD_PRODUCT, 4), ("reverse", gdn.GDN_FWD_REVERSE, 3)):
+        nb = gdn.gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags)
+        ws = torch.empty(nb, dtype=torch.uint8, device=x.q.device)
+
+        def step():
+            st = gdn.gdn_frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, S_out, o, B, H, F, N, D, 0.0, flags,
+                                      ws, nb, stream)
+            if st != gdn.GDN_OK:
+                raise gdn.GdnError(st, "gdn_frame_fwd_ex")
+
+        for _ in range(3):
+            step()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(K):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if gdn.gdn_device_status() != gdn.GDN_OK:
+            raise RuntimeError("device status reports a timed-out wait")
+        ms = t0.elapsed_time(t1) / K
+        out[name] = {"ms_per_step": round(ms, 5), "tokens_per_s": round(B * F * N / (ms * 1e-3), 1),
+                     "path_frac_hbm": round(alg["total"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "steps": K, "gpu_launches_per_step": launches}
+        del ws
+    return out
 
 
 def run_e2e(x, K, W, world):
