@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK1OffBar);
     uint64_t *st_full = bars + 0, *st_prep = bars + kK1Stages, *st_empty = bars + 2 * kK1Stages;
     uint64_t *acc_full = bars + 3 * kK1Stages, *comp_ready = acc_full + 1, *comp_done = acc_full + 2;
-    uint64_t *drain = acc_full + 3, *grp = acc_full + 4;
+    uint64_t *drain = acc_full + 3;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(acc_full + 6);
 
@@ -119,7 +119,6 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         mbar_init(comp_ready, 4);
         mbar_init(comp_done, 1);
         mbar_init(drain, 1);
-        mbar_init(grp, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -166,9 +165,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             int it = 0;
             bool ok = true;
             for (int fl = 0; fl < nf && ok; ++fl) {
-                // the previous frame's composite MMAs read their A operands from the
-                // acc_A columns: they must finish before this frame accumulates there
-                if (fl >= 1 && !(ok = mbar_wait(comp_done, (fl - 1) & 1, abort_flag))) break;
+                // The previous frame's composite MMAs read their A operands from the
+                // acc_A columns that this frame's first MMA overwrites: tcgen05.mma
+                // operations issued by one thread execute in issue order, so no wait.
                 for (int st = 0; st < n_st && ok; ++st, ++it) {
                     const int s = it % kK1Stages, use = it / kK1Stages;
                     if (!(ok = mbar_wait(&st_prep[s], use & 1, abort_flag))) break;
@@ -270,7 +269,6 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        int grp_phase = 0;
         bool ok = true;
         // composites start at C = I, H = 0 (rows 112..127 stay zero)
 #pragma unroll
@@ -328,14 +326,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
             }
-            // all four warps have read acc_A before any writes the composite
-            // images over those columns
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(grp);
-            if (!(ok = mbar_wait_warp(grp, grp_phase & 1, abort_flag))) break;
-            ++grp_phase;
-            tc_fence_after();
+            // pass 2 overwrites acc_A's columns with the composite images: each warp
+            // touches only its own TMEM lanes, and has read all of them above
             // pass 2: H <- gamma H + U_f, C <- gamma C; A operands -bf16(H_prev), -bf16(C_prev)
 #pragma unroll
             for (int cc = 0; cc < 7; ++cc) {

@@ -123,3 +123,10 @@ def test_workspace_and_degenerate_sizes():
     assert st == gdn.GDN_OK
     torch.cuda.synchronize()
     torch.testing.assert_close(S, x.S0 * x.gamma.prod(1)[:, :, None, None], rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("key_scale", [0.0, 1.0])
+def test_long_frames_cfg_batch(key_scale):
+    """Frames of 3520 tokens (55 sub-chunks each) with B=2, the longest frame of the CFG sweep."""
+    x = make_inputs(2, 3, 6, 3520, 112, dtype="bf16", seed=23, device=DEV, s0_std=0.1)
+    _check(x, key_scale, S_in=x.S0)
