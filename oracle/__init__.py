@@ -48,6 +48,7 @@ def _load():
         lib.oracle_gdn_frame_transitions.argtypes = [P] * 4 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_fwd_product.argtypes = [P] * 6 + [I] * 5 + [Dbl, I, P, P]
         lib.oracle_gdn_frame_transitions_product.argtypes = [P] * 4 + [I] * 5 + [Dbl, I, P, P]
+        lib.oracle_gdn_frame_bwd.argtypes = [P] * 8 + [I] * 5 + [Dbl] + [P] * 6
         lib.oracle_gdn_composite.argtypes = [P, P, I, I, P, P]
         lib.oracle_gdn_compose.argtypes = [P, P, P, P, I, P, P]
         lib.oracle_num_threads.restype = I
@@ -146,6 +147,29 @@ def frame_transitions(k, v, beta, gamma, key_scale=0.0, mode="sum", sub=64):
     _load().oracle_gdn_frame_transitions(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),
                                          B, H, F, N, D, float(key_scale), _ptr(M), _ptr(U))
     return M, U
+
+
+def frame_bwd(q, k, v, beta, gamma, S_in, dO, dS_out=None, key_scale=0.0):
+    """Backward pass of the sum reading in fp64 (gradients by the chain rule through
+    the printed recurrence; see oracle_gdn_frame_bwd in gdn_oracle.c).
+
+    dO [B, F*N, H, D] is dL/do, dS_out [B, H, D, D] is dL/dS_out (None: zero).
+    Returns (dq, dk, dv [B, F*N, H, D], dbeta [B, F*N, H], dgamma [B, F, H], dS_in [B, H, D, D]), fp64.
+    """
+    q, k, v, beta, gamma, S_in, dO, dS_out = (_f32(x) for x in (q, k, v, beta, gamma, S_in, dO, dS_out))
+    B, FN, H, D = _shapes(q)
+    F = gamma.shape[1]
+    N = FN // F if F else 0
+    dq = np.zeros((B, FN, H, D), np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    dbeta = np.zeros((B, FN, H), np.float64)
+    dgamma = np.zeros((B, F, H), np.float64)
+    dS_in = np.zeros((B, H, D, D), np.float64)
+    _load().oracle_gdn_frame_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(S_in), _ptr(dO),
+                                 _ptr(dS_out), B, H, F, N, D, float(key_scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(dbeta), _ptr(dgamma), _ptr(dS_in))
+    return dq, dk, dv, dbeta, dgamma, dS_in
 
 
 def composite(M, U):

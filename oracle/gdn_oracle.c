@@ -417,6 +417,130 @@ void oracle_gdn_frame_fwd_product(const float *q, const float *k, const float *v
     }
 }
 
+/*
+ * Backward pass of the sum reading (training, the CSDN article's §六: the layer
+ * is trained end to end; the gradients follow from the forward recurrence by
+ * the chain rule).  With upstream gradients dO = dL/do and dS_out = dL/dS_out
+ * (either may be NULL: zero), per chain:
+ *   G_f = dL/dS_f:  G_{F-1} = dS_out + E_{F-1},  G_{f-1} = G_f M_f^T + E_{f-1},
+ *                   E_f = sum_{n in f} do_n q^_n^T;   dS_in = G_0 M_0^T
+ *   dL/dM_f = S_{f-1}^T G_f,  dL/dU_f = G_f,  dgamma_f = trace(S_{f-1}^T G_f),
+ *   dA_f = -S_{f-1}^T G_f,
+ *   dk^_n = beta_n (dA_f + dA_f^T) k^_n + beta_n G_f^T v_n,   dv_n = beta_n G_f k^_n,
+ *   dbeta_n = k^_n^T dA_f k^_n + v_n^T G_f k^_n,   dq^_n = S_f^T do_n,
+ *   k^ = c k / r:  dk = (c / r) (dk^ - k (k . dk^) / r^2);   q^ = q / rho likewise (c = 1).
+ * r and rho include the same epsilon as the forward.  Outputs are fp64, in the
+ * input layouts: dq, dk, dv [B][F*N][H][D], dbeta [B][F*N][H], dgamma [B][F][H],
+ * dS_in [B][H][D][D].
+ */
+void oracle_gdn_frame_bwd(const float *q, const float *k, const float *v,
+                          const float *beta, const float *gamma, const float *S_in,
+                          const float *dO, const float *dS_out,
+                          int B, int H, int F, int N, int D, double key_scale,
+                          double *dq, double *dk, double *dv, double *dbeta,
+                          double *dgamma, double *dS_in)
+{
+    double c = oracle_key_scale(key_scale, D, N);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * H; ++bh) {
+        int b = bh / H, h = bh % H;
+        size_t DD = (size_t)D * D;
+        double *S = malloc(sizeof(double) * DD * (F + 1));   /* S_{-1} .. S_{F-1} */
+        double *M = malloc(sizeof(double) * DD * (F > 0 ? F : 1));
+        double *U = malloc(sizeof(double) * DD);
+        double *G = malloc(sizeof(double) * DD);
+        double *Gn = malloc(sizeof(double) * DD);
+        double *dA = malloc(sizeof(double) * DD);
+        double *kh = malloc(sizeof(double) * D);
+        double *qh = malloc(sizeof(double) * D);
+        double *t1 = malloc(sizeof(double) * D);
+        load_state(S_in, b, h, H, D, S);
+        for (int f = 0; f < F; ++f) {   /* forward, keeping every state */
+            frame_transition(k, v, beta, gamma, b, h, f, H, F, N, D, c, M + f * DD, U, kh);
+            matmul(S + f * DD, M + f * DD, S + (f + 1) * DD, D);
+            for (size_t e = 0; e < DD; ++e) S[(f + 1) * DD + e] += U[e];
+        }
+        /* G_{F-1} starts from dS_out */
+        for (size_t e = 0; e < DD; ++e)
+            G[e] = dS_out ? (double)dS_out[((size_t)b * H + h) * DD + e] : 0.0;
+        for (int f = F - 1; f >= 0; --f) {
+            const double *Sp = S + f * DD, *Sf = S + (f + 1) * DD;   /* S_{f-1}, S_f */
+            /* G_f += E_f (this frame's outputs read S_f) */
+            for (int n = 0; n < N; ++n) {
+                size_t base = tok_index(b, f, n, h, 0, F, N, H, D);
+                normalise(q + base, D, 1.0, qh);
+                for (int i = 0; i < D; ++i) {
+                    double di = dO ? (double)dO[base + i] : 0.0;
+                    for (int j = 0; j < D; ++j) G[i * D + j] += di * qh[j];
+                }
+            }
+            /* dA_f = -S_{f-1}^T G_f;  dgamma_f = trace(S_{f-1}^T G_f) */
+            double tr = 0.0;
+            for (int i = 0; i < D; ++i)
+                for (int j = 0; j < D; ++j) {
+                    double sacc = 0.0;
+                    for (int l = 0; l < D; ++l) sacc += Sp[l * D + i] * G[l * D + j];
+                    dA[i * D + j] = -sacc;
+                    if (i == j) tr += sacc;
+                }
+            dgamma[((size_t)b * F + f) * H + h] = tr;
+            /* token gradients of frame f */
+            for (int n = 0; n < N; ++n) {
+                size_t base = tok_index(b, f, n, h, 0, F, N, H, D);
+                size_t bi = beta_index(b, f, n, h, F, N, H);
+                const float *kn = k + base, *vn = v + base, *qn = q + base;
+                double bn = beta[bi];
+                normalise(kn, D, c, kh);
+                /* dk^ = beta ((dA + dA^T) k^ + G^T v);  dbeta = k^ dA k^ + v G k^;  dv = beta G k^ */
+                double db = 0.0;
+                for (int i = 0; i < D; ++i) {
+                    double a = 0.0, gv = 0.0, gk = 0.0, ak = 0.0;
+                    for (int j = 0; j < D; ++j) {
+                        a += (dA[i * D + j] + dA[j * D + i]) * kh[j];
+                        gv += G[j * D + i] * (double)vn[j];
+                        gk += G[i * D + j] * kh[j];
+                        ak += dA[i * D + j] * kh[j];
+                    }
+                    t1[i] = bn * (a + gv);
+                    dv[base + i] = bn * gk;
+                    db += kh[i] * ak + (double)vn[i] * gk;
+                }
+                dbeta[bi] = db;
+                /* through k^ = c k / r */
+                double ss = 0.0, kd = 0.0;
+                for (int i = 0; i < D; ++i) {
+                    ss += (double)kn[i] * kn[i];
+                    kd += (double)kn[i] * t1[i];
+                }
+                double r2 = ss + ORACLE_NORM_EPS, r = sqrt(r2);
+                for (int i = 0; i < D; ++i) dk[base + i] = c / r * (t1[i] - (double)kn[i] * kd / r2);
+                /* dq^ = S_f^T do;  through q^ = q / rho */
+                double qs = 0.0, qd = 0.0;
+                for (int j = 0; j < D; ++j) {
+                    double sacc = 0.0;
+                    for (int i = 0; i < D; ++i) sacc += Sf[i * D + j] * (dO ? (double)dO[base + i] : 0.0);
+                    t1[j] = sacc;
+                    qs += (double)qn[j] * qn[j];
+                    qd += (double)qn[j] * sacc;
+                }
+                double p2 = qs + ORACLE_NORM_EPS, rho = sqrt(p2);
+                for (int j = 0; j < D; ++j) dq[base + j] = (t1[j] - (double)qn[j] * qd / p2) / rho;
+            }
+            /* G_{f-1} = G_f M_f^T */
+            const double *Mf = M + f * DD;
+            for (int i = 0; i < D; ++i)
+                for (int j = 0; j < D; ++j) {
+                    double sacc = 0.0;
+                    for (int l = 0; l < D; ++l) sacc += G[i * D + l] * Mf[j * D + l];
+                    Gn[i * D + j] = sacc;
+                }
+            memcpy(G, Gn, sizeof(double) * DD);
+        }
+        if (dS_in) memcpy(dS_in + ((size_t)b * H + h) * DD, G, sizeof(double) * DD);
+        free(S); free(M); free(U); free(G); free(Gn); free(dA); free(kh); free(qh); free(t1);
+    }
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
