@@ -171,6 +171,49 @@ gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v,
                           workspace_bytes, stream, events);
 }
 
+size_t gdn_frame_bwd_workspace_size(int B, int H, int F, int N, int D)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
+    if (B == 0 || H == 0 || F == 0) return 0;
+    if (D != 112 || N == 0) return (size_t)-1;
+    return bwd_workspace_bytes(B, H, F, N);
+}
+
+gdn_status_t gdn_frame_bwd(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
+                           const float *S_in, const void *dO, const float *dS_out, float *dq, float *dk, float *dv,
+                           float *dbeta, float *dgamma, float *dS_in, int B, int H, int F, int N, int D,
+                           float key_scale, void *workspace, size_t workspace_bytes, gdn_stream_t stream)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t state_bytes = (size_t)B * H * D * D * sizeof(float);
+    if ((S_in && !aligned(S_in, 16)) || (dS_out && !aligned(dS_out, 16)) || (dS_in && !aligned(dS_in, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if (F == 0) {  // no frames: S_out = S_in
+        if (!dS_in) return GDN_OK;
+        cudaError_t e = dS_out ? cudaMemcpyAsync(dS_in, dS_out, state_bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(dS_in, 0, state_bytes, st);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (N == 0) return GDN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !beta || !gamma || !dO || !dq || !dk || !dv || !dbeta || !dgamma) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dO, 16) || !aligned(dq, 16) ||
+        !aligned(dk, 16) || !aligned(dv, 16) || !aligned(beta, 4) || !aligned(gamma, 4) || !aligned(dbeta, 4) ||
+        !aligned(dgamma, 4))
+        return GDN_ERR_INVALID_ARG;
+    const size_t need = bwd_workspace_bytes(B, H, F, N);
+    if (need == (size_t)-1) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    cudaError_t e = launch_frame_bwd_tc(q, k, v, beta, gamma, S_in, dO, dS_out, dq, dk, dv, dbeta, dgamma, dS_in, B,
+                                        H, F, N, default_key_scale(key_scale, D, N), workspace, status, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 // Device staging of the host-buffer form: q, k, v, o (bf16), beta, gamma,
 // S_in, S_out (fp32), then the workspace, each 256-byte aligned.
 struct HostLayout {

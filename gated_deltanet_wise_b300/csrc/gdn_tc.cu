@@ -980,6 +980,21 @@ cudaError_t launch_state_compose_tc(const float *S, const float *C, const float 
                       (size_t)kStateFloats, (size_t)0, (float *)nullptr, S, S_out, 1, status);
 }
 
+// K1 alone over a plan: per-frame A_f image and U_f (and chunk composites) in the workspace.
+cudaError_t launch_frame_stats_tc(const void *k, const void *v, const float *beta, const float *gamma,
+                                  const TcPlan &pl, float c, int reverse, void *workspace, unsigned *status,
+                                  cudaStream_t stream)
+{
+    CUtensorMap mk, mv;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS))
+        return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    const K1Params p1 = k1_params(beta, gamma, pl, c, reverse, static_cast<uint8_t *>(workspace), status);
+    return launch_pdl(k1_frame_stats_kernel, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv,
+                      p1);
+}
+
 // K1b + K2: chunk-boundary states from the chunk composites in the workspace,
 // then the scan/output kernel.  events (optional) get records [2] and [3].
 static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, const float *S_in, float *S_out, void *o,

@@ -34,6 +34,7 @@ EXPORTED = [
     "gdn_frame_composite_workspace_size", "gdn_frame_composite", "gdn_state_compose",
     "gdn_frame_fwd_product_workspace_size", "gdn_frame_fwd_product",
     "gdn_frame_fwd_ex_workspace_size", "gdn_frame_fwd_ex",
+    "gdn_frame_bwd_workspace_size", "gdn_frame_bwd",
 ]
 
 GDN_FWD_PRODUCT = 1
@@ -95,6 +96,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_fwd_ex_workspace_size.argtypes = [I] * 5 + [ctypes.c_uint]
         L.gdn_frame_fwd_ex.restype = I
         L.gdn_frame_fwd_ex.argtypes = [P] * 8 + [I] * 5 + [F, ctypes.c_uint, P, Z, P]
+        L.gdn_frame_bwd_workspace_size.restype = Z
+        L.gdn_frame_bwd_workspace_size.argtypes = [I] * 5
+        L.gdn_frame_bwd.restype = I
+        L.gdn_frame_bwd.argtypes = [P] * 14 + [I] * 5 + [F, P, Z, P]
         _lib = L
     return _lib
 
@@ -154,6 +159,17 @@ def gdn_frame_fwd_ex(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_sc
     return int(lib().gdn_frame_fwd_ex(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out), _p(o),
                                       B, H, F, N, D, float(key_scale), int(flags), _p(workspace),
                                       int(workspace_bytes), _stream(stream)))
+
+
+def gdn_frame_bwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
+    return int(lib().gdn_frame_bwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_frame_bwd(q, k, v, beta, gamma, S_in, dO, dS_out, dq, dk, dv, dbeta, dgamma, dS_in, B, H, F, N, D,
+                  key_scale, workspace, workspace_bytes, stream=None) -> int:
+    return int(lib().gdn_frame_bwd(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(dO), _p(dS_out),
+                                   _p(dq), _p(dk), _p(dv), _p(dbeta), _p(dgamma), _p(dS_in), B, H, F, N, D,
+                                   float(key_scale), _p(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def gdn_frame_step(q, k, v, beta, gamma, S_in, S_out, o, B, H, N, D, key_scale, workspace, workspace_bytes,
@@ -321,6 +337,34 @@ def frame_fwd_ex(q, k, v, beta, gamma, S_in=None, *, product: bool = False, reve
     st = gdn_frame_fwd_ex(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, flags, ws, nbytes, stream)
     _check_status(st, "gdn_frame_fwd_ex")
     return o, S_out
+
+
+def frame_bwd(q, k, v, beta, gamma, S_in, dO, dS_out=None, *, key_scale: float = 0.0,
+              workspace: Optional[Workspace] = None, stream=None):
+    """gdn_frame_bwd: returns (dq, dk, dv, dbeta, dgamma, dS_in), fp32."""
+    B, H, F, N, D = _shape(q, gamma)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO")):
+        _check(t, torch.bfloat16, n)
+    _check(beta, torch.float32, "beta")
+    _check(gamma, torch.float32, "gamma")
+    for t, n in ((S_in, "S_in"), (dS_out, "dS_out")):
+        if t is not None:
+            _check(t, torch.float32, n)
+    dev = q.device
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dbeta = torch.empty(beta.shape, dtype=torch.float32, device=dev)
+    dgamma = torch.empty(gamma.shape, dtype=torch.float32, device=dev)
+    dS_in = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
+    nbytes = gdn_frame_bwd_workspace_size(B, H, F, N, D)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_bwd_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, dev)
+    st = gdn_frame_bwd(q, k, v, beta, gamma, S_in, dO, dS_out, dq, dk, dv, dbeta, dgamma, dS_in, B, H, F, N, D,
+                       key_scale, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_bwd")
+    return dq, dk, dv, dbeta, dgamma, dS_in
 
 
 def frame_step(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, o=None, S_out=None,

@@ -149,6 +149,30 @@ gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
                               gdn_stream_t stream);
 
 /*
+ * Backward pass of gdn_frame_fwd (the sum reading), for training (the CSDN
+ * article's §六: the layer is trained end to end).  Given dO = dL/do (bf16,
+ * layout of o) and dS_out = dL/dS_out (fp32 [B][H][D][D], NULL: zero), writes
+ *   dq, dk, dv : fp32 [B][F*N][H][D]      dbeta  : fp32 [B][F*N][H]
+ *   dgamma     : fp32 [B][F][H]           dS_in  : fp32 [B][H][D][D] (may be NULL)
+ * for the same q, k, v, beta, gamma, S_in (NULL: zero) and key_scale as the
+ * forward.  It recomputes the forward states; nothing from a forward call is
+ * kept.  Workspace: gdn_frame_bwd_workspace_size(B,H,F,N,D) bytes, 256-byte
+ * aligned (about 4.9 GB for B=1, H=20, F=121, N=880: the per-frame states,
+ * the gradient states and four fp32 token-row intermediates).  F = 0 copies
+ * dS_out to dS_in; N = 0 with F > 0 returns GDN_ERR_UNSUPPORTED; D != 112
+ * returns GDN_ERR_UNSUPPORTED.  Gradients match the fp64 chain rule (itself
+ * checked against finite differences) within a relative Frobenius error of
+ * 5e-3 per tensor for inputs drawn as in the tests.
+ */
+size_t gdn_frame_bwd_workspace_size(int B, int H, int F, int N, int D);
+gdn_status_t gdn_frame_bwd(const void *q, const void *k, const void *v,
+                           const float *beta, const float *gamma, const float *S_in,
+                           const void *dO, const float *dS_out,
+                           float *dq, float *dk, float *dv, float *dbeta, float *dgamma,
+                           float *dS_in, int B, int H, int F, int N, int D, float key_scale,
+                           void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
  * Streaming step: one latent frame (F = 1) per call, state carried by the
  * caller (chunk-causal / autoregressive generation, the chunk-wise variant of
  * the CSDN article's §六 stage 4; resume by passing the previous call's S_out
