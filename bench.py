@@ -500,7 +500,52 @@ def measure_variants(x, K, stream, alg, peaks):
                      "path_frac_hbm": round(alg["total"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                      "steps": K, "gpu_launches_per_step": launches}
         del ws
+    out["backward"] = measure_backward(x, max(3, min(K, 10)), stream, peaks)
     return out
+
+
+def measure_backward(x, K, stream, peaks):
+    """gdn_frame_bwd on the same layer (dO ~ N(0,1) in bf16, dS_out = 0), K calls after 2 warm-ups.
+    Algorithmic bytes: q, k, v, dO read (bf16), beta and gamma read, dq, dk, dv written (fp32),
+    dbeta and dgamma written (fp32)."""
+    import torch
+    from gated_deltanet_wise_b300 import gdn
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    dev = x.q.device
+    g = torch.Generator(device=dev).manual_seed(1)
+    dO = torch.randn(x.q.shape, generator=g, device=dev).to(torch.bfloat16)
+    dq = torch.empty(x.q.shape, dtype=torch.float32, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+    dbeta = torch.empty(x.beta.shape, dtype=torch.float32, device=dev)
+    dgamma = torch.empty(x.gamma.shape, dtype=torch.float32, device=dev)
+    dS_in = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
+    nb = gdn.gdn_frame_bwd_workspace_size(B, H, F, N, D)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = gdn.gdn_frame_bwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0, dO, None, dq, dk, dv, dbeta, dgamma, dS_in,
+                               B, H, F, N, D, 0.0, ws, nb, stream)
+        if st != gdn.GDN_OK:
+            raise gdn.GdnError(st, "gdn_frame_bwd")
+
+    for _ in range(2):
+        step()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    ms = t0.elapsed_time(t1) / K
+    tok = B * F * N * H * D
+    alg = 4 * tok * 2 + 3 * tok * 4 + 2 * B * F * N * H * 4 + 2 * B * F * H * 4
+    del ws
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(B * F * N / (ms * 1e-3), 1),
+            "algorithmic_bytes": alg, "path_frac_hbm": round(alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "steps": K, "gpu_launches_per_step": 12, "workspace_bytes": nb}
 
 
 def run_e2e(x, K, W, world):

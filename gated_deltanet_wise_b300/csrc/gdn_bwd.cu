@@ -12,20 +12,20 @@
 //   dbeta_n = k^^T dA k^ + v^T G k^,  then through the two normalisations.
 //
 // The path reuses the forward kernels and adds three:
-//   1. K1 on (k, v): A_f images and U_f in a workspace; the state chain kernel
-//      from S_in stores every S_f.
+//   1. K1 on (k, v): A_f images, U_f and chunk composites in a workspace; the
+//      chunk-boundary kernel and the scan kernel without outputs, from S_in,
+//      store every S_f.
 //   2. K1 on (k := q, v := dO, beta := 1, c := 1): its U_f slots are E_f.
 //   3. kb_build_reverse_ws lays out the reverse scan: slot p holds A of frame
-//      F - p (none for p = 0) and E_{F-1-p} (none for p = F), gamma likewise, so
-//      that the state chain kernel from dS_out visits G_{F-1}, ..., G_0 and
-//      ends at dS_in.
+//      F - p (none for p = 0) and E_{F-1-p} (none for p = F), gamma likewise;
+//      its chunk composites (K1c), the chunk-boundary kernel and the scan
+//      kernel without outputs, from dS_out, visit G_{F-1}, ..., G_0 and end at
+//      dS_in.
 //   4. kb_frame_grad: dM_f = S_{f-1}^T G_f (fp32 CUDA cores), dgamma_f, and
 //      Dsym_f = dA_f + dA_f^T.
-//   5. kt_token_matrix_kernel (tcgen05): for every token row x_t of a frame,
-//      x_t^T W_f with W_f one of S_f, Dsym_f, G_f, G_f^T (hi + lo bf16 images),
-//      rows scaled by c / ||k_t|| where the row is k: dq^, k^^T Dsym, v^T G,
-//      k^^T G^T, fp32.
-//   6. kb_finalize: dk^, dv, dbeta, then dk and dq through the normalisations.
+//   5. kg_token_grad_kernel (tcgen05), twice: dO S_f, with q's normalisation
+//      Jacobian in the epilogue, gives dq; k Dsym_f, v G_f and k G_f^T (one G
+//      image read K-major and MN-major), with k's, give dk, dv and dbeta.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -128,36 +128,48 @@ __global__ void __launch_bounds__(256) kb_frame_grad(const float *S_in, const fl
     if (threadIdx.x == 0) dgamma[((size_t)b * F + f) * H + h] = *tr;
 }
 
-// ------------------------------------------------------- token x matrix GEMM
-// out[t][j] = scale_t sum_i x[t][i] W[i][j] for every token t of frame f and
-// chain bh, W = W_base[bh][slot(f)] (fp32 D x D), slot(f) = w_rev ? F - 1 - f : f
-// over w_slots slots per chain; w_rows: use W^T instead (the image rows are W's
-// rows).  norm_c > 0: scale_t = norm_c / ||x_t||, else 1.  One CTA per (frame,
-// chain): four warps build W's hi/lo bf16 images once, then 128-token x tiles
-// stream through TMA (two stages) into tcgen05 GEMMs (two TMEM slots), and four
-// warps write the fp32 rows.
-constexpr int kTThreads = 320;
-constexpr uint32_t kTOffX = 0;                            // two x stages, 32 KB each
-constexpr uint32_t kTOffWhi = 2 * kImgBytes;              // 65536
-constexpr uint32_t kTOffWlo = kTOffWhi + kImgBytes;       // 98304
-constexpr uint32_t kTOffBar = kTOffWlo + kImgBytes;       // 131072
-constexpr uint32_t kTSmem = kTOffBar + 256 + 1024;
+// ------------------------------------------------ token-row gradient kernels
+// One CTA per (frame, chain), 128-token tiles of the frame's rows through TMA
+// into tcgen05 GEMMs against per-frame fp32 matrices given as hi + lo bf16
+// images (image row j = column j of the matrix, K-major); the epilogue (thread
+// = token row) applies the chain rule through the normalisations and writes
+// the final fp32 gradients.
+//   kMode 0: acc = dO W (W = S_f)  ->  dq^ = S_f^T do;  dq = (dq^ - q (q.dq^)/rho^2) / rho
+//            two stages of (dO, q) tiles, two accumulator slots.
+//   kMode 1: acc0 = k Dsym, acc1 = v G, acc2 = k G^T (the G image read MN-major:
+//            row j, column i holds G[i][j], which is B[n = i][k = j] = G[i][j]);
+//            with k^ = (c/r) k: dk^ = beta ((c/r) acc0 + acc1),
+//            dk = (c/r)(dk^ - k (k.dk^)/r^2),  dv = beta (c/r) acc2,
+//            dbeta = 1/2 (c/r)^2 k.acc0 + (c/r) k.acc1;  one stage of (k, v).
+constexpr int kGThreads = 320;                    // producer, MMA, 4 image warps, 4 output warps
+constexpr uint32_t kGOffImg = 0;  // W0 hi, W0 lo (, W1 hi, W1 lo), 32 KB each; then the (x0, x1) tile stages
+// mode 0: 2 images + 2 stages x 2 tiles; mode 1: 4 images + 1 stage x 2 tiles: both 196,608 B
+constexpr uint32_t kGOffBar = 6 * kImgBytes;
+constexpr uint32_t kGSmem = kGOffBar + 256 + 1024;
+static_assert(kGSmem <= kMaxSmem, "token-gradient kernel shared memory");
+constexpr uint32_t kIdescKMN = idesc_bf16(128, kD, false, true);
 
-struct TokMatParams {
-    const float *W;
-    float *out;  // [B][F*N][H][D] fp32
+struct TokGradParams {
+    const float *W0, *W1;   // mode 0: S states [BH][F]; mode 1: Dsym [BH][F], G states [BH][F+1] (G_f at F-1-f)
+    const float *beta;
+    float *g0, *g1, *g_beta;  // mode 0: dq; mode 1: dk, dv, dbeta
     unsigned *status;
     int B, H, F, N;
-    int w_slots, w_rev, w_rows;
-    float norm_c;
+    float c;
 };
 
-__global__ void __launch_bounds__(kTThreads, 1)
-    kt_token_matrix_kernel(const __grid_constant__ CUtensorMap mapX, const TokMatParams p)
+template <int kMode>
+__global__ void __launch_bounds__(kGThreads, 1)
+    kg_token_grad_kernel(const __grid_constant__ CUtensorMap mapX0, const __grid_constant__ CUtensorMap mapX1,
+                         const TokGradParams p)
 {
+    constexpr int kStages = kMode == 0 ? 2 : 1;
+    constexpr int kAcc = kMode == 0 ? 1 : 3;       // accumulators per tile
+    constexpr uint32_t kOffBar = kGOffBar;
+    constexpr uint32_t kOffX = kMode == 0 ? 2 * kImgBytes : 4 * kImgBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTOffBar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint64_t *x_full = bars + 0, *x_empty = bars + 2, *acc_full = bars + 4, *acc_free = bars + 6;
     uint64_t *img_ready = bars + 8, *drain = bars + 9;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
@@ -171,9 +183,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int n_tiles = (p.N + 127) / 128;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 5);  // the tile's MMAs + the four output warps (norms read)
+            mbar_init(&x_empty[i], 5);  // the tile's MMAs + the four output warps (epilogue reads x1 / x0)
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_free[i], 4);
         }
@@ -183,7 +195,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -191,24 +203,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
+    auto xtile = [&](int s, int which) { return kOffX + (uint32_t)(2 * s + which) * kImgBytes; };
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
-                const int s = t & 1;
-                if (t >= 2 && !mbar_wait(&x_empty[s], ((t >> 1) - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&x_full[s], kImgBytes);
-                uint8_t *dst = sm + kTOffX + s * kImgBytes;
-                tma_load_4d(dst, &mapX, &x_full[s], 0, h, t * 128, bf, pol);
-                tma_load_4d(dst + kImgPanel, &mapX, &x_full[s], 64, h, t * 128, bf, pol);
+                const int s = t % kStages, u = t / kStages;
+                if (u >= 1 && !mbar_wait(&x_empty[s], (u - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&x_full[s], 2 * kImgBytes);
+                for (int w = 0; w < 2; ++w) {
+                    uint8_t *dst = sm + xtile(s, w);
+                    const CUtensorMap *m = w ? &mapX1 : &mapX0;
+                    tma_load_4d(dst, m, &x_full[s], 0, h, t * 128, bf, pol);
+                    tma_load_4d(dst + kImgPanel, m, &x_full[s], 64, h, t * 128, bf, pol);
+                }
                 ++issued;
             }
             if (*abort_flag)
-                for (int s = 0; s < 2 && s < issued; ++s) {
-                    const int last = ((issued - 1 - s) / 2) * 2 + s;
-                    mbar_wait_drain(&x_full[s], (last >> 1) & 1);
+                for (int s = 0; s < kStages && s < issued; ++s) {
+                    const int last = ((issued - 1 - s) / kStages) * kStages + s;
+                    mbar_wait_drain(&x_full[s], (last / kStages) & 1);
                 }
         }
     } else if (warp == 1) {
@@ -216,17 +232,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
             bool ok = mbar_wait(img_ready, 0, abort_flag);
             tc_fence_after();
             for (int t = 0; t < n_tiles && ok; ++t) {
-                const int s = t & 1;
-                if (!(ok = mbar_wait(&x_full[s], (t >> 1) & 1, abort_flag))) break;
-                if (t >= 2 && !(ok = mbar_wait(&acc_free[s], ((t >> 1) - 1) & 1, abort_flag))) break;
+                const int s = t % kStages, u = t / kStages;
+                if (!(ok = mbar_wait(&x_full[s], u & 1, abort_flag))) break;
+                if (u >= 1 && !(ok = mbar_wait(&acc_free[s], (u - 1) & 1, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t xb = sbase + kTOffX + s * kImgBytes;
+                const uint32_t x0 = sbase + xtile(s, 0), x1 = sbase + xtile(s, 1);
+                const uint32_t acc = tmem + 128 * kAcc * s;
 #pragma unroll
                 for (int ks = 0; ks < 7; ++ks) {
                     const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(xb + koff, 16, 1024);
-                    mma_bf16(tmem + 128 * s, ad, sdesc_sw128(sbase + kTOffWhi + koff, 16, 1024), kIdescK, ks > 0);
-                    mma_bf16(tmem + 128 * s, ad, sdesc_sw128(sbase + kTOffWlo + koff, 16, 1024), kIdescK, 1u);
+                    const uint32_t w0 = sbase + kGOffImg + koff, w1 = sbase + kGOffImg + 2 * kImgBytes + koff;
+                    const uint64_t a0 = sdesc_sw128(x0 + koff, 16, 1024);
+                    mma_bf16(acc, a0, sdesc_sw128(w0, 16, 1024), kIdescK, ks > 0);
+                    mma_bf16(acc, a0, sdesc_sw128(w0 + kImgBytes, 16, 1024), kIdescK, 1u);
+                    if (kMode == 1) {
+                        const uint64_t a1 = sdesc_sw128(x1 + koff, 16, 1024);
+                        mma_bf16(acc + 128, a1, sdesc_sw128(w1, 16, 1024), kIdescK, ks > 0);
+                        mma_bf16(acc + 128, a1, sdesc_sw128(w1 + kImgBytes, 16, 1024), kIdescK, 1u);
+                        // k G^T: the G image as an MN-major B operand, 16 image rows (K) per step
+                        const uint32_t wm = sbase + kGOffImg + 2 * kImgBytes + ks * 2048;
+                        mma_bf16(acc + 256, a0, sdesc_sw128(wm, kImgPanel, 1024), kIdescKMN, ks > 0);
+                        mma_bf16(acc + 256, a0, sdesc_sw128(wm + kImgBytes, kImgPanel, 1024), kIdescKMN, 1u);
+                    }
                 }
                 mma_commit(&acc_full[s]);
                 mma_commit(&x_empty[s]);
@@ -235,25 +262,27 @@ __global__ void __launch_bounds__(kTThreads, 1)
             mbar_wait_drain(drain, 0);
         }
     } else if (warp < 6) {
-        // W images: image row j holds column j of W (row j of W when w_rows),
-        // as hi + lo bf16 in the 128B-swizzled K-major layout; rows 112..127
-        // and columns 112..127 are zero.
+        // images: row j = column j of W (W0 then W1), hi + lo bf16; rows and
+        // columns 112..127 zero
         const int j = (warp & 3) * 32 + lane;
-        const int slot = p.w_rev ? p.F - 1 - f : f;
-        const float *W = p.W + ((size_t)bh * p.w_slots + slot) * kStateFloats;
+        for (int w = 0; w < (kMode == 1 ? 2 : 1); ++w) {
+            const float *W = w == 0 ? p.W0 + ((size_t)bh * p.F + f) * kStateFloats
+                                    : p.W1 + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kStateFloats;
+            uint8_t *img = sm + kGOffImg + w * 2 * kImgBytes;
 #pragma unroll 1
-        for (int c8 = 0; c8 < 16; ++c8) {
-            float x[8];
+            for (int c8 = 0; c8 < 16; ++c8) {
+                float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = c8 * 8 + e;
-                x[e] = (j < kD && i < kD) ? (p.w_rows ? W[j * kD + i] : W[i * kD + j]) : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const int i = c8 * 8 + e;
+                    x[e] = (j < kD && i < kD) ? W[i * kD + j] : 0.f;
+                }
+                uint4 hi, lo;
+                split_bf16x8(x, hi, lo);
+                const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(j, c8 & 7);
+                *reinterpret_cast<uint4 *>(img + off) = hi;
+                *reinterpret_cast<uint4 *>(img + kImgBytes + off) = lo;
             }
-            uint4 hi, lo;
-            split_bf16x8(x, hi, lo);
-            const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(j, c8 & 7);
-            *reinterpret_cast<uint4 *>(sm + kTOffWhi + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + kTOffWlo + off) = lo;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -264,48 +293,113 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
-            const int s = t & 1;
-            const uint8_t *xs = sm + kTOffX + s * kImgBytes;
-            if (ok) ok = mbar_wait_warp(&x_full[s], (t >> 1) & 1, abort_flag);
-            float scale = 1.f;
-            if (ok && p.norm_c > 0.f) {
-                float ss = 0.f;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(xs + (c >> 3) * kImgPanel + r * kRowB +
-                                                                     (((c & 7) ^ (r & 7)) << 4));
-                    float f8[8];
-                    bf16x8_to_f32(u, f8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
-                }
-                scale = p.norm_c * rsqrtf(ss + kEps);
-            }
-            __syncwarp();
-            if (ok && lane == 0) mbar_arrive(&x_empty[s]);
-            if (ok) ok = mbar_wait_warp(&acc_full[s], (t >> 1) & 1, abort_flag);
+            const int s = t % kStages, u = t / kStages;
+            // the row the normalisation applies to: q (x1) in mode 0, k (x0) in mode 1
+            const uint8_t *xr = sm + xtile(s, kMode == 0 ? 1 : 0);
+            if (ok) ok = mbar_wait_warp(&acc_full[s], u & 1, abort_flag);
             tc_fence_after();
-            if (ok) {
-                const int tok = t * 128 + r;
-                float *dst = p.out + (((size_t)bf * p.N + tok) * p.H + h) * kD;
-#pragma unroll
+            const int tok = t * 128 + r;
+            const bool live = ok && tok < p.N;
+            const size_t rowi = ((size_t)bf * p.N + tok) * p.H + h;
+            const uint32_t acc = tmem + 128 * kAcc * s + lane_off;
+            auto xrow = [&](int cc, float *o16) {  // 16 bf16 values of this thread's row, columns 16 cc..
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc) >> 3) * kImgPanel +
+                                                               sw128_off(r, (2 * cc) & 7)), o16);
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc + 1) >> 3) * kImgPanel +
+                                                               sw128_off(r, (2 * cc + 1) & 7)), o16 + 8);
+            };
+            if (kMode == 0) {
+                float sqq = 0.f, sqd = 0.f;
+#pragma unroll 1
                 for (int cc = 0; cc < 7; ++cc) {
                     uint32_t ra[16];
-                    tmem_ld16(tmem + 128 * s + lane_off + cc * 16, ra);
+                    tmem_ld16(acc + cc * 16, ra);
                     tmem_ld_wait();
-                    if (tok < p.N) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst + cc * 16);
+                    float xq[16];
+                    xrow(cc, xq);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            d4[q4] = make_float4(scale * __uint_as_float(ra[4 * q4]), scale * __uint_as_float(ra[4 * q4 + 1]),
-                                                 scale * __uint_as_float(ra[4 * q4 + 2]),
-                                                 scale * __uint_as_float(ra[4 * q4 + 3]));
+                    for (int e = 0; e < 16; ++e) {
+                        sqq = fmaf(xq[e], xq[e], sqq);
+                        sqd = fmaf(xq[e], __uint_as_float(ra[e]), sqd);
+                    }
+                }
+                const float p2 = sqq + kEps, pinv = rsqrtf(p2), corr = sqd / p2;
+                float *dq = p.g0 + rowi * kD;
+#pragma unroll 1
+                for (int cc = 0; cc < 7; ++cc) {
+                    uint32_t ra[16];
+                    tmem_ld16(acc + cc * 16, ra);
+                    tmem_ld_wait();
+                    float xq[16];
+                    xrow(cc, xq);
+                    if (live) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dq + cc * 16);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[e] = pinv * (__uint_as_float(ra[4 * q4 + e]) - xq[4 * q4 + e] * corr);
+                            d4[q4] = make_float4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            } else {
+                float skk = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < 7; ++cc) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(acc + cc * 16, r0);
+                    tmem_ld16(acc + 128 + cc * 16, r1);
+                    tmem_ld_wait();
+                    float xk[16];
+                    xrow(cc, xk);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        skk = fmaf(xk[e], xk[e], skk);
+                        s2 = fmaf(xk[e], __uint_as_float(r0[e]), s2);
+                        s3 = fmaf(xk[e], __uint_as_float(r1[e]), s3);
+                    }
+                }
+                const float r2 = skk + kEps, kh = p.c * rsqrtf(r2);   // c / r
+                const float bt = live ? __ldg(p.beta + rowi) : 0.f;
+                const float kdk = bt * (kh * s2 + s3);                 // k . dk^
+                if (live) p.g_beta[rowi] = 0.5f * kh * kh * s2 + kh * s3;
+                float *dk = p.g0 + rowi * kD, *dv = p.g1 + rowi * kD;
+#pragma unroll 1
+                for (int cc = 0; cc < 7; ++cc) {
+                    uint32_t r0[16], r1[16], r2v[16];
+                    tmem_ld16(acc + cc * 16, r0);
+                    tmem_ld16(acc + 128 + cc * 16, r1);
+                    tmem_ld16(acc + 256 + cc * 16, r2v);
+                    tmem_ld_wait();
+                    float xk[16];
+                    xrow(cc, xk);
+                    if (live) {
+                        float4 *k4 = reinterpret_cast<float4 *>(dk + cc * 16);
+                        float4 *v4 = reinterpret_cast<float4 *>(dv + cc * 16);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float ok4[4], ov4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 4 * q4 + e;
+                                const float dkh = bt * (kh * __uint_as_float(r0[i]) + __uint_as_float(r1[i]));
+                                ok4[e] = kh * (dkh - xk[i] * kdk / r2);
+                                ov4[e] = bt * kh * __uint_as_float(r2v[i]);
+                            }
+                            k4[q4] = make_float4(ok4[0], ok4[1], ok4[2], ok4[3]);
+                            v4[q4] = make_float4(ov4[0], ov4[1], ov4[2], ov4[3]);
+                        }
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(&acc_free[s]);
+            if (ok && lane == 0) {
+                mbar_arrive(&acc_free[s]);
+                mbar_arrive(&x_empty[s]);
+            }
         }
     }
     tc_fence_before();
@@ -313,100 +407,30 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
-}
-
-// ------------------------------------------------------------------ finalize
-// One warp per (token, head) row; lane l holds elements 4l .. 4l+3 (l < 28).
-__global__ void __launch_bounds__(256) kb_finalize(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                                                   const float *beta, const float *dqh, const float *x23,
-                                                   const float *x4, const float *x5, float *dq, float *dk, float *dv,
-                                                   float *dbeta, float c, size_t rows)
-{
-    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const bool act = lane < kD / 4;
-    const size_t base = row * kD + 4 * lane;
-    float kv[4] = {0, 0, 0, 0}, qv[4] = {0, 0, 0, 0}, a23[4] = {0, 0, 0, 0}, a4[4] = {0, 0, 0, 0};
-    float a5[4] = {0, 0, 0, 0}, dh[4] = {0, 0, 0, 0};
-    if (act) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            kv[e] = __bfloat162float(k[base + e]);
-            qv[e] = __bfloat162float(q[base + e]);
-        }
-        const float4 t23 = *reinterpret_cast<const float4 *>(x23 + base);
-        const float4 t4 = *reinterpret_cast<const float4 *>(x4 + base);
-        const float4 t5 = *reinterpret_cast<const float4 *>(x5 + base);
-        const float4 td = *reinterpret_cast<const float4 *>(dqh + base);
-        a23[0] = t23.x, a23[1] = t23.y, a23[2] = t23.z, a23[3] = t23.w;
-        a4[0] = t4.x, a4[1] = t4.y, a4[2] = t4.z, a4[3] = t4.w;
-        a5[0] = t5.x, a5[1] = t5.y, a5[2] = t5.z, a5[3] = t5.w;
-        dh[0] = td.x, dh[1] = td.y, dh[2] = td.z, dh[3] = td.w;
-    }
-    // warp sums: |k|^2, |q|^2, k . x23, k . x4, q . dq^
-    float s[5] = {0, 0, 0, 0, 0};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        s[0] = fmaf(kv[e], kv[e], s[0]);
-        s[1] = fmaf(qv[e], qv[e], s[1]);
-        s[2] = fmaf(kv[e], a23[e], s[2]);
-        s[3] = fmaf(kv[e], a4[e], s[3]);
-        s[4] = fmaf(qv[e], dh[e], s[4]);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < 5; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], o);
-    const float bt = beta[row];
-    const float r2 = s[0] + kEps, rinv = rsqrtf(r2), kh = c * rinv;  // k^ = kh * k
-    const float p2 = s[1] + kEps, pinv = rsqrtf(p2);
-    // dk^ = beta (x23 + x4);  k . dk^ = beta (k . x23 + k . x4)
-    const float kdk = bt * (s[2] + s[3]);
-    if (act) {
-        float4 o_dk, o_dv, o_dq;
-        float *pk = &o_dk.x, *pv = &o_dv.x, *pq = &o_dq.x;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float dkh = bt * (a23[e] + a4[e]);
-            pk[e] = kh * (dkh - kv[e] * kdk / r2);
-            pv[e] = bt * a5[e];
-            pq[e] = pinv * (dh[e] - qv[e] * s[4] / p2);
-        }
-        *reinterpret_cast<float4 *>(dk + base) = o_dk;
-        *reinterpret_cast<float4 *>(dv + base) = o_dv;
-        *reinterpret_cast<float4 *>(dq + base) = o_dq;
-    }
-    // dbeta = k^ dA k^ + v G k^ = 1/2 k^ . x23 + x4 . k^
-    if (lane == 0) dbeta[row] = kh * (0.5f * s[2] + s[3]);
 }
 
 // ------------------------------------------------------------ orchestration
 namespace {
 struct BwdLayout {
-    TcPlan plan;
-    size_t ws_fwd, ws_E, ones, ws_G, gamma_G, Sst, Gst, Dsym, dqh, x23, x4, x5, total;
+    TcPlan plan, plan_G;  // F frames; the reverse scan's F + 1 slots
+    size_t ws_fwd, ws_E, ones, ws_G, gamma_G, Sst, Gst, Dsym, total;
 };
 
 bool bwd_layout(int B, int H, int F, int N, BwdLayout *L)
 {
-    if (!tc_plan(B, H, F, N, 0, &L->plan)) return false;
-    const size_t BH = (size_t)B * H, tokf = (size_t)B * F * N * H * kD * 4;
+    if (!tc_plan(B, H, F, N, 0, &L->plan) || !tc_plan(B, H, F + 1, N, 0, &L->plan_G)) return false;
+    const size_t BH = (size_t)B * H;
     size_t o = 0;
     L->ws_fwd = o; o = up256(o + L->plan.ws_bytes);
     L->ws_E = o; o = up256(o + L->plan.ws_bytes);
     L->ones = o; o = up256(o + (size_t)B * F * N * H * 4);
-    L->ws_G = o; o = up256(o + BH * (F + 1) * kFrameWs);
+    L->ws_G = o; o = up256(o + L->plan_G.ws_bytes);
     L->gamma_G = o; o = up256(o + (size_t)B * (F + 1) * H * 4);
     L->Sst = o; o = up256(o + BH * F * kStateBytes);
     L->Gst = o; o = up256(o + BH * (F + 1) * kStateBytes);
     L->Dsym = o; o = up256(o + BH * F * kStateBytes);
-    L->dqh = o; o = up256(o + tokf);
-    L->x23 = o; o = up256(o + tokf);
-    L->x4 = o; o = up256(o + tokf);
-    L->x5 = o; o = up256(o + tokf);
     L->total = o;
     return true;
 }
@@ -421,8 +445,11 @@ cudaError_t prepare_bwd_kernels()
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevB) return cudaErrorInvalidDevice;
     if (g_b_attr[dev]) return cudaSuccess;
-    if ((e = cudaFuncSetAttribute(kt_token_matrix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kTSmem)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kg_token_grad_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kGSmem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(kg_token_grad_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kGSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(kb_frame_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFgSmem)) !=
         cudaSuccess)
@@ -431,24 +458,36 @@ cudaError_t prepare_bwd_kernels()
     return cudaSuccess;
 }
 
-cudaError_t token_matrix(const void *x, const float *W, int w_slots, int w_rev, int w_rows, float norm_c, float *out,
-                         int B, int H, int F, int N, unsigned *status, cudaStream_t stream)
+cudaError_t token_grads(const void *dO, const void *q, const void *k, const void *v, const float *beta,
+                        const float *Sst, const float *Dsym, const float *Gst, float *dq, float *dk, float *dv,
+                        float *dbeta, int B, int H, int F, int N, float c, unsigned *status, cudaStream_t stream)
 {
-    CUtensorMap mx;
-    if (!make_token_map(&mx, x, B, H, F, N, 128)) return cudaErrorInvalidValue;
-    TokMatParams p;
-    p.W = W;
-    p.out = out;
+    CUtensorMap mdo, mq, mk, mv;
+    if (!make_token_map(&mdo, dO, B, H, F, N, 128) || !make_token_map(&mq, q, B, H, F, N, 128) ||
+        !make_token_map(&mk, k, B, H, F, N, 128) || !make_token_map(&mv, v, B, H, F, N, 128))
+        return cudaErrorInvalidValue;
+    TokGradParams p;
+    p.beta = beta;
     p.status = status;
     p.B = B;
     p.H = H;
     p.F = F;
     p.N = N;
-    p.w_slots = w_slots;
-    p.w_rev = w_rev;
-    p.w_rows = w_rows;
-    p.norm_c = norm_c;
-    kt_token_matrix_kernel<<<B * H * F, kTThreads, kTSmem, stream>>>(mx, p);
+    p.c = c;
+    p.W0 = Sst;
+    p.W1 = nullptr;
+    p.g0 = dq;
+    p.g1 = nullptr;
+    p.g_beta = nullptr;
+    kg_token_grad_kernel<0><<<B * H * F, kGThreads, kGSmem, stream>>>(mdo, mq, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    p.W0 = Dsym;
+    p.W1 = Gst;
+    p.g0 = dk;
+    p.g1 = dv;
+    p.g_beta = dbeta;
+    kg_token_grad_kernel<1><<<B * H * F, kGThreads, kGSmem, stream>>>(mk, mv, p);
     return cudaGetLastError();
 }
 }  // namespace
@@ -470,18 +509,15 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = B * H;
-    const size_t rows = (size_t)B * F * N * H;
+    const size_t rows = (size_t)B * F * N * H;  // token rows (beta entries)
     float *ones = reinterpret_cast<float *>(ws + L.ones);
     float *gamma_G = reinterpret_cast<float *>(ws + L.gamma_G);
     float *Sst = reinterpret_cast<float *>(ws + L.Sst), *Gst = reinterpret_cast<float *>(ws + L.Gst);
     float *Dsym = reinterpret_cast<float *>(ws + L.Dsym);
-    float *dqh = reinterpret_cast<float *>(ws + L.dqh), *x23 = reinterpret_cast<float *>(ws + L.x23);
-    float *x4 = reinterpret_cast<float *>(ws + L.x4), *x5 = reinterpret_cast<float *>(ws + L.x5);
     // 1. forward statistics and every state S_f
     if ((e = launch_frame_stats_tc(k, v, beta, gamma, L.plan, c, 0, ws + L.ws_fwd, status, stream)) != cudaSuccess)
         return e;
-    if ((e = launch_state_chain_tc(gamma, ws + L.ws_fwd + L.plan.off_frames, S_in, Sst, B, H, F, status, stream)) !=
-        cudaSuccess)
+    if ((e = launch_states_tc(q, gamma, S_in, nullptr, Sst, L.plan, ws + L.ws_fwd, status, stream)) != cudaSuccess)
         return e;
     // 2. E_f = dO^T q^ through the statistics kernel (k := q, v := dO, beta := 1, c := 1)
     kb_fill<<<296, 256, 0, stream>>>(ones, rows, 1.f);
@@ -490,29 +526,21 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
         return e;
     // 3. reverse scan G_{F-1} .. G_0, ending at dS_in
     kb_build_reverse_ws<<<dim3(BH, F + 1), 256, 0, stream>>>(ws + L.ws_fwd + L.plan.off_frames,
-                                                              ws + L.ws_E + L.plan.off_frames, ws + L.ws_G, gamma,
-                                                              gamma_G, B, H, F);
+                                                              ws + L.ws_E + L.plan.off_frames,
+                                                              ws + L.ws_G + L.plan_G.off_frames, gamma, gamma_G, B, H,
+                                                              F);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_state_chain_tc(gamma_G, ws + L.ws_G, dS_out, Gst, B, H, F + 1, status, stream)) != cudaSuccess)
+    if ((e = launch_chunk_composite_tc(gamma_G, L.plan_G, 0, ws + L.ws_G, status, stream)) != cudaSuccess) return e;
+    if ((e = launch_states_tc(q, gamma_G, dS_out, dS_in, Gst, L.plan_G, ws + L.ws_G, status, stream)) != cudaSuccess)
         return e;
     // 4. per-frame dgamma and Dsym = dA + dA^T
     kb_frame_grad<<<dim3(BH, F), 256, kFgSmem, stream>>>(S_in, Sst, Gst, dgamma, Dsym, B, H, F);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 5. token rows times per-frame matrices
-    if ((e = token_matrix(dO, Sst, F, 0, 0, 0.f, dqh, B, H, F, N, status, stream)) != cudaSuccess) return e;
-    if ((e = token_matrix(k, Dsym, F, 0, 0, c, x23, B, H, F, N, status, stream)) != cudaSuccess) return e;
-    if ((e = token_matrix(v, Gst, F + 1, 1, 0, 0.f, x4, B, H, F, N, status, stream)) != cudaSuccess) return e;
-    if ((e = token_matrix(k, Gst, F + 1, 1, 1, c, x5, B, H, F, N, status, stream)) != cudaSuccess) return e;
-    // 6. dk, dv, dq, dbeta
-    kb_finalize<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), beta, dqh, x23, x4, x5, dq, dk,
-        dv, dbeta, c, rows);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 7. dS_in = the reverse scan's last state
-    if (dS_in)
-        e = cudaMemcpy2DAsync(dS_in, kStateBytes, Gst + (size_t)F * kStateFloats, (F + 1) * kStateBytes, kStateBytes,
-                              BH, cudaMemcpyDeviceToDevice, stream);
-    return e;
+    // 5. token gradients: dq from dO S_f; dk, dv, dbeta from k Dsym_f, v G_f, k G_f^T
+    if ((e = token_grads(dO, q, k, v, beta, Sst, Dsym, Gst, dq, dk, dv, dbeta, B, H, F, N, c, status, stream)) !=
+        cudaSuccess)
+        return e;
+    return cudaSuccess;  // dS_in: written by the reverse scan as its final state
 }
 
 }  // namespace gdn

@@ -64,10 +64,10 @@ cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void
 cudaError_t launch_frame_stats_tc(const void *k, const void *v, const float *beta, const float *gamma,
                                   const TcPlan &plan, float c, int reverse, void *workspace, unsigned *status,
                                   cudaStream_t stream);
-// H <- gamma_f H - H A_f + U_f over all F workspace slots of each chain, from H_init
-// (null: zero); H after every slot goes to states [B*H][F][D][D] (gdn_product.cu).
-cudaError_t launch_state_chain_tc(const float *gamma, const uint8_t *ws_frames, const float *H_init, float *states,
-                                  int B, int H, int F, unsigned *status, cudaStream_t stream);
+// The state chain alone (K1b + K2 without outputs) over a plan whose workspace
+// holds statistics and chunk composites; every state to states (gdn_tc.cu).
+cudaError_t launch_states_tc(const void *q, const float *gamma, const float *S_in, float *S_out, float *states,
+                             const TcPlan &plan, uint8_t *ws, unsigned *status, cudaStream_t stream);
 // backward pass of the sum reading (gdn_bwd.cu); D == 112.
 size_t bwd_workspace_bytes(int B, int H, int F, int N);
 cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,

@@ -476,9 +476,7 @@ constexpr uint32_t kCSmem = kCOffBar + 256 + 1024;
 struct CompParams {
     const float *gamma;
     const uint8_t *ws_frames;  // [BH][F] x kFrameWs, by processing position
-    float *ws_comp;            // [BH][n_chunks] x (C, H) fp32, or null
-    const float *H_init;       // [BH][D][D] start of H (chunk 0 only), or null: zero
-    float *states;             // [BH][F][D][D]: H after every frame, or null
+    float *ws_comp;            // [BH][n_chunks] x (C, H) fp32
     unsigned *status;
     int B, H, F, chunk, n_chunks, reverse;
 };
@@ -569,17 +567,6 @@ __global__ void __launch_bounds__(kCThreads, 1) kc_chunk_composite_kernel(const 
         float S[kD];
 #pragma unroll
         for (int j = 0; j < kD; ++j) S[j] = (m == 0 && row == j) ? 1.f : 0.f;
-        if (m == 1 && p.H_init && chunk_idx == 0 && row < kD) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.H_init + (size_t)bh * kStateFloats + row * kD);
-#pragma unroll
-            for (int j = 0; j < kD / 4; ++j) {
-                const float4 v4 = src[j];
-                S[4 * j] = v4.x;
-                S[4 * j + 1] = v4.y;
-                S[4 * j + 2] = v4.z;
-                S[4 * j + 3] = v4.w;
-            }
-        }
         auto write_images = [&]() {
             if (row < kD) {
 #pragma unroll
@@ -640,15 +627,9 @@ __global__ void __launch_bounds__(kCThreads, 1) kc_chunk_composite_kernel(const 
                 for (int j = 0; j < 16; ++j) S[cc * 16 + j] -= __uint_as_float(ra[j]);
             }
             tc_fence_before();
-            if (m == 1 && p.states && row < kD) {
-                float4 *dst = reinterpret_cast<float4 *>(p.states + ((size_t)bh * p.F + f_begin + it) * kStateFloats +
-                                                         row * kD);
-#pragma unroll
-                for (int j = 0; j < kD / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-            }
             if (it + 1 < nf) write_images();
         }
-        if (ok && row < kD && p.ws_comp) {
+        if (ok && row < kD) {
             float *dst = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats +
                          (size_t)m * kStateFloats + row * kD;
 #pragma unroll
@@ -724,43 +705,10 @@ cudaError_t launch_chunk_composite_tc(const float *gamma, const TcPlan &pl, int 
     p.B = pl.B;
     p.H = pl.H;
     p.F = pl.F;
-    p.H_init = nullptr;
-    p.states = nullptr;
     p.chunk = pl.chunk;
     p.n_chunks = pl.n_chunks;
     p.reverse = reverse;
     kc_chunk_composite_kernel<<<pl.B * pl.H * pl.n_chunks, kCThreads, kCSmem, stream>>>(p);
-    return cudaGetLastError();
-}
-
-// One chunk per chain over all F workspace slots: H <- gamma_f H - H Abar_f + U_f from
-// H_init (null: zero), writing H after every slot to states ([BH][F][D][D]).
-cudaError_t launch_state_chain_tc(const float *gamma, const uint8_t *ws_frames, const float *H_init, float *states,
-                                  int B, int H, int F, unsigned *status, cudaStream_t stream)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevP) return cudaErrorInvalidDevice;
-    if (!g_c_attr[dev]) {
-        e = cudaFuncSetAttribute(kc_chunk_composite_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem);
-        if (e != cudaSuccess) return e;
-        g_c_attr[dev] = true;
-    }
-    CompParams p;
-    p.gamma = gamma;
-    p.ws_frames = ws_frames;
-    p.ws_comp = nullptr;
-    p.H_init = H_init;
-    p.states = states;
-    p.status = status;
-    p.B = B;
-    p.H = H;
-    p.F = F;
-    p.chunk = F;
-    p.n_chunks = 1;
-    p.reverse = 0;
-    kc_chunk_composite_kernel<<<B * H, kCThreads, kCSmem, stream>>>(p);
     return cudaGetLastError();
 }
 

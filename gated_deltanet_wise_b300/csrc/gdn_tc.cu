@@ -494,10 +494,12 @@ struct K2Params {
     const float *gamma;
     const uint8_t *ws_frames;
     const float *ws_start;
-    float *S_out;  // non-null: the last chunk's CTAs write the chain's final state here
+    float *S_out;   // non-null: the last chunk's CTAs write the chain's final state here
+    float *states;  // non-null: the state after every frame, [B*H][F][D][D] by processing position
     unsigned *status;
     int B, H, F, N, chunk, n_chunks;
-    int reverse;  // 1: frames are visited from the last to the first
+    int reverse;      // 1: frames are visited from the last to the first
+    int states_only;  // 1: no outputs (the state chain alone)
 };
 
 // Named barrier over K2's four output warps (id 0 is __syncthreads).
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const int b = bh / p.H, h = bh % p.H;
     const int f_begin = chunk_idx * p.chunk;
     const int nf = min(p.F, f_begin + p.chunk) - f_begin;
-    const int n_tiles = (p.N + kTQ - 1) / kTQ;
+    const int n_tiles = p.states_only ? 0 : (p.N + kTQ - 1) / kTQ;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kK2QStages; ++i) {
@@ -719,6 +721,12 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 for (int j = 0; j < 16; ++j) S[cc * 16 + j] -= __uint_as_float(ra[j]);
             }
             tc_fence_before();
+            if (p.states && row < kD) {
+                float4 *dst = reinterpret_cast<float4 *>(p.states + ((size_t)bh * p.F + f_begin + it) * kStateFloats +
+                                                         row * kD);
+#pragma unroll
+                for (int j = 0; j < kD / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+            }
             if (it >= 1 && !mbar_wait_warp(o_done, (it - 1) & 1, abort_flag)) break;
             write_images();
         }
@@ -1017,6 +1025,8 @@ static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, cons
     p2.ws_frames = ws + pl.off_frames;
     p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
     p2.S_out = S_out;  // the last chunk's state after its last frame
+    p2.states = nullptr;
+    p2.states_only = 0;
     p2.status = status;
     p2.B = pl.B;
     p2.H = pl.H;
@@ -1029,6 +1039,41 @@ static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, cons
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
     return cudaSuccess;
+}
+
+// The state chain alone over a plan whose workspace holds per-frame statistics
+// and chunk composites: K1b from S_in (null: zero), then K2 without outputs,
+// storing the state after every frame (states, [B*H][F][D][D]) and the final
+// state (S_out, may be null).  q only shapes K2's (unused) tensor maps.
+cudaError_t launch_states_tc(const void *q, const float *gamma, const float *S_in, float *S_out, float *states,
+                             const TcPlan &pl, uint8_t *ws, unsigned *status, cudaStream_t stream)
+{
+    CUtensorMap mq;
+    if (!make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ)) return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    const int BH = pl.B * pl.H;
+    const float *comp = reinterpret_cast<const float *>(ws + pl.off_comp);
+    e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream, comp,
+                   comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats, (size_t)2 * kStateFloats,
+                   reinterpret_cast<float *>(ws + pl.off_start), S_in, (float *)nullptr, pl.n_chunks, status);
+    if (e != cudaSuccess) return e;
+    K2Params p2;
+    p2.gamma = gamma;
+    p2.ws_frames = ws + pl.off_frames;
+    p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
+    p2.S_out = S_out;
+    p2.states = states;
+    p2.states_only = 1;
+    p2.status = status;
+    p2.B = pl.B;
+    p2.H = pl.H;
+    p2.F = pl.F;
+    p2.N = pl.N;
+    p2.chunk = pl.chunk;
+    p2.n_chunks = pl.n_chunks;
+    p2.reverse = 0;
+    return launch_pdl(k2_scan_output_kernel, dim3(BH * pl.n_chunks), kK2Threads, kK2Smem, stream, mq, mq, p2);
 }
 
 cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
