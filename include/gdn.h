@@ -157,8 +157,9 @@ gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
  * for the same q, k, v, beta, gamma, S_in (NULL: zero) and key_scale as the
  * forward.  It recomputes the forward states; nothing from a forward call is
  * kept.  Workspace: gdn_frame_bwd_workspace_size(B,H,F,N,D) bytes, 256-byte
- * aligned (about 4.9 GB for B=1, H=20, F=121, N=880: the per-frame states,
- * the gradient states and four fp32 token-row intermediates).  F = 0 copies
+ * aligned (about 1.0 GB for B=1, H=20, F=121, N=880: two statistics
+ * workspaces, the per-frame states, the gradient states and their
+ * symmetrised products).  F = 0 copies
  * dS_out to dS_in; N = 0 with F > 0 returns GDN_ERR_UNSUPPORTED; D != 112
  * returns GDN_ERR_UNSUPPORTED.  Gradients match the fp64 chain rule (itself
  * checked against finite differences) within a relative Frobenius error of
