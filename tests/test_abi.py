@@ -130,3 +130,22 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         gdn.lib()
+
+
+def test_plain_c_consumer(L, tmp_path):
+    """include/gdn.h compiles as C (gcc, no CUDA headers) and a C program linked
+    against the library runs its host-side entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    from gated_deltanet_wise_b300 import build
+    libdir = os.path.dirname(build.LIB)
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c", "abi_consumer.c"), "-o", exe, "-L", libdir,
+                           "-l:" + os.path.basename(build.LIB), "-Wl,-rpath," + libdir])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "abi consumer ok" in r.stdout
