@@ -244,11 +244,13 @@ def barrier(world):
 
 
 def max_over_ranks(world, value):
+    """The slowest rank's time (every rank gets it); NCCL groups reduce on the GPU, others on the CPU."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

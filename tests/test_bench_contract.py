@@ -54,3 +54,31 @@ def test_algorithmic_counts():
     assert a["state"] == 2 * 20 * 112 * 112 * 4
     assert a["flops"] == 20 * 121 * (6 * 880 * 112 ** 2 + 2 * 112 ** 3)
     assert bench.step_bytes(1, 20, 880, 112) == 17847120
+
+
+def _max_rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        sys.path.insert(0, ROOT)
+        import bench
+        bench.barrier(world)
+        v = bench.max_over_ranks(world, 1.5 + rank)   # per-rank step times
+        with open(os.path.join(out, f"r{rank}.txt"), "w") as fh:
+            fh.write(repr(v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_on_cpu_ranks(tmp_path):
+    """The timing reduction of a multi-rank run: every rank sees the slowest rank's time."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.spawn(_max_rank, args=(3, port, str(tmp_path)), nprocs=3, join=True)
+    for r in range(3):
+        assert float(open(tmp_path / f"r{r}.txt").read()) == 3.5
