@@ -159,7 +159,8 @@ gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
  * kept.  Workspace: gdn_frame_bwd_workspace_size(B,H,F,N,D) bytes, 256-byte
  * aligned (about 1.0 GB for B=1, H=20, F=121, N=880: two statistics
  * workspaces, the per-frame states, the gradient states and their
- * symmetrised products).  F = 0 copies
+ * symmetrised products).  F must stay below 65,535 (a grid dimension of the
+ * per-frame kernels; larger F fails with GDN_ERR_CUDA).  F = 0 copies
  * dS_out to dS_in; N = 0 with F > 0 returns GDN_ERR_UNSUPPORTED; D != 112
  * returns GDN_ERR_UNSUPPORTED.  Gradients match the fp64 chain rule (itself
  * checked against finite differences) within a relative Frobenius error of
