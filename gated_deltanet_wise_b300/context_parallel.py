@@ -88,9 +88,8 @@ def cp_forward(q, k, v, beta, gamma, S_in=None, *, ops: Optional[CpOps] = None, 
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
     C, H = ops.composite(k, v, beta, gamma)
-    Cs = [torch.empty_like(C) for _ in range(world)]
-    Hs = [torch.empty_like(H) for _ in range(world)]
-    dist.all_gather(Cs, C.contiguous(), group=group)
-    dist.all_gather(Hs, H.contiguous(), group=group)
-    S_start = start_state(S_in, list(zip(Cs, Hs)), rank, ops.compose)
+    CH = torch.stack([C, H]).contiguous()   # one message per rank: (C_p, H_p) back to back
+    parts = [torch.empty_like(CH) for _ in range(world)]
+    dist.all_gather(parts, CH, group=group)
+    S_start = start_state(S_in, [(x[0], x[1]) for x in parts], rank, ops.compose)
     return ops.forward(q, k, v, beta, gamma, S_start)

@@ -103,7 +103,8 @@ size_t gdn_frame_fwd_ex_workspace_size(int B, int H, int F, int N, int D, unsign
 static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, const float *beta,
                                    const float *gamma, const float *S_in, float *S_out, void *o, int B, int H, int F,
                                    int N, int D, float key_scale, unsigned flags, void *workspace,
-                                   size_t workspace_bytes, gdn_stream_t stream, void **events)
+                                   size_t workspace_bytes, gdn_stream_t stream, void **events,
+                                   int withhold_loads = 0)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
     if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE)) return GDN_ERR_INVALID_ARG;
@@ -128,6 +129,7 @@ static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, 
     if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
     unsigned *status = device_status_word();
     if (!status) return GDN_ERR_CUDA;
+    plan.withhold_loads = withhold_loads;
     const float c = default_key_scale(key_scale, D, N);
     cudaError_t e = product ? launch_frame_fwd_product_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse,
                                                           workspace, status, st)
@@ -171,11 +173,24 @@ gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v,
                           workspace_bytes, stream, events);
 }
 
+gdn_status_t gdn_test_frame_fwd_expired_wait(const void *q, const void *k, const void *v, const float *beta,
+                                              const float *gamma, const float *S_in, float *S_out, void *o, int B,
+                                              int H, int F, int N, int D, float key_scale, void *workspace,
+                                              size_t workspace_bytes, gdn_stream_t stream)
+{
+    return frame_fwd_impl(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, 0, workspace,
+                          workspace_bytes, stream, nullptr, 1);
+}
+
+// The backward's per-frame kernels put the frame index on a grid dimension
+// limited to 65,535, so longer runs are refused before anything is enqueued.
+constexpr int kBwdMaxFrames = 65535;
+
 size_t gdn_frame_bwd_workspace_size(int B, int H, int F, int N, int D)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
     if (B == 0 || H == 0 || F == 0) return 0;
-    if (D != 112 || N == 0) return (size_t)-1;
+    if (D != 112 || N == 0 || F >= kBwdMaxFrames) return (size_t)-1;
     return bwd_workspace_bytes(B, H, F, N);
 }
 
@@ -197,7 +212,7 @@ gdn_status_t gdn_frame_bwd(const void *q, const void *k, const void *v, const fl
                                : cudaMemsetAsync(dS_in, 0, state_bytes, st);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
-    if (N == 0) return GDN_ERR_UNSUPPORTED;
+    if (N == 0 || F >= kBwdMaxFrames) return GDN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !beta || !gamma || !dO || !dq || !dk || !dv || !dbeta || !dgamma) return GDN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dO, 16) || !aligned(dq, 16) ||
         !aligned(dk, 16) || !aligned(dv, 16) || !aligned(beta, 4) || !aligned(gamma, 4) || !aligned(dbeta, 4) ||

@@ -31,6 +31,9 @@ struct TcPlan {
     int n_chunks;    // chunks per chain
     size_t ws_bytes; // total workspace
     size_t off_frames, off_comp, off_start;  // workspace sections
+    // Failure-detection test only: the frame-statistics kernel issues no loads,
+    // so its first bounded wait expires and the status word records a timeout.
+    int withhold_loads = 0;
 };
 // force_chunks > 0 fixes the number of frame chunks (1: one chunk per chain,
 // whose composite is then the whole range's); 0 lets the plan choose.

@@ -59,12 +59,21 @@ gdn_status_t gdn_frame_step_noalloc(const void *q, const void *k, const void *v,
                                     int D, float key_scale, gdn_stream_t stream)
 {
     // The frame runs through the multi-frame kernels with F = 1, whose
-    // frame statistics and chunk composites live in the scratch.
+    // frame statistics and chunk composites live in the scratch.  Whenever the
+    // scratch is not used (degenerate or unsupported sizes, bad arguments, a
+    // request larger than the array), the call is handed to gdn_frame_fwd
+    // without a workspace, so both entries report the same status for the same
+    // arguments, in the same order, before anything is enqueued.
     const size_t need = gdn_frame_fwd_workspace_size(B, H, 1, N, D);
-    if (need == (size_t)-1) return D > 0 && D != 112 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
-    if (need > gdn::kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
-    if (need == 0)  // degenerate sizes use no scratch
+    if (need == 0 || need == (size_t)-1 || need > gdn::kNoAllocScratchBytes)
         return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, nullptr, 0, stream);
+    // Sizes that use the scratch: the pointers are validated first, exactly as
+    // gdn_frame_fwd does it.  Without a workspace that call stops at its
+    // workspace check (GDN_ERR_WORKSPACE) when every argument is valid, and
+    // enqueues nothing either way.
+    const gdn_status_t pre =
+        gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, nullptr, 0, stream);
+    if (pre != GDN_ERR_WORKSPACE) return pre;
     void *scratch = gdn::scratch_address();
     if (!scratch) return GDN_ERR_CUDA;
     return gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, 1, N, D, key_scale, scratch,

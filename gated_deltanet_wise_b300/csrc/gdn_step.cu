@@ -198,9 +198,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
-    // The next step on the stream may start (its stats phase reads only its own
-    // inputs); it waits for this grid before it touches the state or outputs.
+    // Programmatic dependent launch: the next kernel on the stream may be
+    // scheduled now, but this grid reads no global memory (q, k, v, beta,
+    // gamma, S_in: any of them may come from the previous kernel, e.g. a
+    // projection or the previous step) before that kernel has completed and
+    // its writes are visible.  Only the prologue above overlaps its tail.
     griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -386,10 +390,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
         }
 
-        // 2b. the previous grid on the stream (e.g. the previous step, whose
-        //     S_out is this S_in) must be complete before the state is read or
-        //     any output written; then S_in goes into registers for its images
-        griddep_wait();
+        // 2b. S_in into registers for its images
         constexpr int kIt = (kD * 14 + 255) / 256;
         float4 x0[kIt], x1[kIt];
 #pragma unroll
@@ -717,7 +718,7 @@ cudaError_t launch_frame_step_tc(const void *q, const void *k, const void *v, co
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the previous step's tail
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the previous kernel
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(BH * cl));
     cfg.blockDim = dim3(kSThreads);

@@ -77,6 +77,7 @@ struct K1Params {
     int B, H, F, N, chunk, n_chunks;
     float c;
     int reverse;  // 1: frames are visited from the last to the first
+    int withhold_loads;  // failure-detection test: the producer issues nothing
 };
 
 // Tensor memory of K1 (512 columns, fp32 unless noted):
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int it = 0;
-            bool ok = true;
+            bool ok = !p.withhold_loads;  // withheld: no stage ever fills, the consumers' waits expire
             for (int fl = 0; fl < nf && ok; ++fl) {
                 const int bf = b * p.F + frame_at(f_begin + fl, p.F, p.reverse);
                 for (int st = 0; st < n_st; ++st, ++it) {
@@ -950,6 +951,7 @@ K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, floa
     p1.n_chunks = pl.n_chunks;
     p1.c = c;
     p1.reverse = reverse;
+    p1.withhold_loads = pl.withhold_loads;
     return p1;
 }
 }  // namespace

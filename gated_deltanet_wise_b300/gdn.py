@@ -34,7 +34,7 @@ EXPORTED = [
     "gdn_frame_composite_workspace_size", "gdn_frame_composite", "gdn_state_compose",
     "gdn_frame_fwd_product_workspace_size", "gdn_frame_fwd_product",
     "gdn_frame_fwd_ex_workspace_size", "gdn_frame_fwd_ex",
-    "gdn_frame_bwd_workspace_size", "gdn_frame_bwd",
+    "gdn_frame_bwd_workspace_size", "gdn_frame_bwd", "gdn_test_frame_fwd_expired_wait",
 ]
 
 GDN_FWD_PRODUCT = 1
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_bwd_workspace_size.argtypes = [I] * 5
         L.gdn_frame_bwd.restype = I
         L.gdn_frame_bwd.argtypes = [P] * 14 + [I] * 5 + [F, P, Z, P]
+        L.gdn_test_frame_fwd_expired_wait.restype = I
+        L.gdn_test_frame_fwd_expired_wait.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
         _lib = L
     return _lib
 
@@ -126,6 +128,13 @@ def _check_status(st: int, what: str):
 # ---------------------------------------------------------------- raw C entry points
 def gdn_frame_fwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
     return int(lib().gdn_frame_fwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_test_frame_fwd_expired_wait(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
+                                    workspace_bytes, stream=None) -> int:
+    return int(lib().gdn_test_frame_fwd_expired_wait(_p(q), _p(k), _p(v), _p(beta), _p(gamma), _p(S_in), _p(S_out),
+                                                     _p(o), B, H, F, N, D, float(key_scale), _p(workspace),
+                                                     int(workspace_bytes), _stream(stream)))
 
 
 def gdn_frame_step_workspace_size(B: int, H: int, N: int, D: int) -> int:

@@ -160,7 +160,8 @@ gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
  * aligned (about 1.0 GB for B=1, H=20, F=121, N=880: two statistics
  * workspaces, the per-frame states, the gradient states and their
  * symmetrised products).  F must stay below 65,535 (a grid dimension of the
- * per-frame kernels; larger F fails with GDN_ERR_CUDA).  F = 0 copies
+ * per-frame kernels): larger F returns GDN_ERR_UNSUPPORTED before anything is
+ * enqueued, and the size query returns (size_t)-1.  F = 0 copies
  * dS_out to dS_in; N = 0 with F > 0 returns GDN_ERR_UNSUPPORTED; D != 112
  * returns GDN_ERR_UNSUPPORTED.  Gradients match the fp64 chain rule (itself
  * checked against finite differences) within a relative Frobenius error of
@@ -289,6 +290,10 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,
  *   - Limit: gdn_frame_fwd_workspace_size(B, H, 1, N, D) must not exceed the
  *     array (about 226 KiB per chain at D = 112, so B*H <= 72).  Larger
  *     requests return GDN_ERR_WORKSPACE before anything is enqueued.
+ *   - Status codes: for every argument list the call returns what
+ *     gdn_frame_fwd (F = 1) returns when given a workspace of the array's
+ *     size, checked in the same order (negative sizes, then D, then
+ *     pointers, then the size plan, then the scratch limit).
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current.  Make that first call
@@ -305,6 +310,26 @@ gdn_status_t gdn_frame_step_noalloc(const void *q, const void *k, const void *v,
                                     const float *S_in, float *S_out, void *o,
                                     int B, int H, int N, int D, float key_scale,
                                     gdn_stream_t stream);
+
+/*
+ * Failure-detection test entry: gdn_frame_fwd (sum reading, same arguments,
+ * checks and status codes) with the frame-statistics kernel told to issue no
+ * loads.  Its consumers' bounded waits on the first pipeline stage then run
+ * out (after about 2 s of GPU time: the wait limit is ~4e9 SM cycles), the
+ * kernel sets its abort flag, lets every role leave its loop, frees its tensor
+ * memory and exits; no fault, trap or unbounded wait is involved.  The
+ * following kernels of the call still run (on undefined statistics), so o and
+ * S_out are undefined, and gdn_device_status() afterwards returns
+ * GDN_ERR_TIMEOUT.  The context stays usable: later calls behave normally.
+ * There is no counterpart on the pages; it exists so that tests can exercise
+ * the timeout path end to end.
+ */
+gdn_status_t gdn_test_frame_fwd_expired_wait(const void *q, const void *k, const void *v,
+                                             const float *beta, const float *gamma,
+                                             const float *S_in, float *S_out, void *o,
+                                             int B, int H, int F, int N, int D, float key_scale,
+                                             void *workspace, size_t workspace_bytes,
+                                             gdn_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status

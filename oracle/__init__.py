@@ -46,8 +46,8 @@ def _load():
         lib.oracle_gdn_frame_fwd.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_fwd_tokacc.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_transitions.argtypes = [P] * 4 + [I] * 5 + [Dbl, P, P]
-        lib.oracle_gdn_frame_fwd_product.argtypes = [P] * 6 + [I] * 5 + [Dbl, I, P, P]
-        lib.oracle_gdn_frame_transitions_product.argtypes = [P] * 4 + [I] * 5 + [Dbl, I, P, P]
+        lib.oracle_gdn_frame_fwd_product.argtypes = [P] * 6 + [I] * 5 + [Dbl, P, P]
+        lib.oracle_gdn_frame_transitions_product.argtypes = [P] * 4 + [I] * 5 + [Dbl, P, P]
         lib.oracle_gdn_frame_bwd.argtypes = [P] * 8 + [I] * 5 + [Dbl] + [P] * 6
         lib.oracle_gdn_composite.argtypes = [P, P, I, I, P, P]
         lib.oracle_gdn_compose.argtypes = [P, P, P, P, I, P, P]
@@ -80,7 +80,7 @@ def _flip_frames(x, F):
 
 
 def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulation="recurrence",
-              mode="sum", sub=64, reverse=False):
+              mode="sum", reverse=False):
     """Frame-wise GDN forward in fp64.
 
     Shapes: q, k, v [B, F*N, H, D]; beta [B, F*N, H]; gamma [B, F, H];
@@ -90,8 +90,8 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
     ``formulation`` picks the printed recurrence ("recurrence") or the
     token-accumulation rewrite ("tokacc").  ``mode="product"`` is the
     token-ordered reading M_f = gamma_f I - (I - prod_n (I - beta_n k^_n k^_n^T))
-    with the frame's tokens applied in order from zero for U_f, computed through
-    the UT transform over sub-chunks of ``sub`` tokens.
+    with the frame's tokens applied in order from zero for U_f, computed by the
+    plain definition, one token at a time.
 
     ``reverse=True`` is the reverse-direction scan of the bidirectional stage-1
     model (summary page, section 局限与改进): the frames are visited from the
@@ -104,7 +104,7 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
         q, k, v, beta, gamma = (_f32(x) for x in (q, k, v, beta, gamma))
         F = gamma.shape[1]
         o, S_out = frame_fwd(*(_flip_frames(x, F) for x in (q, k, v, beta, gamma)), S_in, N=N, key_scale=key_scale,
-                             formulation=formulation, mode=mode, sub=sub)
+                             formulation=formulation, mode=mode)
         return _flip_frames(o, F), S_out
     q, k, v, beta, gamma, S_in = (_f32(x) for x in (q, k, v, beta, gamma, S_in))
     B, FN, H, D = _shapes(q)
@@ -118,7 +118,7 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
     S_out = np.zeros((B, H, D, D), np.float64)
     if mode == "product":
         _load().oracle_gdn_frame_fwd_product(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(S_in),
-                                             B, H, F, N, D, float(key_scale), int(sub), _ptr(o), _ptr(S_out))
+                                             B, H, F, N, D, float(key_scale), _ptr(o), _ptr(S_out))
         return o, S_out
     assert mode == "sum", mode
     fn = {"recurrence": _load().oracle_gdn_frame_fwd,
@@ -128,10 +128,10 @@ def frame_fwd(q, k, v, beta, gamma, S_in=None, N=None, key_scale=0.0, formulatio
     return o, S_out
 
 
-def frame_transitions(k, v, beta, gamma, key_scale=0.0, mode="sum", sub=64):
+def frame_transitions(k, v, beta, gamma, key_scale=0.0, mode="sum"):
     """Per-frame (M_f, U_f), each [B, H, F, D, D] fp64 (module 2: M_t = gamma_t I - K^ beta K^T).
 
-    ``mode`` as in ``frame_fwd``; ``sub`` is the UT-transform sub-chunk of the product reading.
+    ``mode`` as in ``frame_fwd``.
     """
     k, v, beta, gamma = (_f32(x) for x in (k, v, beta, gamma))
     B, FN, H, D = _shapes(k)
@@ -141,7 +141,7 @@ def frame_transitions(k, v, beta, gamma, key_scale=0.0, mode="sum", sub=64):
     U = np.zeros((B, H, F, D, D), np.float64)
     if mode == "product":
         _load().oracle_gdn_frame_transitions_product(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),
-                                                     B, H, F, N, D, float(key_scale), int(sub), _ptr(M), _ptr(U))
+                                                     B, H, F, N, D, float(key_scale), _ptr(M), _ptr(U))
         return M, U
     assert mode == "sum", mode
     _load().oracle_gdn_frame_transitions(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma),

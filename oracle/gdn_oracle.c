@@ -278,102 +278,57 @@ void oracle_gdn_compose(const double *C1, const double *H1, const double *C2,
  * beta_t between K^_t and K^_t^T.  Read with beta_t = diag(beta) this is the sum
  * form above.  The token-wise Gated DeltaNet that the frame-wise one
  * generalises (novelty section) instead applies the frame's tokens one after
- * another, S <- S (I - beta_n k^_n k^_n^T) + beta_n v_n k^_n^T.  Over a run of
- * tokens that product has the WY form
- *     prod_n (I - beta_n k^_n k^_n^T) = I - K^ T K^^T,  state input V T K^^T,
- * with the UT transform T = (I + StrictLower(diag(beta) K^^T K^))^-1 diag(beta)
- * (the same printed shape with beta_t replaced by the matrix T).  This reading
+ * another, S <- S (I - beta_n k^_n k^_n^T) + beta_n v_n k^_n^T.  This reading
  * keeps the frame's decay where the printed formula puts it:
- *     M_f = gamma_f I - (I - prod_n (I - beta_n k^_n k^_n^T)),
- *     U_f = state reached from zero by the frame's tokens in order.
- * The product is accumulated over sub-chunks of `sub` tokens.  Each sub-chunk
- * forms its T explicitly (forward substitution of the unit lower-triangular
- * matrix), then updates the pair (Abar = I - P, W) of the frame so far:
- *     Abar <- Abar + (K_c - Abar K_c) T_c^T K_c^T,   W <- W + (V_c - W K_c) T_c^T K_c^T,
- * the delta rule applied to the pair with the keys themselves as Abar's values.
+ *     P_f = (I - beta_1 k^_1 k^_1^T) (I - beta_2 k^_2 k^_2^T) ... (I - beta_N k^_N k^_N^T),
+ *     M_f = gamma_f I - (I - P_f),
+ *     U_f = the state the frame's tokens reach from zero, in token order.
+ * Both are built here by the plain definition, one token at a time: the
+ * product P is multiplied on the right by the token's factor, and W (which
+ * ends as U_f) takes the token's delta-rule write.
  */
 static void frame_transition_product(const float *k, const float *v, const float *beta,
                                      const float *gamma, int b, int h, int f,
-                                     int H, int F, int N, int D, double c, int sub,
+                                     int H, int F, int N, int D, double c,
                                      double *M, double *U)
 {
-    if (sub < 1) sub = 1;
-    double *Ab = calloc((size_t)D * D, sizeof(double));       /* Abar = I - P */
-    double *Kc = malloc(sizeof(double) * sub * D);              /* sub-chunk keys k^ */
-    double *Bc = malloc(sizeof(double) * sub);
-    double *L = malloc(sizeof(double) * sub * sub);             /* I + StrictLower(diag(b) G) */
-    double *T = malloc(sizeof(double) * sub * sub);             /* L^-1 diag(b) */
-    double *Ra = malloc(sizeof(double) * sub * D);              /* rows: k_n - Abar k_n */
-    double *Rw = malloc(sizeof(double) * sub * D);              /* rows: v_n - W k_n */
-    double *Xa = malloc(sizeof(double) * sub * D);              /* T (K - Abar K)^T rows */
-    double *Xw = malloc(sizeof(double) * sub * D);
-    memset(U, 0, sizeof(double) * D * D);                       /* W */
-    for (int n0 = 0; n0 < N; n0 += sub) {
-        int m = N - n0 < sub ? N - n0 : sub;
-        for (int a = 0; a < m; ++a) {
-            normalise(k + tok_index(b, f, n0 + a, h, 0, F, N, H, D), D, c, Kc + (size_t)a * D);
-            Bc[a] = beta[beta_index(b, f, n0 + a, h, F, N, H)];
+    double *P = calloc((size_t)D * D, sizeof(double));         /* running product */
+    double *kh = malloc(sizeof(double) * D);
+    double *Pk = malloc(sizeof(double) * D);                    /* P k^_n */
+    double *Wk = malloc(sizeof(double) * D);                    /* W k^_n */
+    for (int i = 0; i < D; ++i) P[i * D + i] = 1.0;
+    memset(U, 0, sizeof(double) * D * D);                       /* W starts at zero */
+    for (int n = 0; n < N; ++n) {
+        normalise(k + tok_index(b, f, n, h, 0, F, N, H, D), D, c, kh);
+        const float *vn = v + tok_index(b, f, n, h, 0, F, N, H, D);
+        double bn = beta[beta_index(b, f, n, h, F, N, H)];
+        for (int i = 0; i < D; ++i) {
+            double sp = 0.0, sw = 0.0;
+            for (int j = 0; j < D; ++j) {
+                sp += P[i * D + j] * kh[j];
+                sw += U[i * D + j] * kh[j];
+            }
+            Pk[i] = sp;
+            Wk[i] = sw;
         }
-        /* L = I + StrictLower(diag(beta) K^T K) */
-        for (int a = 0; a < m; ++a)
-            for (int e = 0; e < m; ++e) {
-                double g = 0.0;
-                if (e < a)
-                    for (int d = 0; d < D; ++d) g += Kc[(size_t)a * D + d] * Kc[(size_t)e * D + d];
-                L[a * sub + e] = (a == e) ? 1.0 : (e < a ? Bc[a] * g : 0.0);
+        /* P <- P (I - b k k^T);   W <- W (I - b k k^T) + b v k^T */
+        for (int i = 0; i < D; ++i)
+            for (int j = 0; j < D; ++j) {
+                P[i * D + j] -= bn * Pk[i] * kh[j];
+                U[i * D + j] += bn * ((double)vn[i] - Wk[i]) * kh[j];
             }
-        /* T = L^-1 diag(beta): column e solves L t = beta_e e_e by forward substitution */
-        for (int e = 0; e < m; ++e)
-            for (int a = 0; a < m; ++a) {
-                double s = (a == e) ? Bc[e] : 0.0;
-                for (int r = 0; r < a; ++r) s -= L[a * sub + r] * T[r * sub + e];
-                T[a * sub + e] = s;
-            }
-        /* residual rows against the pair's sub-chunk-start values */
-        for (int a = 0; a < m; ++a) {
-            const float *vn = v + tok_index(b, f, n0 + a, h, 0, F, N, H, D);
-            const double *ka = Kc + (size_t)a * D;
-            for (int i = 0; i < D; ++i) {
-                double sa = 0.0, sw = 0.0;
-                for (int j = 0; j < D; ++j) {
-                    sa += Ab[i * D + j] * ka[j];
-                    sw += U[i * D + j] * ka[j];
-                }
-                Ra[(size_t)a * D + i] = ka[i] - sa;
-                Rw[(size_t)a * D + i] = (double)vn[i] - sw;
-            }
-        }
-        /* new values X = T R (rows indexed by token) */
-        for (int a = 0; a < m; ++a)
-            for (int i = 0; i < D; ++i) {
-                double sa = 0.0, sw = 0.0;
-                for (int r = 0; r < m; ++r) {
-                    sa += T[a * sub + r] * Ra[(size_t)r * D + i];
-                    sw += T[a * sub + r] * Rw[(size_t)r * D + i];
-                }
-                Xa[(size_t)a * D + i] = sa;
-                Xw[(size_t)a * D + i] = sw;
-            }
-        /* pair += X^T K^ */
-        for (int a = 0; a < m; ++a) {
-            const double *ka = Kc + (size_t)a * D;
-            for (int i = 0; i < D; ++i)
-                for (int j = 0; j < D; ++j) {
-                    Ab[i * D + j] += Xa[(size_t)a * D + i] * ka[j];
-                    U[i * D + j] += Xw[(size_t)a * D + i] * ka[j];
-                }
-        }
     }
+    /* M = gamma I - (I - P) = P - (1 - gamma) I */
     double g = gamma[((size_t)b * F + f) * H + h];
-    for (int e = 0; e < D * D; ++e) M[e] = -Ab[e];
-    for (int i = 0; i < D; ++i) M[i * D + i] += g;
-    free(Ab); free(Kc); free(Bc); free(L); free(T); free(Ra); free(Rw); free(Xa); free(Xw);
+    for (int e = 0; e < D * D; ++e) M[e] = P[e];
+    for (int i = 0; i < D; ++i) M[i * D + i] -= 1.0 - g;
+    free(P); free(kh); free(Pk); free(Wk);
 }
 
 /* (M_f, U_f) of the product reading for every (b, f, h): [B][H][F][D][D]. */
 void oracle_gdn_frame_transitions_product(const float *k, const float *v, const float *beta,
                                           const float *gamma, int B, int H, int F, int N,
-                                          int D, double key_scale, int sub,
+                                          int D, double key_scale,
                                           double *M_out, double *U_out)
 {
     double c = oracle_key_scale(key_scale, D, N);
@@ -381,7 +336,7 @@ void oracle_gdn_frame_transitions_product(const float *k, const float *v, const 
     for (int bhf = 0; bhf < B * H * F; ++bhf) {
         int b = bhf / (H * F), h = (bhf / F) % H, f = bhf % F;
         size_t off = (size_t)bhf * D * D;
-        frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c, sub,
+        frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c,
                                  M_out + off, U_out + off);
     }
 }
@@ -393,7 +348,7 @@ void oracle_gdn_frame_transitions_product(const float *k, const float *v, const 
  */
 void oracle_gdn_frame_fwd_product(const float *q, const float *k, const float *v,
                                   const float *beta, const float *gamma, const float *S_in,
-                                  int B, int H, int F, int N, int D, double key_scale, int sub,
+                                  int B, int H, int F, int N, int D, double key_scale,
                                   double *o, double *S_out)
 {
     double c = oracle_key_scale(key_scale, D, N);
@@ -407,7 +362,7 @@ void oracle_gdn_frame_fwd_product(const float *q, const float *k, const float *v
         double *vec = malloc(sizeof(double) * D);
         load_state(S_in, b, h, H, D, S);
         for (int f = 0; f < F; ++f) {
-            frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c, sub, M, U);
+            frame_transition_product(k, v, beta, gamma, b, h, f, H, F, N, D, c, M, U);
             matmul(S, M, Sn, D);
             for (int e = 0; e < D * D; ++e) S[e] = Sn[e] + U[e];
             if (o) frame_output(q, S, b, h, f, H, F, N, D, o, vec);

@@ -124,6 +124,52 @@ def test_host_side_validation_without_gpu(L):
     assert f32(None, fake, fake, fake, fake, None, fake, fake, 1, 1, 1, 1, 16, 0.0, None) == gdn.GDN_ERR_INVALID_ARG
 
 
+def test_noalloc_step_statuses_match_frame_fwd(L):
+    """The scratch-free step reports, for every argument list, the status gdn_frame_fwd
+    (F = 1) reports when given a workspace of the scratch array's size, before any CUDA call:
+    bad sizes, unsupported head sizes, null or misaligned pointers, shapes the size plan
+    refuses, and requests larger than the array."""
+    from gated_deltanet_wise_b300 import gdn
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every case below is refused on the host
+    limit = L.gdn_frame_step_noalloc_limit_bytes()
+    base = dict(q=fake, k=fake, v=fake, beta=fake, gamma=fake, S_in=None, S_out=fake, o=fake)
+    cases = [
+        ((-1, 1, 8, 112), {}), ((1, -2, 8, 112), {}), ((1, 1, -8, 112), {}), ((1, 1, 8, 0), {}),
+        ((1, 1, 8, -112), {}), ((1, 1, 8, 64), {}), ((1, 1, 8, 128), {}), ((-1, 1, 8, 64), {}),
+        ((1, 1, 8, 112), dict(q=None)), ((1, 1, 8, 112), dict(k=P(0x10008))),
+        ((1, 1, 8, 112), dict(beta=P(0x10002))), ((1, 1, 8, 112), dict(S_in=P(0x10004))),
+        ((1, (1 << 20) + 1, 8, 112), {}),                  # more chains than the size plan takes
+        ((1, (1 << 20) + 1, 8, 112), dict(o=None)),        # ... with a bad pointer: the pointer first
+        ((4, 40, 880, 112), {}),                           # 160 chains: larger than the array
+        ((4, 40, 880, 112), dict(v=None)),
+    ]
+    for (B, H, N, D), over in cases:
+        a = dict(base, **over)
+        ptrs = (a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"])
+        st_na = L.gdn_frame_step_noalloc(*ptrs, B, H, N, D, 0.0, None)
+        st_fw = L.gdn_frame_fwd(*ptrs, B, H, 1, N, D, 0.0, fake, limit, None)
+        assert st_na == st_fw, ((B, H, N, D), over, st_na, st_fw)
+        assert st_na != gdn.GDN_OK, ((B, H, N, D), over)
+    assert L.gdn_frame_step_noalloc(*(fake,) * 5, None, fake, fake, 4, 40, 880, 112, 0.0, None) == \
+        gdn.GDN_ERR_WORKSPACE
+    assert L.gdn_frame_step_noalloc(*(fake,) * 5, None, fake, fake, 1, (1 << 20) + 1, 8, 112, 0.0, None) == \
+        gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_backward_frame_limit_refused_on_host(L):
+    """Runs of 65,535 frames or more exceed a grid dimension of the backward's per-frame
+    kernels: refused before anything is enqueued, and the size query says so."""
+    from gated_deltanet_wise_b300 import gdn
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    assert gdn.gdn_frame_bwd_workspace_size(1, 1, 65535, 8, 112) == 2 ** 64 - 1
+    assert gdn.gdn_frame_bwd_workspace_size(1, 1, 65534, 8, 112) not in (0, 2 ** 64 - 1)
+    st = L.gdn_frame_bwd(fake, fake, fake, fake, fake, None, fake, None, fake, fake, fake, fake, fake, None,
+                         1, 1, 65535, 8, 112, 0.0, fake, 1 << 40, None)
+    assert st == gdn.GDN_ERR_UNSUPPORTED
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from gated_deltanet_wise_b300 import gdn
     monkeypatch.setattr(gdn, "_lib", None)

@@ -2,7 +2,7 @@
 (which tests/test_oracle_backward_pins.py checks against finite differences of
 the forward).  Every gradient tensor must match within a relative Frobenius
 error of 5e-3; the cases cover a ragged token tail, several frame chunks, a
-zero and a random dS_out, a non-default key scale, and sampled heads of the
+zero and a random dS_out, a non-default key scale, and four heads of the
 20-head layer."""
 import numpy as np
 import pytest
@@ -64,20 +64,22 @@ def test_backward_without_initial_state():
     _compare(got, ref)
 
 
-def test_backward_layer_size_sampled_head():
-    """The 20-head layer (F=121, N=880); the oracle checks one head (chains are independent)."""
+def test_backward_layer_size_four_heads():
+    """The 20-head layer (F=121, N=880); the oracle checks four heads spread over the
+    layer (chains are independent; first, last and two inner head offsets)."""
     x = make_inputs(1, 20, 121, 880, 112, dtype="bf16", seed=92, device=DEV)
     dO, dS = _upstream(x, 10)
     got = gdn.frame_bwd(x.q, x.k, x.v, x.beta, x.gamma, None, dO, dS)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
-    h = 6
-    sl = lambda t: t[:, :, h:h + 1].contiguous()
+    heads = torch.tensor([0, 6, 13, 19], device=DEV)
+    sl = lambda t: t.index_select(2, heads).contiguous()
     ref = oracle.frame_bwd(sl(x.q), sl(x.k), sl(x.v), sl(x.beta), sl(x.gamma), None, sl(dO),
-                           dS[:, h:h + 1].contiguous())
-    got_h = [got[0][:, :, h:h + 1], got[1][:, :, h:h + 1], got[2][:, :, h:h + 1], got[3][:, :, h:h + 1],
-             got[4][:, :, h:h + 1], got[5][:, h:h + 1]]
-    _compare(got_h, ref)
+                           dS.index_select(1, heads).contiguous())
+    got_h = [sl(got[0]), sl(got[1]), sl(got[2]), sl(got[3]), sl(got[4]), got[5].index_select(1, heads)]
+    head = lambda t, i, j: t[:, j:j + 1] if i == 5 else t[:, :, j:j + 1]   # dS_in has heads on axis 1
+    for j in range(len(heads)):   # every head on its own
+        _compare([head(g, i, j) for i, g in enumerate(got_h)], [head(r, i, j) for i, r in enumerate(ref)])
 
 
 def test_backward_degenerate_sizes():

@@ -26,8 +26,8 @@ def _inputs(F, N, seed):
 def test_reverse_is_the_transitions_composed_from_the_last_frame(mode):
     F, N, ks = 4, 5, 0.7
     q, k, v, beta, gamma, S0 = _inputs(F, N, 3)
-    o, S = oracle.frame_fwd(q, k, v, beta, gamma, S0, key_scale=ks, mode=mode, sub=3, reverse=True)
-    M, U = oracle.frame_transitions(k, v, beta, gamma, key_scale=ks, mode=mode, sub=3)
+    o, S = oracle.frame_fwd(q, k, v, beta, gamma, S0, key_scale=ks, mode=mode, reverse=True)
+    M, U = oracle.frame_transitions(k, v, beta, gamma, key_scale=ks, mode=mode)
     for h in range(H):
         St = S0[0, h].astype(np.float64)
         for f in reversed(range(F)):
