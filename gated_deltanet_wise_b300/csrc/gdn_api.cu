@@ -230,18 +230,30 @@ gdn_status_t gdn_frame_bwd(const void *q, const void *k, const void *v, const fl
 }
 
 // Device staging of the host-buffer form: q, k, v, o (bf16), beta, gamma,
-// S_in, S_out (fp32), then the workspace, each 256-byte aligned.
+// S_in, S_out (fp32), then the workspace, each 256-byte aligned.  The frames
+// are cut into pieces that are copied in, run and copied out as a pipeline, so
+// the token tensors are staged piece-major: piece p holds its frames as a
+// [B][F_p*N][H][D] (or [B][F_p*N][H], [B][F_p][H]) tensor of its own.
 struct HostLayout {
+    int pieces;
     size_t tok, beta, gamma, state, ws;
     size_t off_q, off_k, off_v, off_o, off_beta, off_gamma, off_sin, off_sout, off_ws, total;
 };
 
+// Frames [piece_f0(p), piece_f0(p + 1)) form piece p; pieces differ by at most one frame.
+static int piece_f0(int p, int pieces, int F) { return (int)((long long)F * p / pieces); }
+
+// Pieces of at least 16 frames (so that each piece's forward still fills the
+// GPU), at most 8 (beyond that the per-piece launches stop paying off).
+static int host_pieces(int F) { return F >= 32 ? (F / 16 < 8 ? F / 16 : 8) : 1; }
+
 static bool host_layout(int B, int H, int F, int N, int D, HostLayout *L)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return false;
-    const size_t ws = gdn_frame_fwd_workspace_size(B, H, F, N, D);
+    const size_t ws = gdn_frame_fwd_workspace_size(B, H, F, N, D);  // covers every piece's plan
     if (ws == (size_t)-1) return false;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    L->pieces = host_pieces(F);
     L->tok = (size_t)B * F * N * H * D * 2;
     L->beta = (size_t)B * F * N * H * 4;
     L->gamma = (size_t)B * F * H * 4;
@@ -260,6 +272,46 @@ static bool host_layout(int B, int H, int F, int N, int D, HostLayout *L)
     L->total = o;
     return true;
 }
+
+namespace gdn {
+namespace {
+// Per-device copy streams and events of the host-buffer entry, created on
+// first use (never destroyed: they live as long as the process, like the
+// library's other per-device state).  Calls are enqueued under a mutex, so
+// concurrent callers cannot interleave their event records.
+constexpr int kMaxPieces = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, in_done[kMaxPieces] = {}, run_done[kMaxPieces] = {}, out_done = nullptr;
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+cudaError_t host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    HostPipe &P = g_pipe[dev];
+    if (!P.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&P.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&P.start, ef)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&P.out_done, ef)) != cudaSuccess) return e;
+        for (int i = 0; i < kMaxPieces; ++i) {
+            if ((e = cudaEventCreateWithFlags(&P.in_done[i], ef)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&P.run_done[i], ef)) != cudaSuccess) return e;
+        }
+        P.ready = true;
+    }
+    *out = &P;
+    return cudaSuccess;
+}
+}  // namespace
+}  // namespace gdn
 
 size_t gdn_frame_fwd_host_buffer_size(int B, int H, int F, int N, int D)
 {
@@ -282,25 +334,61 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v, con
     if (F > 0 && !gamma) return GDN_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *d = static_cast<uint8_t *>(device_buffer);
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *P = nullptr;
+    if (host_pipe(&P) != cudaSuccess) return GDN_ERR_CUDA;
+    // The copy streams start after everything already on `stream`.
+    if (cudaEventRecord(P->start, st) != cudaSuccess || cudaStreamWaitEvent(P->in, P->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(P->out, P->start, 0) != cudaSuccess)
+        return GDN_ERR_CUDA;
     auto h2d = [&](size_t off, const void *src, size_t n) {
-        return n == 0 || cudaMemcpyAsync(d + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+        return n == 0 || cudaMemcpyAsync(d + off, src, n, cudaMemcpyHostToDevice, P->in) == cudaSuccess;
     };
     auto d2h = [&](void *dst, size_t off, size_t n) {
-        return n == 0 || cudaMemcpyAsync(dst, d + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        return n == 0 || cudaMemcpyAsync(dst, d + off, n, cudaMemcpyDeviceToHost, P->out) == cudaSuccess;
     };
-    if (has_tokens && (!h2d(L.off_q, q, L.tok) || !h2d(L.off_k, k, L.tok) || !h2d(L.off_v, v, L.tok) ||
-                       !h2d(L.off_beta, beta, L.beta)))
-        return GDN_ERR_CUDA;
-    if (F > 0 && !h2d(L.off_gamma, gamma, L.gamma)) return GDN_ERR_CUDA;
+    float *d_sin = S_in ? reinterpret_cast<float *>(d + L.off_sin) : nullptr;
+    float *d_sout = reinterpret_cast<float *>(d + L.off_sout);
     if (S_in && !h2d(L.off_sin, S_in, L.state)) return GDN_ERR_CUDA;
-    gdn_status_t s = frame_fwd_impl(d + L.off_q, d + L.off_k, d + L.off_v, reinterpret_cast<float *>(d + L.off_beta),
-                                    reinterpret_cast<float *>(d + L.off_gamma),
-                                    S_in ? reinterpret_cast<float *>(d + L.off_sin) : nullptr,
-                                    reinterpret_cast<float *>(d + L.off_sout), d + L.off_o, B, H, F, N, D, key_scale, 0,
-                                    L.ws ? d + L.off_ws : nullptr, L.ws, stream, nullptr);
-    if (s != GDN_OK) return s;
-    if (has_tokens && o && !d2h(o, L.off_o, L.tok)) return GDN_ERR_CUDA;
+    const int pieces = has_tokens ? L.pieces : 1;
+    const size_t row = (size_t)N * H;  // token-head rows per frame
+    for (int p = 0; p < pieces; ++p) {
+        const int f0 = piece_f0(p, pieces, F), fp = piece_f0(p + 1, pieces, F) - f0;
+        // piece p's region starts after the pieces before it: B * f0 frames' worth of each tensor
+        const size_t tb = (size_t)B * f0 * row * D * 2, bb = (size_t)B * f0 * row * 4, gb = (size_t)B * f0 * H * 4;
+        for (int b = 0; b < B; ++b) {
+            const size_t hs = ((size_t)b * F + f0) * row, ds = (size_t)b * fp * row;  // first row: host, piece
+            if (has_tokens &&
+                (!h2d(L.off_q + tb + ds * D * 2, static_cast<const uint8_t *>(q) + hs * D * 2, (size_t)fp * row * D * 2) ||
+                 !h2d(L.off_k + tb + ds * D * 2, static_cast<const uint8_t *>(k) + hs * D * 2, (size_t)fp * row * D * 2) ||
+                 !h2d(L.off_v + tb + ds * D * 2, static_cast<const uint8_t *>(v) + hs * D * 2, (size_t)fp * row * D * 2) ||
+                 !h2d(L.off_beta + bb + ds * 4, beta + hs, (size_t)fp * row * 4)))
+                return GDN_ERR_CUDA;
+            if (fp > 0 && !h2d(L.off_gamma + gb + (size_t)b * fp * H * 4, gamma + ((size_t)b * F + f0) * H,
+                               (size_t)fp * H * 4))
+                return GDN_ERR_CUDA;
+        }
+        if (cudaEventRecord(P->in_done[p], P->in) != cudaSuccess || cudaStreamWaitEvent(st, P->in_done[p], 0) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        // piece p continues from the state piece p - 1 left in S_out (S_out may alias S_in)
+        gdn_status_t s = frame_fwd_impl(d + L.off_q + tb, d + L.off_k + tb, d + L.off_v + tb,
+                                        reinterpret_cast<float *>(d + L.off_beta + bb),
+                                        reinterpret_cast<float *>(d + L.off_gamma + gb), p == 0 ? d_sin : d_sout,
+                                        d_sout, d + L.off_o + tb, B, H, fp, N, D, key_scale, 0,
+                                        L.ws ? d + L.off_ws : nullptr, L.ws, stream, nullptr);
+        if (s != GDN_OK) return s;
+        if (cudaEventRecord(P->run_done[p], st) != cudaSuccess || cudaStreamWaitEvent(P->out, P->run_done[p], 0) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        for (int b = 0; b < B && has_tokens && o; ++b) {
+            const size_t hs = ((size_t)b * F + f0) * row, ds = (size_t)b * fp * row;
+            if (!d2h(static_cast<uint8_t *>(o) + hs * D * 2, L.off_o + tb + ds * D * 2, (size_t)fp * row * D * 2))
+                return GDN_ERR_CUDA;
+        }
+    }
     if (S_out && !d2h(S_out, L.off_sout, L.state)) return GDN_ERR_CUDA;
+    // `stream` completes only once the last copy out has landed
+    if (cudaEventRecord(P->out_done, P->out) != cudaSuccess || cudaStreamWaitEvent(st, P->out_done, 0) != cudaSuccess)
+        return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

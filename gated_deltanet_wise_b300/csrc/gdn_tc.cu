@@ -44,11 +44,22 @@ namespace gdn {
 
 // ------------------------------------------------------------------ sizes
 // K1
-constexpr int kTS = 32;                               // tokens per stage
-constexpr uint32_t kTSPanel = kTS * kRowB;            // 4096: one 64-column panel of a stage
-constexpr uint32_t kStageBytes = 8 * kTSPanel;        // K->K^, V, B_hi, B_lo (2 panels each) = 32768
+#ifndef GDN_K1_TS
+#define GDN_K1_TS 32
+#endif
+#ifndef GDN_K1_STAGES
+#define GDN_K1_STAGES 6
+#endif
+#ifndef GDN_K1_LO
+#define GDN_K1_LO 1
+#endif
+constexpr int kTS = GDN_K1_TS;                        // tokens per stage (one TMA box height)
+constexpr bool kK1Lo = GDN_K1_LO != 0;                // B as bf16 hi + lo (fp32-accurate U_f)
+constexpr uint32_t kTSPanel = kTS * kRowB;            // one 64-column panel of a stage
+constexpr uint32_t kStageBytes = (kK1Lo ? 8 : 6) * kTSPanel;  // K->K^, V, B_hi[, B_lo] (2 panels each)
 constexpr uint32_t kOffK = 0, kOffV = 2 * kTSPanel, kOffBhi = 4 * kTSPanel, kOffBlo = 6 * kTSPanel;
-constexpr int kK1Stages = 6;
+constexpr int kK1Stages = GDN_K1_STAGES;
+static_assert(kTS % 32 == 0 && kTS <= 128, "K1 stage height");
 constexpr int kK1Threads = 448;                       // producer, MMA, 2 x 4 prep warps, 4 epilogue warps
 constexpr uint32_t kK1OffAimg = kK1Stages * kStageBytes;   // 196608
 constexpr uint32_t kK1OffBar = kK1OffAimg + kAimgBytes;    // 225280
@@ -56,13 +67,32 @@ constexpr uint32_t kK1Smem = kK1OffBar + 256 + 1024;
 
 // K2
 constexpr int kTQ = 128;                              // tokens per Q/O tile
-constexpr int kK2QStages = 2;                         // Q tiles in flight
+#ifndef GDN_K2_QSTAGES
+#define GDN_K2_QSTAGES 2
+#endif
+#ifndef GDN_K2_OSTAGES
+#define GDN_K2_OSTAGES 2
+#endif
+#ifndef GDN_K2_SLO
+#define GDN_K2_SLO 1
+#endif
+#ifndef GDN_K2_SBUF
+#define GDN_K2_SBUF 1
+#endif
+constexpr int kK2QStages = GDN_K2_QSTAGES;            // Q tiles in flight
+constexpr int kK2OStages = GDN_K2_OSTAGES;            // output staging tiles (0: rows stored from registers)
+constexpr bool kK2Lo = GDN_K2_SLO != 0;               // S as bf16 hi + lo images
+constexpr int kK2SBuf = GDN_K2_SBUF;                  // S image sets (2: the next state's images are
+                                                      // written while the previous frame's outputs run)
+static_assert(kK2QStages >= 2 && kK2QStages <= 4 && kK2OStages >= 0 && kK2OStages <= 2, "K2 rings");
+static_assert(kK2SBuf == 1 || kK2SBuf == 2, "K2 S image sets");
 constexpr int kK2Threads = 320;                       // producers, MMA, 4 state warps, 4 output warps
-constexpr uint32_t kK2OffO = kK2QStages * kImgBytes;       // 65536: two output staging tiles
-constexpr uint32_t kK2OffA = kK2OffO + 2 * kImgBytes;      // 131072
-constexpr uint32_t kK2OffShi = kK2OffA + kAimgBytes;       // 159744
-constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // 192512
-constexpr uint32_t kK2OffBar = kK2OffSlo + kImgBytes;      // 225280
+constexpr uint32_t kK2OffO = kK2QStages * kImgBytes;       // output staging tiles
+constexpr uint32_t kK2OffA = kK2OffO + kK2OStages * kImgBytes;
+constexpr uint32_t kK2SetBytes = (kK2Lo ? 2 : 1) * kImgBytes;  // one S image set: hi [, lo]
+constexpr uint32_t kK2OffShi = kK2OffA + kAimgBytes;
+constexpr uint32_t kK2OffSlo = kK2OffShi + kImgBytes;      // lo image of set 0 (set i at + i * kK2SetBytes)
+constexpr uint32_t kK2OffBar = kK2OffShi + kK2SBuf * kK2SetBytes;
 constexpr uint32_t kK2Smem = kK2OffBar + 256 + 1024;
 static_assert(kK2OffShi % 1024 == 0 && kK2OffA % 1024 == 0, "K2 smem layout");
 static_assert(kK1Smem <= kMaxSmem && kK2Smem <= kMaxSmem, "shared memory budget");
@@ -183,7 +213,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
                         mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffK + o, kTSPanel, 1024), bhi, kIdescMN, acc);
                         mma_bf16(tmem + kTmAccU, av, bhi, kIdescMN, acc);
-                        mma_bf16(tmem + kTmAccU, av, blo, kIdescMN, 1u);
+                        if (kK1Lo) mma_bf16(tmem + kTmAccU, av, blo, kIdescMN, 1u);
                     }
                     mma_commit(&st_empty[s]);
                 }
@@ -210,25 +240,35 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // prepared at once.  Thread (token r, quarter qq) handles panel qq>>1,
         // chunks 4*(qq&1).. of its token; the eight threads of a quarter-warp
         // phase touch eight different bank groups.
+        constexpr int kTH = kTS / 32;              // 32-token rows of a stage per thread
         const int grpi = (warp - 2) >> 2;          // 0: even stages, 1: odd stages
         const int t = threadIdx.x - 64 - 128 * grpi;  // 0..127
-        const int r = t >> 2, qq = t & 3;
-        const uint32_t prep_off = (qq >> 1) * kTSPanel + r * kRowB;
+        const int r0 = t >> 2, qq = t & 3;
         const size_t FN = (size_t)p.F * p.N;
         const int total = nf * n_st;
-        auto load_beta = [&](int itx) -> float {
+        auto load_beta = [&](int itx, int r) -> float {
             if (itx >= total) return 0.f;
             const int fl = itx / n_st, n = (itx - fl * n_st) * kTS + r;
             if (n >= p.N) return 0.f;
             return __ldg(p.beta + ((size_t)b * FN + (size_t)frame_at(f_begin + fl, p.F, p.reverse) * p.N + n) * p.H + h);
         };
-        float bt_next = load_beta(grpi);
+        float bt_next[kTH];
+#pragma unroll
+        for (int hh = 0; hh < kTH; ++hh) bt_next[hh] = load_beta(grpi, r0 + 32 * hh);
         for (int it = grpi; it < total; it += 2) {
             const int s = it % kK1Stages, use = it / kK1Stages;
-            const float bt = bt_next;
-            bt_next = load_beta(it + 2);
+            float bts[kTH];
+#pragma unroll
+            for (int hh = 0; hh < kTH; ++hh) {
+                bts[hh] = bt_next[hh];
+                bt_next[hh] = load_beta(it + 2, r0 + 32 * hh);
+            }
             if (!mbar_wait_warp(&st_full[s], use & 1, abort_flag)) break;
-            uint8_t *stg = sm + s * kStageBytes + prep_off;
+#pragma unroll
+            for (int hh = 0; hh < kTH; ++hh) {
+            const int r = r0 + 32 * hh;
+            const float bt = bts[hh];
+            uint8_t *stg = sm + s * kStageBytes + (qq >> 1) * kTSPanel + r * kRowB;
             float kf[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -251,11 +291,16 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                     kh[e] = inv * kf[8 * i + e];
                     y[e] = wb * kf[8 * i + e];
                 }
-                uint4 hi, lo;
-                split_bf16x8(y, hi, lo);
                 *reinterpret_cast<uint4 *>(stg + kOffK + pos) = f32x8_to_bf16(kh);
-                *reinterpret_cast<uint4 *>(stg + kOffBhi + pos) = hi;
-                *reinterpret_cast<uint4 *>(stg + kOffBlo + pos) = lo;
+                if (kK1Lo) {
+                    uint4 hi, lo;
+                    split_bf16x8(y, hi, lo);
+                    *reinterpret_cast<uint4 *>(stg + kOffBhi + pos) = hi;
+                    *reinterpret_cast<uint4 *>(stg + kOffBlo + pos) = lo;
+                } else {
+                    *reinterpret_cast<uint4 *>(stg + kOffBhi + pos) = f32x8_to_bf16(y);
+                }
+            }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -492,6 +537,7 @@ __global__ void __launch_bounds__(kK1bThreads)
 
 // ===================================================================== K2
 struct K2Params {
+    void *o;  // bf16 output (row stores when the kernel is built without output staging)
     const float *gamma;
     const uint8_t *ws_frames;
     const float *ws_start;
@@ -513,11 +559,13 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK2OffBar);
-    uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages, *a_full = bars + 4, *a_empty = bars + 5;
-    uint64_t *s_ready = bars + 6, *accS_full = bars + 7, *o_done = bars + 8;
-    uint64_t *o_full = bars + 9, *o_free = bars + 12, *drain = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+    uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages;
+    uint64_t *a_full = bars + 2 * kK2QStages, *a_empty = a_full + 1;
+    // o_done[m]: the MMAs of iteration j (outputs of frame j - 1) have completed, for j % kK2SBuf == m
+    uint64_t *s_ready = a_full + 2, *accS_full = a_full + 3, *o_done = a_full + 4;
+    uint64_t *o_full = a_full + 6, *o_free = a_full + 9, *drain = a_full + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(a_full + 13);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(a_full + 14);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = p.B * p.H;
@@ -537,7 +585,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         mbar_init(a_empty, 1);
         mbar_init(s_ready, 4);
         mbar_init(accS_full, 1);
-        mbar_init(o_done, 1);
+        for (int i = 0; i < kK2SBuf; ++i) mbar_init(&o_done[i], 1);
         for (int i = 0; i < 3; ++i) {
             mbar_init(&o_full[i], 1);
             mbar_init(&o_free[i], 4);
@@ -550,7 +598,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         tmem_relinquish();
     }
     // zero the S images (rows 112..127 and key columns 112..127 stay zero)
-    for (int o = threadIdx.x * 16; o < 2 * (int)kImgBytes; o += kK2Threads * 16)
+    for (int o = threadIdx.x * 16; o < kK2SBuf * (int)kK2SetBytes; o += kK2Threads * 16)
         *reinterpret_cast<uint4 *>(sm + kK2OffShi + o) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     tc_fence_before();
@@ -612,13 +660,14 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                 if (it < nf) {
                     if (!(ok = mbar_wait(a_full, it & 1, abort_flag))) break;
                     tc_fence_after();
+                    const uint32_t sset = (uint32_t)(it % kK2SBuf) * kK2SetBytes;
 #pragma unroll
                     for (int ks = 0; ks < 7; ++ks) {
                         const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
                         const uint64_t bd =
                             sdesc_sw128(sbase + kK2OffA + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
-                        mma_bf16(tmem, sdesc_sw128(sbase + kK2OffShi + koff, 16, 1024), bd, kIdescK, ks > 0);
-                        mma_bf16(tmem, sdesc_sw128(sbase + kK2OffSlo + koff, 16, 1024), bd, kIdescK, 1);
+                        mma_bf16(tmem, sdesc_sw128(sbase + kK2OffShi + sset + koff, 16, 1024), bd, kIdescK, ks > 0);
+                        if (kK2Lo) mma_bf16(tmem, sdesc_sw128(sbase + kK2OffSlo + sset + koff, 16, 1024), bd, kIdescK, 1);
                     }
                     mma_commit(accS_full);
                     mma_commit(a_empty);
@@ -631,17 +680,19 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                         tc_fence_after();
                         const uint32_t acc = tmem + 128 * (slot + 1);
                         const uint32_t qb = sbase + s * kImgBytes;
+                        const uint32_t sset = (uint32_t)(it % kK2SBuf) * kK2SetBytes;  // S_{it-1}: image set of iteration it
 #pragma unroll
                         for (int ks = 0; ks < 7; ++ks) {
                             const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
                             const uint64_t ad = sdesc_sw128(qb + koff, 16, 1024);
-                            mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffShi + koff, 16, 1024), kIdescK, ks > 0);
-                            mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffSlo + koff, 16, 1024), kIdescK, 1);
+                            mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffShi + sset + koff, 16, 1024), kIdescK, ks > 0);
+                            if (kK2Lo)
+                                mma_bf16(acc, ad, sdesc_sw128(sbase + kK2OffSlo + sset + koff, 16, 1024), kIdescK, 1);
                         }
                         mma_commit(&o_full[slot]);
                         mma_commit(&q_empty[s]);
                     }
-                    if (ok) mma_commit(o_done);
+                    if (ok) mma_commit(&o_done[it % kK2SBuf]);
                 }
             }
             mma_commit(drain);  // every MMA issued above has completed once this phase lands
@@ -668,15 +719,20 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             S[j + 2] = v4.z;
             S[j + 3] = v4.w;
         }
-        auto write_images = [&]() {
+        auto write_images = [&](int set) {
             if (row < kD) {
+                const uint32_t sset = (uint32_t)set * kK2SetBytes;
 #pragma unroll
                 for (int c8 = 0; c8 < kD / 8; ++c8) {
-                    uint4 hi, lo;
-                    split_bf16x8(S + 8 * c8, hi, lo);
-                    const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
-                    *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = hi;
-                    *reinterpret_cast<uint4 *>(sm + kK2OffSlo + off) = lo;
+                    const uint32_t off = sset + (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
+                    if (kK2Lo) {
+                        uint4 hi, lo;
+                        split_bf16x8(S + 8 * c8, hi, lo);
+                        *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = hi;
+                        *reinterpret_cast<uint4 *>(sm + kK2OffSlo + off) = lo;
+                    } else {
+                        *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = f32x8_to_bf16(S + 8 * c8);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -684,7 +740,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(s_ready);
         };
-        write_images();
+        write_images(0);
         const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
         float g_next = __ldg(gam + (size_t)frame_at(f_begin, p.F, p.reverse) * p.H);
         for (int it = 0; it < nf; ++it) {
@@ -728,8 +784,17 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 #pragma unroll
                 for (int j = 0; j < kD / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
             }
-            if (it >= 1 && !mbar_wait_warp(o_done, (it - 1) & 1, abort_flag)) break;
-            write_images();
+            // S_it goes into image set (it + 1) % kK2SBuf, which MMA iteration it + 1 - kK2SBuf
+            // read last: with one set, wait for this iteration's outputs (frame it - 1); with
+            // two, for the previous iteration's (frame it - 2), whose images are the other set.
+            {
+                // MMA iteration j commits o_done[j % kK2SBuf], whose phase (j - 1) / kK2SBuf it completes;
+                // the next commit there (iteration j + kK2SBuf = it + 1) needs this iteration's images,
+                // so the phase waited for is always the latest one of that barrier.
+                const int j = it + 1 - kK2SBuf;
+                if (j >= 1 && !mbar_wait_warp(&o_done[j % kK2SBuf], ((j - 1) / kK2SBuf) & 1, abort_flag)) break;
+            }
+            write_images((it + 1) % kK2SBuf);
         }
         if (p.S_out && chunk_idx + 1 == p.n_chunks && row < kD) {
             float *dst = p.S_out + (size_t)bh * kStateFloats + row * kD;
@@ -758,7 +823,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             for (int t = 0; t < n_tiles; ++t, ++qc) {
                 const int s = qc % kK2QStages, slot = qc % 3;
                 const uint8_t *qs = sm + s * kImgBytes;
-                uint8_t *os = sm + kK2OffO + (qc & 1) * kImgBytes;
+                uint8_t *os = sm + kK2OffO + (kK2OStages ? qc % kK2OStages : 0) * kImgBytes;
                 if (ok) ok = mbar_wait_warp(&q_full[s], (qc / kK2QStages) & 1, abort_flag);
                 float rq = 0.f;
                 if (ok) {
@@ -778,10 +843,18 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     ok = mbar_wait_warp(&o_full[slot], (qc / 3) & 1, abort_flag);
                 }
                 tc_fence_after();
-                if (leader) bulk_wait_read_le1();  // the store from this staging tile (two tiles ago) has read it
-                out_warps_sync();
+                if (kK2OStages > 0) {
+                    if (leader) {  // the store issued from this staging tile kK2OStages tiles ago has read it
+                        if (kK2OStages == 2) bulk_wait_read_le1();
+                        else bulk_wait_read_all();
+                    }
+                    out_warps_sync();
+                }
                 if (ok) {
                     const uint32_t acc = tmem + 128 * (slot + 1) + lane_off;
+                    const int n = t * kTQ + r;  // token of this row
+                    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) +
+                                                            (((size_t)bf * p.N + n) * p.H + h) * kD);
 #pragma unroll
                     for (int cc = 0; cc < 7; ++cc) {
                         uint32_t ra[16];
@@ -791,16 +864,22 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
                         const int c8 = cc * 2;
-                        *reinterpret_cast<uint4 *>(os + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
-                            f32x8_to_bf16(o);
-                        *reinterpret_cast<uint4 *>(os + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
-                            f32x8_to_bf16(o + 8);
+                        if (kK2OStages > 0) {
+                            *reinterpret_cast<uint4 *>(os + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) =
+                                f32x8_to_bf16(o);
+                            *reinterpret_cast<uint4 *>(os + ((c8 + 1) >> 3) * kImgPanel + sw128_off(r, (c8 + 1) & 7)) =
+                                f32x8_to_bf16(o + 8);
+                        } else if (n < p.N) {  // the row straight to global memory (tail rows past N skipped)
+                            orow[c8] = f32x8_to_bf16(o);
+                            orow[c8 + 1] = f32x8_to_bf16(o + 8);
+                        }
                     }
                 }
-                fence_proxy_async_smem();
+                if (kK2OStages > 0) fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0 && ok) mbar_arrive(&o_free[slot]);
+                if (kK2OStages == 0) continue;
                 out_warps_sync();
                 if (leader && ok) {
                     tma_store_4d(&mapO, os, 0, h, t * kTQ, bf);
@@ -1023,6 +1102,7 @@ static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, cons
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
     K2Params p2;
+    p2.o = o;
     p2.gamma = gamma;
     p2.ws_frames = ws + pl.off_frames;
     p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
@@ -1061,6 +1141,7 @@ cudaError_t launch_states_tc(const void *q, const float *gamma, const float *S_i
                    reinterpret_cast<float *>(ws + pl.off_start), S_in, (float *)nullptr, pl.n_chunks, status);
     if (e != cudaSuccess) return e;
     K2Params p2;
+    p2.o = nullptr;
     p2.gamma = gamma;
     p2.ws_frames = ws + pl.off_frames;
     p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);

@@ -260,10 +260,19 @@ gdn_status_t gdn_frame_fwd_profiled(const void *q, const void *k, const void *v,
  * (pinned memory gives asynchronous copies), o and S_out are host pointers
  * written on completion.  `device_buffer` (caller-owned device memory of
  * gdn_frame_fwd_host_buffer_size() bytes, 256-byte aligned) holds the device
- * copies and the workspace.  The call enqueues the host-to-device copies, the
- * forward pass and the device-to-host copies on `stream` and returns; the
- * results are valid after the stream is synchronised.  S_in may be NULL (zero
- * state); S_out may be NULL.
+ * copies and the workspace.  S_in may be NULL (zero state); S_out may be NULL.
+ * The call enqueues everything and returns; the results are valid after
+ * `stream` is synchronised.  Runs of 32 frames or more are pipelined: the
+ * frames are cut into up to 8 pieces of at least 16 frames, and piece p's
+ * host-to-device copies, piece p-1's forward (on `stream`, continuing from the
+ * state the piece before it left) and piece p-2's device-to-host copies run at
+ * the same time, the copies on two copy streams the library creates once per
+ * device.  The copies start after the work already on `stream`, and `stream`
+ * waits for the last copy out.  The pieces re-associate the state sums like
+ * split gdn_frame_fwd calls (results agree within the stated tolerance, not
+ * bit for bit, with one gdn_frame_fwd call); shorter runs are one piece.  Calls
+ * from several host threads are serialised inside the library while they
+ * enqueue.
  */
 size_t gdn_frame_fwd_host_buffer_size(int B, int H, int F, int N, int D);
 gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,

@@ -211,7 +211,8 @@ def test_profiled_entry_records_stage_events():
 
 
 def test_host_buffer_entry_matches_device_entry():
-    """gdn_frame_fwd_host: pinned host buffers in and out, copies and compute on one stream."""
+    """gdn_frame_fwd_host: pinned host buffers in and out; a run short enough to be one piece
+    equals the device entry bit for bit."""
     x = make_inputs(1, 3, 5, 200, 112, dtype="bf16", seed=6, device=DEV, s0_std=0.1)
     B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
     o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
@@ -224,3 +225,28 @@ def test_host_buffer_entry_matches_device_entry():
     assert st == gdn.GDN_OK
     torch.cuda.synchronize()
     assert torch.equal(ho, o_ref.cpu()) and torch.equal(hS, S_ref.cpu())
+
+
+@pytest.mark.parametrize("B,F,with_s0", [(2, 70, True), (1, 121, False)])
+def test_host_buffer_entry_pipelined_pieces(B, F, with_s0):
+    """Runs of 32+ frames are copied in, run and copied out piece by piece on overlapping
+    streams; batches are gathered per piece.  Every chain against the oracle, twice in a row
+    on one device buffer (the second call must not see the first call's data)."""
+    H, N, D = 2, 96, 112
+    nb = gdn.gdn_frame_fwd_host_buffer_size(B, H, F, N, D)
+    dbuf = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    for call in range(2):
+        x = make_inputs(B, H, F, N, D, dtype="bf16", seed=60 + call + F, device=DEV, s0_std=0.1 if with_s0 else 0.0)
+        hq, hk, hv, hb, hg = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.beta, x.gamma))
+        hs = x.S0.cpu().pin_memory() if with_s0 else None
+        ho = torch.full_like(hq, float("nan")).pin_memory()
+        hS = torch.full((B, H, D, D), float("nan")).pin_memory()
+        st = gdn.gdn_frame_fwd_host(hq, hk, hv, hb, hg, hs, hS, ho, B, H, F, N, D, 0.0, dbuf, nb)
+        assert st == gdn.GDN_OK
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+        for b in range(B):
+            for h in range(H):
+                assert rel_fro(ho[b:b + 1, :, h:h + 1].float().numpy(), o_ref[b:b + 1, :, h:h + 1]) <= TOL_BF16
+                assert rel_fro(hS[b:b + 1, h:h + 1].numpy(), S_ref[b:b + 1, h:h + 1]) <= TOL_BF16
