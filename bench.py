@@ -503,7 +503,68 @@ def measure_variants(x, K, stream, alg, peaks):
                      "steps": K, "gpu_launches_per_step": launches}
         del ws
     out["backward"] = measure_backward(x, max(3, min(K, 10)), stream, peaks)
+    out["block"] = measure_block(x, max(3, min(K, 10)), stream, peaks)
     return out
+
+
+def measure_block(x, K, stream, peaks):
+    """The GDN block with its projections (gdn_block_fwd) at the layer's shape: x [B, F*N, H*D]
+    bf16 with random-init weights W_in [3HD + 2H, HD], W_out [HD, HD]; K calls after 2 warm-ups.
+    Also the two projection GEMMs alone, as tensor-pipe throughput against the bf16 peak."""
+    import torch
+    from gated_deltanet_wise_b300 import gdn
+    from gated_deltanet_wise_b300.inputs import make_block_inputs
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    xb = make_block_inputs(B, H, F, N, D, seed=5, device=x.q.device)
+    HD, M = H * D, B * F * N
+    y = torch.empty_like(xb.x)
+    S = torch.empty(B, H, D, D, dtype=torch.float32, device=x.q.device)
+    nb = gdn.gdn_block_fwd_workspace_size(B, H, F, N, D)
+    ws = torch.empty(nb, dtype=torch.uint8, device=x.q.device)
+    q = torch.empty(B, F * N, H, D, dtype=torch.bfloat16, device=x.q.device)
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    beta = torch.empty(B, F * N, H, device=x.q.device)
+    gamma = torch.empty(B, F, H, device=x.q.device)
+
+    def block():
+        st = gdn.gdn_block_fwd(xb.x, xb.W_in, xb.W_out, None, S, y, B, H, F, N, D, 0.0, ws, nb, stream)
+        if st != gdn.GDN_OK:
+            raise gdn.GdnError(st, "gdn_block_fwd")
+
+    def in_proj():
+        st = gdn.gdn_block_in_proj(xb.x, xb.W_in, q, k, v, beta, gamma, B, H, F, N, D, stream)
+        if st != gdn.GDN_OK:
+            raise gdn.GdnError(st, "gdn_block_in_proj")
+
+    def out_proj():
+        st = gdn.gdn_block_out_proj(q, xb.W_out, y, B, H, F, N, D, stream)
+        if st != gdn.GDN_OK:
+            raise gdn.GdnError(st, "gdn_block_out_proj")
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(K):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / K
+
+    ms_block, ms_in, ms_out = timed(block), timed(in_proj), timed(out_proj)
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    f_in, f_out = 2.0 * M * HD * (3 * HD + 2 * H), 2.0 * M * HD * HD
+    del ws
+    return {"ms_per_step": round(ms_block, 4), "tokens_per_s": round(M / (ms_block * 1e-3), 1),
+            "in_proj": {"ms": round(ms_in, 4), "tflops": round(f_in / (ms_in * 1e-3) / 1e12, 1),
+                        "tensor_frac": round(f_in / (ms_in * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
+            "out_proj": {"ms": round(ms_out, 4), "tflops": round(f_out / (ms_out * 1e-3) / 1e12, 1),
+                         "tensor_frac": round(f_out / (ms_out * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
+            "peak_source": "bf16_tflops (burst) of MEASURED_PEAKS.json",
+            "steps": K, "gpu_launches_per_step": 7, "d_model": HD}
 
 
 def measure_backward(x, K, stream, peaks):

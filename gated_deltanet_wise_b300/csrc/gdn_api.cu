@@ -479,6 +479,115 @@ gdn_status_t gdn_state_compose(const float *S, const float *C, const float *Hc, 
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ block projections
+static bool block_sizes_ok(int B, int H, int F, int N, int D)
+{
+    return B >= 0 && H >= 0 && F >= 0 && N >= 0 && D > 0;
+}
+
+gdn_status_t gdn_block_in_proj(const void *x, const void *W_in, void *q, void *k, void *v, float *beta,
+                               float *gamma, int B, int H, int F, int N, int D, gdn_stream_t stream)
+{
+    if (!block_sizes_ok(B, H, F, N, D)) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || F == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * F * N > (1LL << 30) || H > 512) return GDN_ERR_UNSUPPORTED;
+    if (!x || !W_in || !gamma || (N > 0 && (!q || !k || !v || !beta))) return GDN_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W_in, 16) || !aligned(gamma, 4) ||
+        (N > 0 && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(beta, 4))))
+        return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (N == 0) {  // no tokens: gamma of the frame mean over no tokens is undefined; report it
+        return GDN_ERR_UNSUPPORTED;
+    }
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    return launch_in_proj_tc(x, W_in, q, k, v, beta, gamma, B, H, F, N, status, st) == cudaSuccess ? GDN_OK
+                                                                                             : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_block_out_proj(const void *o, const void *W_out, void *y, int B, int H, int F, int N, int D,
+                                gdn_stream_t stream)
+{
+    if (!block_sizes_ok(B, H, F, N, D)) return GDN_ERR_INVALID_ARG;
+    if ((long long)B * F * N == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * F * N > (1LL << 30) || H > 512) return GDN_ERR_UNSUPPORTED;
+    if (!o || !W_out || !y) return GDN_ERR_INVALID_ARG;
+    if (!aligned(o, 16) || !aligned(W_out, 16) || !aligned(y, 16)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    const int HD = H * D;
+    return launch_linear_tc(o, W_out, y, B * F * N, HD, HD, status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
+}
+
+// Block workspace: q, k, v, o (bf16 [B][F*N][H][D]), beta (fp32), gamma (fp32
+// [B][F][H]), then the forward's workspace; each 256-byte aligned.
+struct BlockLayout {
+    size_t tok, beta, gamma, fwd, off_q, off_k, off_v, off_o, off_beta, off_gamma, off_fwd, total;
+};
+
+static bool block_layout(int B, int H, int F, int N, int D, BlockLayout *L)
+{
+    if (!block_sizes_ok(B, H, F, N, D)) return false;
+    const size_t fwd = gdn_frame_fwd_workspace_size(B, H, F, N, D);
+    if (fwd == (size_t)-1) return false;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    L->tok = (size_t)B * F * N * H * D * 2;
+    L->beta = (size_t)B * F * N * H * 4;
+    L->gamma = (size_t)B * F * H * 4;
+    L->fwd = fwd;
+    size_t o = 0;
+    L->off_q = o; o = up(o + L->tok);
+    L->off_k = o; o = up(o + L->tok);
+    L->off_v = o; o = up(o + L->tok);
+    L->off_o = o; o = up(o + L->tok);
+    L->off_beta = o; o = up(o + L->beta);
+    L->off_gamma = o; o = up(o + L->gamma);
+    L->off_fwd = o; o = up(o + L->fwd);
+    L->total = o;
+    return true;
+}
+
+size_t gdn_block_fwd_workspace_size(int B, int H, int F, int N, int D)
+{
+    BlockLayout L;
+    if (!block_layout(B, H, F, N, D, &L)) return (size_t)-1;
+    if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
+    if (D != 112) return (size_t)-1;
+    return L.total;
+}
+
+gdn_status_t gdn_block_fwd(const void *x, const void *W_in, const void *W_out, const float *S_in, float *S_out,
+                           void *y, int B, int H, int F, int N, int D, float key_scale, void *workspace,
+                           size_t workspace_bytes, gdn_stream_t stream)
+{
+    BlockLayout L;
+    if (!block_layout(B, H, F, N, D, &L)) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if (F == 0)  // no frames: the state passes through (S_out = S_in, or zero)
+        return gdn_frame_fwd(nullptr, nullptr, nullptr, nullptr, nullptr, S_in, S_out, nullptr, B, H, 0, N, D,
+                             key_scale, nullptr, 0, stream);
+    if (N == 0) return GDN_ERR_UNSUPPORTED;  // the frame-mean decay logit needs tokens
+    if (!x || !W_in || !W_out || !y) return GDN_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W_in, 16) || !aligned(W_out, 16) || !aligned(y, 16) ||
+        (S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16)))
+        return GDN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < L.total) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return GDN_ERR_INVALID_ARG;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    void *q = w + L.off_q, *k = w + L.off_k, *v = w + L.off_v, *o = w + L.off_o;
+    float *beta = reinterpret_cast<float *>(w + L.off_beta), *gamma = reinterpret_cast<float *>(w + L.off_gamma);
+    gdn_status_t s = gdn_block_in_proj(x, W_in, q, k, v, beta, gamma, B, H, F, N, D, stream);
+    if (s != GDN_OK) return s;
+    s = gdn_frame_fwd(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, w + L.off_fwd, L.fwd, stream);
+    if (s != GDN_OK) return s;
+    return gdn_block_out_proj(o, W_out, y, B, H, F, N, D, stream);
+}
+
 gdn_status_t gdn_frame_fwd_f32(const float *q, const float *k, const float *v, const float *beta,
                                const float *gamma, const float *S_in, float *S_out, float *o, int B, int H, int F,
                                int N, int D, float key_scale, gdn_stream_t stream)

@@ -23,6 +23,19 @@ unsigned *device_status_word();
 // 4-D TMA view (D, H, N, B*F) of a bf16 [B][F*N][H][D] token tensor, 128-byte
 // swizzle, boxes of 64 head-dim elements x `rows` tokens (gdn_tc.cu).
 bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N, int rows);
+// 2-D view of a bf16 row-major [rows][cols] matrix, 128-byte swizzle, boxes of
+// 64 columns x `box_rows` rows (gdn_tc.cu).
+bool make_matrix_map(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
+
+// Block projections (gdn_proj.cu), tcgen05 GEMMs C = A W^T with bf16 A [M][K]
+// and W [N][K]: the plain form (C bf16 [M][N]) and the input projection of the
+// GDN block, whose epilogue writes q, k, v (bf16 [M][H*112] each), beta =
+// sigmoid(logit) (fp32 [M][H]) and gamma = exp(-softplus(frame mean of the
+// decay logit)) (fp32 [B][F][H]).
+cudaError_t launch_linear_tc(const void *A, const void *W, void *C, int M, int N, int K, unsigned *status,
+                             cudaStream_t stream);
+cudaError_t launch_in_proj_tc(const void *x, const void *W_in, void *q, void *k, void *v, float *beta,
+                              float *gamma, int B, int H, int F, int N, unsigned *status, cudaStream_t stream);
 
 // tensor-core path (gdn_tc.cu); D == 112.
 struct TcPlan {

@@ -45,13 +45,13 @@ namespace gdn {
 // ------------------------------------------------------------------ sizes
 // K1
 #ifndef GDN_K1_TS
-#define GDN_K1_TS 32
+#define GDN_K1_TS 64
 #endif
 #ifndef GDN_K1_STAGES
-#define GDN_K1_STAGES 6
+#define GDN_K1_STAGES 4
 #endif
 #ifndef GDN_K1_LO
-#define GDN_K1_LO 1
+#define GDN_K1_LO 0
 #endif
 constexpr int kTS = GDN_K1_TS;                        // tokens per stage (one TMA box height)
 constexpr bool kK1Lo = GDN_K1_LO != 0;                // B as bf16 hi + lo (fp32-accurate U_f)
@@ -931,6 +931,22 @@ bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N
     cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D view of a bf16 row-major [rows][cols] matrix, 128B swizzle, boxes of
+// 64 columns (one swizzled 128-byte row) x `box_rows` rows.  cols must be a
+// multiple of 8 (16-byte row stride); out-of-range elements load as zero.
+bool make_matrix_map(CUtensorMap *m, const void *base, int rows, int cols, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn || rows <= 0 || cols <= 0 || cols % 8 != 0 || box_rows <= 0 || box_rows > 256) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -35,6 +35,7 @@ EXPORTED = [
     "gdn_frame_fwd_product_workspace_size", "gdn_frame_fwd_product",
     "gdn_frame_fwd_ex_workspace_size", "gdn_frame_fwd_ex",
     "gdn_frame_bwd_workspace_size", "gdn_frame_bwd", "gdn_test_frame_fwd_expired_wait",
+    "gdn_block_in_proj", "gdn_block_out_proj", "gdn_block_fwd_workspace_size", "gdn_block_fwd",
 ]
 
 GDN_FWD_PRODUCT = 1
@@ -100,6 +101,14 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_bwd_workspace_size.argtypes = [I] * 5
         L.gdn_frame_bwd.restype = I
         L.gdn_frame_bwd.argtypes = [P] * 14 + [I] * 5 + [F, P, Z, P]
+        L.gdn_block_in_proj.restype = I
+        L.gdn_block_in_proj.argtypes = [P] * 7 + [I] * 5 + [P]
+        L.gdn_block_out_proj.restype = I
+        L.gdn_block_out_proj.argtypes = [P] * 3 + [I] * 5 + [P]
+        L.gdn_block_fwd_workspace_size.restype = Z
+        L.gdn_block_fwd_workspace_size.argtypes = [I] * 5
+        L.gdn_block_fwd.restype = I
+        L.gdn_block_fwd.argtypes = [P] * 6 + [I] * 5 + [F, P, Z, P]
         L.gdn_test_frame_fwd_expired_wait.restype = I
         L.gdn_test_frame_fwd_expired_wait.argtypes = [P] * 8 + [I] * 5 + [F, P, Z, P]
         _lib = L
@@ -128,6 +137,25 @@ def _check_status(st: int, what: str):
 # ---------------------------------------------------------------- raw C entry points
 def gdn_frame_fwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
     return int(lib().gdn_frame_fwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_block_in_proj(x, W_in, q, k, v, beta, gamma, B, H, F, N, D, stream=None) -> int:
+    return int(lib().gdn_block_in_proj(_p(x), _p(W_in), _p(q), _p(k), _p(v), _p(beta), _p(gamma), B, H, F, N, D,
+                                       _stream(stream)))
+
+
+def gdn_block_out_proj(o, W_out, y, B, H, F, N, D, stream=None) -> int:
+    return int(lib().gdn_block_out_proj(_p(o), _p(W_out), _p(y), B, H, F, N, D, _stream(stream)))
+
+
+def gdn_block_fwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
+    return int(lib().gdn_block_fwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_block_fwd(x, W_in, W_out, S_in, S_out, y, B, H, F, N, D, key_scale, workspace, workspace_bytes,
+                  stream=None) -> int:
+    return int(lib().gdn_block_fwd(_p(x), _p(W_in), _p(W_out), _p(S_in), _p(S_out), _p(y), B, H, F, N, D,
+                                   float(key_scale), _p(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def gdn_test_frame_fwd_expired_wait(q, k, v, beta, gamma, S_in, S_out, o, B, H, F, N, D, key_scale, workspace,
@@ -428,3 +456,29 @@ def state_compose(S, C, Hc, *, out=None, stream=None):
     st = gdn_state_compose(S, C, Hc, out, BH, D, stream)
     _check_status(st, "gdn_state_compose")
     return out
+
+
+def block_fwd(x, W_in, W_out, S_in=None, *, F: int, key_scale: float = 0.0, y=None, S_out=None,
+              workspace: Optional[Workspace] = None, stream=None):
+    """GDN block with its projections (gdn_block_fwd).  x: bf16 [B, F*N, H*D];
+    W_in: bf16 [3*H*D + 2*H, H*D]; W_out: bf16 [H*D, H*D].  Returns (y, S_out)."""
+    _check(x, torch.bfloat16, "x")
+    _check(W_in, torch.bfloat16, "W_in")
+    _check(W_out, torch.bfloat16, "W_out")
+    B, FN, HD = x.shape
+    D = 112
+    H = HD // D
+    N = FN // F
+    if H * D != HD or F * N != FN or W_in.shape != (3 * HD + 2 * H, HD) or W_out.shape != (HD, HD):
+        raise ValueError("block shapes: x [B, F*N, H*112], W_in [3HD+2H, HD], W_out [HD, HD]")
+    if S_in is not None:
+        _check(S_in, torch.float32, "S_in")
+    y = torch.empty_like(x) if y is None else y
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=x.device) if S_out is None else S_out
+    nbytes = gdn_block_fwd_workspace_size(B, H, F, N, D)
+    if nbytes == 2 ** 64 - 1:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_block_fwd_workspace_size")
+    ws = (workspace or _default_ws).get(nbytes, x.device)
+    st = gdn_block_fwd(x, W_in, W_out, S_in, S_out, y, B, H, F, N, D, key_scale, ws, nbytes, stream)
+    _check_status(st, "gdn_block_fwd")
+    return y, S_out

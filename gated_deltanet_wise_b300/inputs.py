@@ -72,3 +72,36 @@ def make_workload(name: str, *, seed: int = 0, device="cpu", F: Optional[int] = 
     B, H, F0, N, D, dtype, s0 = WORKLOADS[name]
     return make_inputs(B, H, F0 if F is None else F, N, D, dtype=dtype, seed=seed,
                        device=device, s0_std=s0)
+
+
+@dataclass
+class BlockInputs:
+    x: torch.Tensor       # [B, F*N, H*D] bf16
+    W_in: torch.Tensor    # [3*H*D + 2*H, H*D] bf16
+    W_out: torch.Tensor   # [H*D, H*D] bf16
+    S0: Optional[torch.Tensor]
+    B: int
+    H: int
+    F: int
+    N: int
+    D: int
+
+
+def make_block_inputs(B: int, H: int, F: int, N: int, D: int = 112, *, seed: int = 0, device="cpu",
+                      s0_std: float = 0.0) -> BlockInputs:
+    """Seeded synthetic block input and random-init weights (no trained weights exist here):
+    x ~ N(0, 1); W_in, W_out ~ N(0, 1 / (H*D)) (unit-variance projections), all rounded to bf16;
+    S_0 = 0 or N(0, s0_std^2)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    HD = H * D
+
+    def normal(*s):
+        return torch.randn(*s, generator=g, device=dev, dtype=torch.float32)
+
+    x = normal(B, F * N, HD).to(torch.bfloat16)
+    W_in = (normal(3 * HD + 2 * H, HD) / HD ** 0.5).to(torch.bfloat16)
+    W_out = (normal(HD, HD) / HD ** 0.5).to(torch.bfloat16)
+    S0 = normal(B, H, D, D) * float(s0_std) if s0_std > 0 else None
+    return BlockInputs(x, W_in, W_out, S0, B, H, F, N, D)

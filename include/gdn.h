@@ -283,6 +283,48 @@ gdn_status_t gdn_frame_fwd_host(const void *q, const void *k, const void *v,
                                 gdn_stream_t stream);
 
 /*
+ * GDN block with its projections (summary page, section 方法步骤详情 module 1:
+ * the DiT's GDN blocks have d_model = H * D = 2240, 20 heads of 112).  The
+ * pages print no projection shapes; these entries take the plainest block of
+ * that width, with nn.Linear-style weights W[out][in] (bf16, row-major):
+ *   [q | k | v | a | g] = x W_in^T            W_in : [3*H*D + 2*H][H*D]
+ *   beta_{n,h}  = sigmoid(a_{n,h})             (per token and head)
+ *   gamma_{f,h} = exp(-softplus(mean_{n in frame f} g_{n,h}))   (per frame and head)
+ *   (o, S_out)  = gdn_frame_fwd(q, k, v, beta, gamma, S_in)
+ *   y           = o W_out^T                    W_out: [H*D][H*D]
+ * x and y are bf16 [B][F*N][H*D] (the token-major layout whose [H][D] view is
+ * the layer's q/k/v/o layout).  q, k, v are rounded to bf16 as the layer's
+ * inputs; the gates stay fp32.  The input projection is one tcgen05 GEMM whose
+ * epilogue writes q, k, v, beta and the per-frame decay-logit sums directly
+ * (no activation or re-layout pass over memory); a small kernel turns the sums
+ * into gamma.  The output projection is the same GEMM with a plain bf16
+ * epilogue.  D == 112 only (GDN_ERR_UNSUPPORTED otherwise); N == 0 with F > 0
+ * returns GDN_ERR_UNSUPPORTED (the frame mean needs tokens).  All pointers are
+ * device pointers, 16-byte aligned (beta, gamma: 4).  Results match the fp64
+ * definition (x W^T in fp64, q/k/v rounded to bf16 as the layer's inputs)
+ * within a relative Frobenius error of 5e-3 on y and S_out for inputs drawn
+ * as in the tests.
+ *
+ * gdn_block_in_proj : x -> q, k, v (bf16 [B][F*N][H][D]), beta (fp32
+ *                     [B][F*N][H]), gamma (fp32 [B][F][H]); no workspace.
+ * gdn_block_out_proj: o (bf16 [B][F*N][H*D]) -> y; no workspace.
+ * gdn_block_fwd     : the whole block; workspace of
+ *                     gdn_block_fwd_workspace_size() bytes, 256-byte aligned
+ *                     (holds q, k, v, o, beta, gamma and the forward's
+ *                     workspace).  S_in may be NULL (zero state), S_out NULL.
+ */
+gdn_status_t gdn_block_in_proj(const void *x, const void *W_in, void *q, void *k, void *v,
+                               float *beta, float *gamma,
+                               int B, int H, int F, int N, int D, gdn_stream_t stream);
+gdn_status_t gdn_block_out_proj(const void *o, const void *W_out, void *y,
+                                int B, int H, int F, int N, int D, gdn_stream_t stream);
+size_t gdn_block_fwd_workspace_size(int B, int H, int F, int N, int D);
+gdn_status_t gdn_block_fwd(const void *x, const void *W_in, const void *W_out,
+                           const float *S_in, float *S_out, void *y,
+                           int B, int H, int F, int N, int D, float key_scale,
+                           void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
  * Streaming step without caller-supplied scratch.  The paper has no
  * counterpart: this is a library convenience.  Same arguments, layouts and
  * results as gdn_frame_step, minus the workspace.

@@ -172,6 +172,47 @@ def frame_bwd(q, k, v, beta, gamma, S_in, dO, dS_out=None, key_scale=0.0):
     return dq, dk, dv, dbeta, dgamma, dS_in
 
 
+def _round_bf16(a):
+    """Round-to-nearest-even to bf16, returned as float32 (the layer's input type)."""
+    a32 = np.ascontiguousarray(a, dtype=np.float32)
+    u = a32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def block_in_proj(x, W_in, F, D=112):
+    """The GDN block's input projection in fp64 (summary page, section 方法步骤详情 module 1:
+    d_model = H * D; the projection shapes are a reading, the pages print none):
+    [q | k | v | a | g] = x W_in^T, beta = sigmoid(a), gamma_f = exp(-softplus(mean over the
+    frame's tokens of g)).  q, k, v are rounded to bf16, the layer's input type.
+    x [B, F*N, H*D]; returns (q, k, v [B, F*N, H, D] fp32 holding bf16 values, beta [B, F*N, H],
+    gamma [B, F, H] fp64)."""
+    x = np.asarray(_f32(x), dtype=np.float64)
+    W = np.asarray(_f32(W_in), dtype=np.float64)
+    B, FN, HD = x.shape
+    H = HD // D
+    N = FN // F
+    P = x @ W.T                      # library matmul as one step: [B, F*N, 3HD + 2H]
+    q, k, v = (_round_bf16(P[..., i * HD:(i + 1) * HD]).reshape(B, FN, H, D) for i in range(3))
+    a = P[..., 3 * HD:3 * HD + H]
+    g = P[..., 3 * HD + H:3 * HD + 2 * H]
+    beta = 1.0 / (1.0 + np.exp(-a))
+    gmean = g.reshape(B, F, N, H).mean(axis=2)
+    gamma = np.exp(-np.logaddexp(0.0, gmean))   # exp(-softplus)
+    return q, k, v, beta, gamma
+
+
+def block_fwd(x, W_in, W_out, S_in=None, F=None, key_scale=0.0, D=112):
+    """The whole GDN block in fp64: input projection, the frame-wise forward (frame_fwd, sum
+    reading), output projection y = o W_out^T (o kept in fp64).  Returns (y [B, F*N, H*D],
+    S_out [B, H, D, D])."""
+    q, k, v, beta, gamma = block_in_proj(x, W_in, F, D)
+    o, S_out = frame_fwd(q, k, v, beta, gamma, S_in, key_scale=key_scale)
+    B, FN, H, _ = o.shape
+    y = o.reshape(B, FN, H * D) @ np.asarray(_f32(W_out), dtype=np.float64).T
+    return y, S_out
+
+
 def composite(M, U):
     """(C, H) of a run of frames: C = prod M_f, H = state reached from zero (novelty section, C_p / H_p)."""
     M = np.ascontiguousarray(M, dtype=np.float64)

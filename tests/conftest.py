@@ -22,7 +22,7 @@ def rel_fro(a, b):
     return float(np.linalg.norm((a - b).ravel()) / (nb if nb > 0 else 1.0))
 
 
-def chain_groups(B, H, bytes_per_chain, budget=6e9):
+def chain_groups(B, H, bytes_per_chain, budget=32e9):
     """(b, h0, h1) head groups covering every (batch, head) chain, each group small
     enough that the oracle's fp32 inputs and fp64 outputs for it stay within
     `budget` bytes of host memory.  The oracle runs the chains of one call in

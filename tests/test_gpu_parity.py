@@ -63,8 +63,8 @@ def test_bf16_single_head_config():
     eo, es = rel_fro(o.float().cpu().numpy(), o_ref), rel_fro(S.cpu().numpy(), S_ref)
     print(f"single head: rel_fro o={eo:.3e} S={es:.3e}")
     assert eo <= TOL_BF16 and es <= TOL_BF16
-    # output error is dominated by the final bf16 rounding (~1.7e-3)
-    assert eo < 2.5e-3 and es < 1e-4
+    # error budget: the bf16 rounding of o (~1.7e-3) and of the key-side operand of U_f (~1.7e-3 on S)
+    assert eo < 3.5e-3 and es < 3e-3
 
 
 @pytest.mark.parametrize("B,H,F,N", [(1, 1, 1, 1), (2, 3, 5, 15), (1, 2, 7, 64), (1, 2, 9, 65), (2, 1, 3, 130),
