@@ -49,17 +49,24 @@ class CpOps:
 
 
 def library_ops(key_scale: float = 0.0) -> CpOps:
-    """The CUDA library's operations (device tensors)."""
+    """The CUDA library's operations (device tensors) for one rank.
+
+    The composite pass is the forward's frame-statistics pass over the rank's
+    frames; its per-frame statistics stay in this rank's workspace, and the
+    forward resumes from them (gdn_frame_fwd_resume), so each rank reads its k,
+    v and beta once.  Use one instance per rank and call composite before
+    forward on the same frames."""
     from gated_deltanet_wise_b300 import gdn
+    ws = gdn.Workspace()
 
     def composite(k, v, beta, gamma):
-        return gdn.frame_composite(k, v, beta, gamma, key_scale=key_scale)
+        return gdn.frame_composite(k, v, beta, gamma, key_scale=key_scale, workspace=ws)
 
     def compose(S, C, H):
         return gdn.state_compose(S, C, H)
 
     def forward(q, k, v, beta, gamma, S):
-        return gdn.frame_fwd(q, k, v, beta, gamma, S, key_scale=key_scale)
+        return gdn.frame_fwd_resume(q, gamma, S, workspace=ws)
 
     return CpOps(composite, compose, forward)
 

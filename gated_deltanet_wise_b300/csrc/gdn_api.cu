@@ -431,7 +431,7 @@ size_t gdn_frame_composite_workspace_size(int B, int H, int F, int N, int D)
     if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
     if (D != 112) return (size_t)-1;
     TcPlan plan;
-    if (!tc_plan(B, H, F, N, 1, &plan)) return (size_t)-1;
+    if (!tc_plan(B, H, F, N, 0, &plan)) return (size_t)-1;
     return plan.ws_bytes;
 }
 
@@ -453,7 +453,7 @@ gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta
     if (!k || !v || !beta) return GDN_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v, 16) || !aligned(beta, 4)) return GDN_ERR_INVALID_ARG;
     TcPlan plan;
-    if (!tc_plan(B, H, F, N, 1, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (!tc_plan(B, H, F, N, 0, &plan)) return GDN_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
     unsigned *status = device_status_word();
@@ -461,6 +461,32 @@ gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta
     cudaError_t e = launch_frame_composite_tc(k, v, beta, gamma, C_out, H_out, plan,
                                               default_key_scale(key_scale, D, N), workspace, status, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_frame_fwd_resume(const void *q, const float *gamma, const float *S_in, float *S_out, void *o,
+                                  int B, int H, int F, int N, int D, void *workspace, size_t workspace_bytes,
+                                  gdn_stream_t stream)
+{
+    if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return GDN_OK;
+    if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (F == 0 || N == 0) {  // no statistics to resume from: the forward's degenerate rules
+        if (F > 0 && (!gamma || !aligned(gamma, 4))) return GDN_ERR_INVALID_ARG;
+        if (!S_out) return GDN_OK;
+        return launch_decay_only(gamma, S_in, S_out, B, H, F, D, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (!q || !o || !gamma) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(o, 16) || !aligned(gamma, 4)) return GDN_ERR_INVALID_ARG;
+    TcPlan plan;
+    if (!tc_plan(B, H, F, N, 0, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+    unsigned *status = device_status_word();
+    if (!status) return GDN_ERR_CUDA;
+    return launch_fwd_resume_tc(q, gamma, S_in, S_out, o, plan, workspace, status, st) == cudaSuccess ? GDN_OK
+                                                                                                    : GDN_ERR_CUDA;
 }
 
 gdn_status_t gdn_state_compose(const float *S, const float *C, const float *Hc, float *S_out, int BH, int D,
@@ -564,10 +590,11 @@ gdn_status_t gdn_block_fwd(const void *x, const void *W_in, const void *W_out, c
                            void *y, int B, int H, int F, int N, int D, float key_scale, void *workspace,
                            size_t workspace_bytes, gdn_stream_t stream)
 {
-    BlockLayout L;
-    if (!block_layout(B, H, F, N, D, &L)) return GDN_ERR_INVALID_ARG;
+    if (!block_sizes_ok(B, H, F, N, D)) return GDN_ERR_INVALID_ARG;
     if (B == 0 || H == 0) return GDN_OK;
     if (D != 112) return GDN_ERR_UNSUPPORTED;
+    BlockLayout L;
+    if (!block_layout(B, H, F, N, D, &L)) return GDN_ERR_UNSUPPORTED;
     if (F == 0)  // no frames: the state passes through (S_out = S_in, or zero)
         return gdn_frame_fwd(nullptr, nullptr, nullptr, nullptr, nullptr, S_in, S_out, nullptr, B, H, 0, N, D,
                              key_scale, nullptr, 0, stream);

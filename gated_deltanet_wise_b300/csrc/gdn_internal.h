@@ -51,10 +51,14 @@ struct TcPlan {
 // force_chunks > 0 fixes the number of frame chunks (1: one chunk per chain,
 // whose composite is then the whole range's); 0 lets the plan choose.
 bool tc_plan(int B, int H, int F, int N, int force_chunks, TcPlan *plan);
-// K1 alone with a one-chunk plan: per-chain composites (C, H) of all F frames.
+// Per-chain composites (C, H) of all F frames: K1 over the plan's chunks, then the
+// chunk composites composed in frame order (the statistics stay in the workspace).
 cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float *beta, const float *gamma,
                                       float *C_out, float *H_out, const TcPlan &plan, float c, void *workspace,
                                       unsigned *status, cudaStream_t stream);
+// K1b + K2 from statistics a launch_frame_composite_tc call left in the workspace.
+cudaError_t launch_fwd_resume_tc(const void *q, const float *gamma, const float *S_in, float *S_out, void *o,
+                                 const TcPlan &plan, void *workspace, unsigned *status, cudaStream_t stream);
 // S_out = S C + H per chain (S may be null: zero), fp32.
 cudaError_t launch_state_compose_tc(const float *S, const float *C, const float *H, float *S_out, int BH,
                                     unsigned *status, cudaStream_t stream);

@@ -63,6 +63,154 @@ constexpr uint32_t kIdU = idesc_bf16(128, kD, true, true);      // pair += X'^T 
 
 __device__ __forceinline__ void p_math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// Named barrier over the four solver warps (2, 3, 6, 7).
+__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 4, 128;" ::: "memory"); }
+
+// Shared-memory scratch of the blocked solve (inside regions that are idle while it
+// runs): T in fp32, column-major (the second half of the X_lo region, which X' fills
+// only after the solve), and, in the T_off tile's slack rows 64..127 (read only into
+// the MMA's unused accumulator lanes), the diagonal tiles row-major and the Y tiles.
+// Layouts keep the solver's shared-memory accesses free of bank conflicts:
+//  - Tf: column e of T holds 16 float4 chunks; chunk c of column e sits at chunk
+//    position c ^ (e & 15), so lanes reading the same rows of 16 different columns
+//    hit 16 different bank groups;
+//  - Y tiles: column j at a stride of 20 floats (five float4 chunks).
+constexpr uint32_t kPOffTf = 196608 + 16384;              // fp32 T, column-major, chunk-swizzled
+constexpr uint32_t kPOffTrm = 147456 + 8192;              // diagonal tiles, row-major [4][16][16]
+constexpr uint32_t kPOffY = kPOffTrm + 4096;              // Y tiles of one distance, [3][16 columns][20]
+constexpr int kYStride = 20;
+
+__device__ __forceinline__ int tf_idx(int a, int e) { return e * 64 + ((((a >> 2) ^ (e & 15))) << 2) + (a & 3); }
+
+__device__ __forceinline__ void st_timg(uint8_t *sm, int a, int e, float v)
+{
+    __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + 147456);
+    const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
+    timg[off >> 1] = __float2bfloat16_rn(v);
+}
+
+// sum_{m < 16} x[m] y[m] for 16 consecutive floats x (16-byte aligned) and
+// 16 rows 4 k0 .. 4 k0 + 15 of column e of Tf.
+__device__ __forceinline__ float dot16_tf(const float *x, const float *Tf, int e, int k0)
+{
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 a = reinterpret_cast<const float4 *>(x)[m4];
+        const float4 b = reinterpret_cast<const float4 *>(Tf + e * 64)[(k0 + m4) ^ (e & 15)];
+        s0 = fmaf(a.x, b.x, s0);
+        s1 = fmaf(a.y, b.y, s1);
+        s0 = fmaf(a.z, b.z, s0);
+        s1 = fmaf(a.w, b.w, s1);
+    }
+    return s0 + s1;
+}
+
+__device__ __forceinline__ float dot16(const float *x, const float *y)
+{
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 a = reinterpret_cast<const float4 *>(x)[m4], b = reinterpret_cast<const float4 *>(y)[m4];
+        s0 = fmaf(a.x, b.x, s0);
+        s1 = fmaf(a.y, b.y, s1);
+        s0 = fmaf(a.z, b.z, s0);
+        s1 = fmaf(a.w, b.w, s1);
+    }
+    return s0 + s1;
+}
+
+// One distance d of the blocked solve: the (4 - d) tiles T_IJ, I = J + d, with
+// 2 (4 - d) elements per thread (the 128 solver threads), unrolled so that the
+// independent elements' loads and FMA chains interleave.
+template <int d>
+__device__ __forceinline__ void solve_level(const float *Gs, float *Tf, const float *Trm, float *Yb, uint8_t *sm,
+                                            int tn)
+{
+    constexpr int kPer = 2 * (4 - d);
+    // Y_IJ = sum_{K=J}^{I-1} G_IK T_KJ
+    float y[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tn + 128 * u;
+        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < d; ++k) {  // K = J + k; G[16I + i][16K + m] = Gs[(16I + i) * 64 + 16K + m]
+            const int K = J + k;
+            acc += dot16_tf(Gs + (16 * I + i) * 64 + 16 * K, Tf, 16 * J + j, 4 * K);
+        }
+        y[u] = acc;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tn + 128 * u;
+        const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+        Yb[(J * 16 + j) * kYStride + i] = y[u];
+    }
+    solver_sync();
+    // T_IJ = -T_II Y_IJ
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tn + 128 * u;
+        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
+        y[u] = -dot16(Trm + I * 256 + i * 16, Yb + (J * 16 + j) * kYStride);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tn + 128 * u;
+        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
+        Tf[tf_idx(16 * I + i, 16 * J + j)] = y[u];
+        st_timg(sm, 16 * I + i, 16 * J + j, y[u]);
+    }
+    solver_sync();
+}
+
+// T = (I + StrictLower(diag(beta) G))^-1 diag(beta) for a 64-token sub-chunk, by the
+// four solver warps; see the call site.
+__device__ __noinline__ void solve_T(const float *Gs, const float *bt, uint8_t *sm, int warp, int lane)
+{
+    const int tn = ((warp < 4 ? warp - 2 : warp - 4) << 5) + lane;  // 0..127
+    float *Tf = reinterpret_cast<float *>(sm + kPOffTf);
+    float *Trm = reinterpret_cast<float *>(sm + kPOffTrm);
+    float *Yb = reinterpret_cast<float *>(sm + kPOffY);
+    // diagonal tiles: thread (I, e) runs the forward substitution of column e of T_II,
+    // t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r (rows of tile I)
+    if (tn < 64) {
+        const int I = tn >> 4, e = tn & 15, b0 = 16 * I;
+        float tc[16];
+#pragma unroll
+        for (int a = 0; a < 16; ++a) tc[a] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            tc[r] = (r == e ? bt[b0 + e] : 0.f) - bt[b0 + r] * tc[r];
+            const float *gcol = Gs + (b0 + r) * 64 + b0;  // G[b0 + a][b0 + r], a = 0..15
+#pragma unroll
+            for (int a4 = (r + 1) >> 2; a4 < 4; ++a4) {
+                const float4 g4 = reinterpret_cast<const float4 *>(gcol)[a4];
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (4 * a4 + j > r) tc[4 * a4 + j] = fmaf(gv[j], tc[r], tc[4 * a4 + j]);
+            }
+        }
+#pragma unroll
+        for (int a4 = 0; a4 < 4; ++a4)
+            reinterpret_cast<float4 *>(Tf + (b0 + e) * 64)[(4 * I + a4) ^ e] =
+                make_float4(tc[4 * a4], tc[4 * a4 + 1], tc[4 * a4 + 2], tc[4 * a4 + 3]);
+#pragma unroll
+        for (int a = 0; a < 16; ++a) {
+            Trm[I * 256 + a * 16 + e] = tc[a];
+            st_timg(sm, b0 + a, b0 + e, a > e ? tc[a] : 0.f);
+        }
+    }
+    solver_sync();
+    // off-diagonal tiles, by distance d = I - J
+    solve_level<1>(Gs, Tf, Trm, Yb, sm, tn);
+    solve_level<2>(Gs, Tf, Trm, Yb, sm, tn);
+    solve_level<3>(Gs, Tf, Trm, Yb, sm, tn);
+}
+
 struct ProdParams {
     const float *beta;
     uint8_t *ws_frames;  // [BH][F] x kFrameWs, by processing position
@@ -213,9 +361,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float *Gs = reinterpret_cast<float *>(sm + kPOffXlo);
         bool ok = true;
 
-        // the pair starts at zero: zero image
+        // the pair starts at zero: zero image; the T_off image's tiles above the
+        // diagonal are never written by the solve and stay zero
         for (int e = t; e < (int)(4 * kPSPanel / 16); e += 256)
             reinterpret_cast<uint4 *>(sm + kPOffSA)[e] = make_uint4(0, 0, 0, 0);
+        for (int e = t; e < (int)(kPC * kRowB / 16); e += 256)
+            reinterpret_cast<uint4 *>(sm + kPOffT)[e] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(simg_ready);
@@ -282,35 +433,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             p_math_sync();
 
-            if (warp == 2 || warp == 3) {
-                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta), column e = t per thread,
-                //     by forward substitution in right-looking order: once t_r is known it is
-                //     added into every later row's sum (independent FMAs, broadcast reads of
-                //     column r of G); t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r.
-                //     The strictly lower part T_off goes to the bf16 image (row a, column e).
-                const int e = t;
-                const float be = bt[e];
-                float Tc[kPC];
-#pragma unroll
-                for (int a = 0; a < kPC; ++a) Tc[a] = 0.f;
-#pragma unroll
-                for (int r2 = 0; r2 < kPC; ++r2) {
-                    Tc[r2] = (r2 == e ? be : 0.f) - bt[r2] * Tc[r2];
-#pragma unroll
-                    for (int a4 = (r2 + 1) >> 2; a4 < kPC / 4; ++a4) {
-                        const float4 g4 = reinterpret_cast<const float4 *>(Gs + r2 * 64)[a4];
-                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (4 * a4 + j > r2) Tc[4 * a4 + j] = fmaf(gv[j], Tc[r2], Tc[4 * a4 + j]);
-                    }
-                }
-                __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + kPOffT);
-#pragma unroll
-                for (int a = 0; a < kPC; ++a) {
-                    const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
-                    timg[off >> 1] = __float2bfloat16_rn(a > e ? Tc[a] : 0.f);
-                }
+            if (!tok_warp) {
+                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta) on the four warps whose
+                //     TMEM lanes hold no token rows (warps 2, 3, 6, 7), blocked in 16 x 16 tiles:
+                //     the diagonal tiles T_II = (I + L_II)^-1 diag(beta_I) by forward substitution
+                //     (one column per thread), then the off-diagonal tiles by distance from the
+                //     diagonal, T_IJ = -T_II sum_{K=J}^{I-1} G_IK T_KJ (I > J), one element per
+                //     thread and step: the unit-lower system's rows I depend only on tiles of
+                //     smaller distance.  G is symmetric, so its column-major copy Gs is also
+                //     row-major.  The strictly lower part T_off goes to the bf16 image.
+                solve_T(Gs, bt, sm, warp, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(r_ready);
@@ -323,12 +455,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_after();
                 if (ok) {
                     const float btt = bt[row];
-                    for (int cc = 0; cc < 8; ++cc) {
+                    // two 16-column chunks per TMEM round trip (a load's latency, not its
+                    // bandwidth, sets this loop's pace)
+                    for (int cp = 0; cp < 8; cp += 2) {
+                    uint32_t rr2[2][16];
+                    tmem_ld16(tmem + lane_off + kPTmX + g * 128 + cp * 16, rr2[0]);
+                    tmem_ld16(tmem + lane_off + kPTmX + g * 128 + cp * 16 + 16, rr2[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int cc = cp + half;
                         const int n0 = g * 128 + cc * 16;  // column of [Abar | W] (padded to 128 each)
                         const int y0 = cc * 16;            // column inside K or V
-                        uint32_t rr[16];
-                        tmem_ld16(tmem + lane_off + kPTmX + n0, rr);
-                        tmem_ld_wait();
+                        const uint32_t *rr = rr2[half];
                         float y[16];
                         if (y0 < kD) {
                             const uint8_t *src = g == 0 ? sm + kPOffKh : vraw;
@@ -355,13 +494,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         *reinterpret_cast<uint4 *>(dst + sw128_off(row, (n0 & 63) >> 3)) = f32x8_to_bf16(rv);
                         *reinterpret_cast<uint4 *>(dst + sw128_off(row, ((n0 & 63) >> 3) + 1)) = f32x8_to_bf16(rv + 8);
                     }
+                    }
                     tmem_st_wait();
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(r_ready);
-            } else {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(r_ready);
             }
@@ -372,11 +509,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_after();
                 if (ok) {
                     const float crt = cr[row];
-                    for (int cc = 0; cc < 8; ++cc) {
+                    for (int cp = 0; cp < 8; cp += 2) {  // two chunks per TMEM round trip
+                    uint32_t rx2[2][16];
+                    tmem_ld16(tmem + lane_off + kPTmX + g * 128 + cp * 16, rx2[0]);
+                    tmem_ld16(tmem + lane_off + kPTmX + g * 128 + cp * 16 + 16, rx2[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int cc = cp + half;
                         const int n0 = g * 128 + cc * 16;
-                        uint32_t rx[16];
-                        tmem_ld16(tmem + lane_off + kPTmX + n0, rx);
-                        tmem_ld_wait();
+                        const uint32_t *rx = rx2[half];
                         float xv[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) xv[j] = __uint_as_float(rx[j]) * crt;
@@ -389,6 +531,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         *reinterpret_cast<uint4 *>(sm + kPOffR + o1) = hi1;
                         *reinterpret_cast<uint4 *>(sm + kPOffXlo + o0) = lo0;
                         *reinterpret_cast<uint4 *>(sm + kPOffXlo + o1) = lo1;
+                    }
                     }
                 }
                 fence_proxy_async_smem();

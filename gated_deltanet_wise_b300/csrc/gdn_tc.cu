@@ -456,11 +456,15 @@ constexpr int kK1bThreads = 224;
 constexpr uint32_t kK1bOffS = 2 * (uint32_t)kStateBytes;           // S rows [8][112]
 constexpr uint32_t kK1bOffBar = kK1bOffS + kK1bRows * kD * 4;      // 2 mbarriers + abort flag
 constexpr uint32_t kK1bSmem = kK1bOffBar + 64;
+// K1b modes: the start state is the identity (instead of S_in), and/or the input
+// composites are zero.  With both the scan composes the transition composites,
+// C_0 C_1 ... C_{n-1}; with neither it is the chunk-boundary scan proper.
+constexpr int kK1bIdentityIn = 1, kK1bZeroH = 2;
 
 __global__ void __launch_bounds__(kK1bThreads)
     k1b_chunk_boundary_kernel(const float *__restrict__ compC, const float *__restrict__ compH, size_t chain_stride,
                               size_t chunk_stride, float *__restrict__ ws_start, const float *S_in, float *S_out,
-                              int n_chunks, unsigned *status)
+                              int n_chunks, unsigned *status, int mode)
 {
     extern __shared__ __align__(128) uint8_t k1b_smem[];
     float *Cb0 = reinterpret_cast<float *>(k1b_smem);
@@ -481,7 +485,8 @@ __global__ void __launch_bounds__(kK1bThreads)
     griddep_wait();  // composites and S_in come from earlier kernels on the stream
     for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
         const int rr = e / kD, cc = e % kD;
-        Srows[rr][cc] = S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
+        Srows[rr][cc] = (mode & kK1bIdentityIn) ? (r0 + rr == cc ? 1.f : 0.f)
+                        : S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
     }
     __syncthreads();
     // composite steps to apply: without S_out the state after the last chunk is not needed
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(kK1bThreads)
         const float *Hc = cH + (size_t)c * chunk_stride;
         float acc[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = Hc[(r0 + 4 * rp + q) * kD + j];
+        for (int q = 0; q < 4; ++q) acc[q] = (mode & kK1bZeroH) ? 0.f : Hc[(r0 + 4 * rp + q) * kD + j];
         if (t == 0 && !mbar_wait(&bar[c & 1], (c >> 1) & 1, abort_flag)) *abort_flag = 1;
         __syncthreads();
         if (*abort_flag) break;
@@ -1051,11 +1056,16 @@ K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, floa
 }
 }  // namespace
 
+// Composites of a whole run of frames for context parallelism: K1 over the
+// plan's chunks (the same launch as the forward, every SM busy, the per-frame
+// statistics left in the workspace), then the chunk composites composed in
+// frame order by the chunk-boundary kernel: from the identity with no inputs it
+// yields C = C_0 C_1 ... C_{n-1}, from zero with the inputs H = the state the
+// run reaches from zero.
 cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float *beta, const float *gamma,
                                       float *C_out, float *H_out, const TcPlan &pl, float c, void *workspace,
                                       unsigned *status, cudaStream_t stream)
 {
-    if (pl.n_chunks != 1) return cudaErrorInvalidValue;
     CUtensorMap mk, mv;
     if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS))
         return cudaErrorInvalidValue;
@@ -1064,14 +1074,19 @@ cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = pl.B * pl.H;
     const K1Params p1 = k1_params(beta, gamma, pl, c, 0, ws, status);
-    if ((e = launch_pdl(k1_frame_stats_kernel, dim3(BH), kK1Threads, kK1Smem, stream, mk, mv, p1)) != cudaSuccess)
+    if ((e = launch_pdl(k1_frame_stats_kernel, dim3(BH * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1)) !=
+        cudaSuccess)
         return e;
-    // the chain's composite is (C, H) back to back in the workspace
-    if (C_out && (e = cudaMemcpy2DAsync(C_out, kStateBytes, p1.ws_comp, 2 * kStateBytes, kStateBytes, BH,
-                                        cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+    const float *comp = p1.ws_comp;
+    const size_t chain_stride = (size_t)pl.n_chunks * 2 * kStateFloats, chunk_stride = (size_t)2 * kStateFloats;
+    if (C_out && (e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
+                                 comp, comp + kStateFloats, chain_stride, chunk_stride, (float *)nullptr,
+                                 (const float *)nullptr, C_out, pl.n_chunks, status,
+                                 kK1bIdentityIn | kK1bZeroH)) != cudaSuccess)
         return e;
-    if (H_out && (e = cudaMemcpy2DAsync(H_out, kStateBytes, p1.ws_comp + kStateFloats, 2 * kStateBytes, kStateBytes,
-                                        BH, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+    if (H_out && (e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
+                                 comp, comp + kStateFloats, chain_stride, chunk_stride, (float *)nullptr,
+                                 (const float *)nullptr, H_out, pl.n_chunks, status, 0)) != cudaSuccess)
         return e;
     return cudaSuccess;
 }
@@ -1082,7 +1097,7 @@ cudaError_t launch_state_compose_tc(const float *S, const float *C, const float 
     cudaError_t e = prepare_tc_kernels();
     if (e != cudaSuccess) return e;
     return launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream, C, H,
-                      (size_t)kStateFloats, (size_t)0, (float *)nullptr, S, S_out, 1, status);
+                      (size_t)kStateFloats, (size_t)0, (float *)nullptr, S, S_out, 1, status, 0);
 }
 
 // K1 alone over a plan: per-frame A_f image and U_f (and chunk composites) in the workspace.
@@ -1114,7 +1129,7 @@ static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, cons
     cudaError_t e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream,
                                comp, comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats,
                                (size_t)2 * kStateFloats, reinterpret_cast<float *>(ws + pl.off_start), S_in,
-                               (float *)nullptr, pl.n_chunks, status);
+                               (float *)nullptr, pl.n_chunks, status, 0);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
     K2Params p2;
@@ -1139,7 +1154,18 @@ static cudaError_t launch_scan_output_tc(const void *q, const float *gamma, cons
     return cudaSuccess;
 }
 
-// The state chain alone over a plan whose workspace holds per-frame statistics
+// K1b + K2 over a plan whose workspace already holds K1's statistics and chunk
+// composites (left there by launch_frame_composite_tc on the same frames).
+cudaError_t launch_fwd_resume_tc(const void *q, const float *gamma, const float *S_in, float *S_out, void *o,
+                                 const TcPlan &pl, void *workspace, unsigned *status, cudaStream_t stream)
+{
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    return launch_scan_output_tc(q, gamma, S_in, S_out, o, pl, 0, static_cast<uint8_t *>(workspace), status, stream,
+                                 nullptr);
+}
+
+// The state chain alone (K1b + K2 without outputs) over a plan whose workspace
 // and chunk composites: K1b from S_in (null: zero), then K2 without outputs,
 // storing the state after every frame (states, [B*H][F][D][D]) and the final
 // state (S_out, may be null).  q only shapes K2's (unused) tensor maps.
@@ -1154,7 +1180,7 @@ cudaError_t launch_states_tc(const void *q, const float *gamma, const float *S_i
     const float *comp = reinterpret_cast<const float *>(ws + pl.off_comp);
     e = launch_pdl(k1b_chunk_boundary_kernel, dim3(BH, kD / kK1bRows), kK1bThreads, kK1bSmem, stream, comp,
                    comp + kStateFloats, (size_t)pl.n_chunks * 2 * kStateFloats, (size_t)2 * kStateFloats,
-                   reinterpret_cast<float *>(ws + pl.off_start), S_in, (float *)nullptr, pl.n_chunks, status);
+                   reinterpret_cast<float *>(ws + pl.off_start), S_in, (float *)nullptr, pl.n_chunks, status, 0);
     if (e != cudaSuccess) return e;
     K2Params p2;
     p2.o = nullptr;

@@ -36,6 +36,7 @@ EXPORTED = [
     "gdn_frame_fwd_ex_workspace_size", "gdn_frame_fwd_ex",
     "gdn_frame_bwd_workspace_size", "gdn_frame_bwd", "gdn_test_frame_fwd_expired_wait",
     "gdn_block_in_proj", "gdn_block_out_proj", "gdn_block_fwd_workspace_size", "gdn_block_fwd",
+    "gdn_frame_fwd_resume",
 ]
 
 GDN_FWD_PRODUCT = 1
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_frame_bwd_workspace_size.argtypes = [I] * 5
         L.gdn_frame_bwd.restype = I
         L.gdn_frame_bwd.argtypes = [P] * 14 + [I] * 5 + [F, P, Z, P]
+        L.gdn_frame_fwd_resume.restype = I
+        L.gdn_frame_fwd_resume.argtypes = [P] * 5 + [I] * 5 + [P, Z, P]
         L.gdn_block_in_proj.restype = I
         L.gdn_block_in_proj.argtypes = [P] * 7 + [I] * 5 + [P]
         L.gdn_block_out_proj.restype = I
@@ -137,6 +140,11 @@ def _check_status(st: int, what: str):
 # ---------------------------------------------------------------- raw C entry points
 def gdn_frame_fwd_workspace_size(B: int, H: int, F: int, N: int, D: int) -> int:
     return int(lib().gdn_frame_fwd_workspace_size(B, H, F, N, D))
+
+
+def gdn_frame_fwd_resume(q, gamma, S_in, S_out, o, B, H, F, N, D, workspace, workspace_bytes, stream=None) -> int:
+    return int(lib().gdn_frame_fwd_resume(_p(q), _p(gamma), _p(S_in), _p(S_out), _p(o), B, H, F, N, D,
+                                          _p(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def gdn_block_in_proj(x, W_in, q, k, v, beta, gamma, B, H, F, N, D, stream=None) -> int:
@@ -446,6 +454,21 @@ def frame_composite(k, v, beta, gamma, *, key_scale: float = 0.0, workspace: Opt
     st = gdn_frame_composite(k, v, beta, gamma, C, Hc, B, H, F, N, D, key_scale, ws, nbytes, stream)
     _check_status(st, "gdn_frame_composite")
     return C, Hc
+
+
+def frame_fwd_resume(q, gamma, S_in=None, *, workspace: Workspace, o=None, S_out=None, stream=None):
+    """Finish the forward of the frames whose composites the last frame_composite call on
+    `workspace` computed (gdn_frame_fwd_resume).  Returns (o, S_out)."""
+    B, H, F, N, D = _shape(q, gamma)
+    _check(q, torch.bfloat16, "q")
+    _check(gamma, torch.float32, "gamma")
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device) if S_out is None else S_out
+    nbytes = gdn_frame_composite_workspace_size(B, H, F, N, D)
+    ws = workspace.get(nbytes, q.device)
+    st = gdn_frame_fwd_resume(q, gamma, S_in, S_out, o, B, H, F, N, D, ws, nbytes, stream)
+    _check_status(st, "gdn_frame_fwd_resume")
+    return o, S_out
 
 
 def state_compose(S, C, Hc, *, out=None, stream=None):

@@ -210,7 +210,20 @@ gdn_status_t gdn_frame_step(const void *q, const void *k, const void *v,
  * layouts and key_scale as gdn_frame_fwd (frames [0, F) of the arrays passed);
  * C_out, H_out: fp32 [B][H][D][D] (either may be NULL).  Workspace:
  * gdn_frame_composite_workspace_size() bytes (0 for F == 0 or N == 0, where
- * C = (prod gamma) I and H = 0).  Same errors as gdn_frame_fwd.
+ * C = (prod gamma) I and H = 0; otherwise the size gdn_frame_fwd needs for the
+ * same frames).  Same errors as gdn_frame_fwd.  The call runs the forward's
+ * frame-statistics pass over all the frames (every SM busy) and composes the
+ * per-chunk composites in frame order; the per-frame statistics stay in the
+ * workspace, so that gdn_frame_fwd_resume can finish the forward of the same
+ * frames without reading k, v or beta again.
+ *
+ * gdn_frame_fwd_resume: the rest of gdn_frame_fwd for the frames of the last
+ * gdn_frame_composite call on `workspace` (same k, v, beta, gamma, B, H, F, N,
+ * D, key_scale; the workspace untouched in between): from S_in (NULL: zero)
+ * it writes o for every token and S_out, reading only q and gamma.  In the
+ * context-parallel form each rank therefore reads its k and v once.  With any
+ * other workspace contents the results are undefined.  Statuses as
+ * gdn_frame_fwd (workspace size: gdn_frame_composite_workspace_size()).
  */
 size_t gdn_frame_composite_workspace_size(int B, int H, int F, int N, int D);
 gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta,
@@ -218,6 +231,10 @@ gdn_status_t gdn_frame_composite(const void *k, const void *v, const float *beta
                                  int B, int H, int F, int N, int D, float key_scale,
                                  void *workspace, size_t workspace_bytes,
                                  gdn_stream_t stream);
+
+gdn_status_t gdn_frame_fwd_resume(const void *q, const float *gamma, const float *S_in, float *S_out,
+                                  void *o, int B, int H, int F, int N, int D,
+                                  void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /*
  * gdn_state_compose: S_out = S C + Hc for each of BH chains (fp32

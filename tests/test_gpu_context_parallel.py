@@ -67,16 +67,16 @@ def test_split_runs_equal_one_forward(world):
     B, H, F, N = 1, 4, 9, 300
     x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=40 + world, device=DEV, s0_std=0.1)
     o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
-    ops = library_ops()
     runs = frame_split(F, world)
+    ops = [library_ops() for _ in runs]   # one per emulated rank: each keeps its statistics
     sl = lambda t, f0, f1: t[:, f0 * N:f1 * N].contiguous()
-    comps = [ops.composite(sl(x.k, *r), sl(x.v, *r), sl(x.beta, *r), x.gamma[:, r[0]:r[1]].contiguous())
-             for r in runs]
+    comps = [ops[i].composite(sl(x.k, *r), sl(x.v, *r), sl(x.beta, *r), x.gamma[:, r[0]:r[1]].contiguous())
+             for i, r in enumerate(runs)]
     outs, S_end = [], None
     for rank, r in enumerate(runs):
-        S_start = start_state(x.S0, comps, rank, ops.compose)
-        o, S_end = ops.forward(sl(x.q, *r), sl(x.k, *r), sl(x.v, *r), sl(x.beta, *r),
-                               x.gamma[:, r[0]:r[1]].contiguous(), S_start)
+        S_start = start_state(x.S0, comps, rank, ops[rank].compose)
+        o, S_end = ops[rank].forward(sl(x.q, *r), sl(x.k, *r), sl(x.v, *r), sl(x.beta, *r),
+                                     x.gamma[:, r[0]:r[1]].contiguous(), S_start)
         outs.append(o)
     torch.cuda.synchronize()
     o = torch.cat(outs, 1)
@@ -85,3 +85,24 @@ def test_split_runs_equal_one_forward(world):
     o_orc, S_orc = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
     assert rel_fro(o.float().cpu().numpy(), o_orc) <= TOL
     assert rel_fro(S_end.cpu().numpy(), S_orc) <= TOL
+
+
+def test_resume_equals_forward_and_reads_no_keys():
+    """gdn_frame_fwd_resume after gdn_frame_composite on the same frames equals gdn_frame_fwd
+    (several chunks, a random start state); k, v and beta are not read again (they are
+    overwritten with NaN before the resume)."""
+    B, H, F, N = 2, 3, 23, 150
+    x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=77, device=DEV, s0_std=0.1)
+    o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    ws = gdn.Workspace()
+    C, Hc = gdn.frame_composite(x.k, x.v, x.beta, x.gamma, workspace=ws)
+    for t in (x.k, x.v, x.beta):
+        t.fill_(float("nan"))
+    o, S = gdn.frame_fwd_resume(x.q, x.gamma, x.S0, workspace=ws)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert rel_fro(o.float().cpu().numpy(), o_ref.float().cpu().numpy()) <= 1e-6
+    assert rel_fro(S.cpu().numpy(), S_ref.cpu().numpy()) <= 1e-6
+    # the composites describe the same run: S_out = S_in C + H
+    S_comp = gdn.state_compose(x.S0, C, Hc)
+    assert rel_fro(S_comp.cpu().numpy(), S_ref.cpu().numpy()) <= TOL
