@@ -63,152 +63,39 @@ constexpr uint32_t kIdU = idesc_bf16(128, kD, true, true);      // pair += X'^T 
 
 __device__ __forceinline__ void p_math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Named barrier over the four solver warps (2, 3, 6, 7).
-__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 4, 128;" ::: "memory"); }
-
-// Shared-memory scratch of the blocked solve (inside regions that are idle while it
-// runs): T in fp32, column-major (the second half of the X_lo region, which X' fills
-// only after the solve), and, in the T_off tile's slack rows 64..127 (read only into
-// the MMA's unused accumulator lanes), the diagonal tiles row-major and the Y tiles.
-// Layouts keep the solver's shared-memory accesses free of bank conflicts:
-//  - Tf: column e of T holds 16 float4 chunks; chunk c of column e sits at chunk
-//    position c ^ (e & 15), so lanes reading the same rows of 16 different columns
-//    hit 16 different bank groups;
-//  - Y tiles: column j at a stride of 20 floats (five float4 chunks).
-constexpr uint32_t kPOffTf = 196608 + 16384;              // fp32 T, column-major, chunk-swizzled
-constexpr uint32_t kPOffTrm = 147456 + 8192;              // diagonal tiles, row-major [4][16][16]
-constexpr uint32_t kPOffY = kPOffTrm + 4096;              // Y tiles of one distance, [3][16 columns][20]
-constexpr int kYStride = 20;
-
-__device__ __forceinline__ int tf_idx(int a, int e) { return e * 64 + ((((a >> 2) ^ (e & 15))) << 2) + (a & 3); }
-
-__device__ __forceinline__ void st_timg(uint8_t *sm, int a, int e, float v)
+// T = (I + StrictLower(diag(beta) G))^-1 diag(beta) for a 64-token sub-chunk by
+// warps 2 and 3, one column e per thread, by forward substitution in right-looking
+// order: once t_r is final it is added into every later row's sum (independent
+// FMAs, broadcast float4 reads of column r of G);
+//     t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r.
+// The strictly lower part T_off goes to the bf16 image (row a, column e).  (Timed
+// alone, one CTA of these two warps per SM: ~6,000 cycles per solve; a
+// left-looking order with four partial sums took ~6,500, and neither a 16 x 16
+// blocked form on four warps nor two lanes per column beat it inside the kernel.)
+__device__ __noinline__ void solve_T(const float *Gs, const float *bt, uint8_t *sm, int e)
 {
-    __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + 147456);
-    const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
-    timg[off >> 1] = __float2bfloat16_rn(v);
-}
-
-// sum_{m < 16} x[m] y[m] for 16 consecutive floats x (16-byte aligned) and
-// 16 rows 4 k0 .. 4 k0 + 15 of column e of Tf.
-__device__ __forceinline__ float dot16_tf(const float *x, const float *Tf, int e, int k0)
-{
-    float s0 = 0.f, s1 = 0.f;
+    const float be = bt[e];
+    float tc[kPC];
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 a = reinterpret_cast<const float4 *>(x)[m4];
-        const float4 b = reinterpret_cast<const float4 *>(Tf + e * 64)[(k0 + m4) ^ (e & 15)];
-        s0 = fmaf(a.x, b.x, s0);
-        s1 = fmaf(a.y, b.y, s1);
-        s0 = fmaf(a.z, b.z, s0);
-        s1 = fmaf(a.w, b.w, s1);
-    }
-    return s0 + s1;
-}
-
-__device__ __forceinline__ float dot16(const float *x, const float *y)
-{
-    float s0 = 0.f, s1 = 0.f;
+    for (int a = 0; a < kPC; ++a) tc[a] = 0.f;
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 a = reinterpret_cast<const float4 *>(x)[m4], b = reinterpret_cast<const float4 *>(y)[m4];
-        s0 = fmaf(a.x, b.x, s0);
-        s1 = fmaf(a.y, b.y, s1);
-        s0 = fmaf(a.z, b.z, s0);
-        s1 = fmaf(a.w, b.w, s1);
-    }
-    return s0 + s1;
-}
-
-// One distance d of the blocked solve: the (4 - d) tiles T_IJ, I = J + d, with
-// 2 (4 - d) elements per thread (the 128 solver threads), unrolled so that the
-// independent elements' loads and FMA chains interleave.
-template <int d>
-__device__ __forceinline__ void solve_level(const float *Gs, float *Tf, const float *Trm, float *Yb, uint8_t *sm,
-                                            int tn)
-{
-    constexpr int kPer = 2 * (4 - d);
-    // Y_IJ = sum_{K=J}^{I-1} G_IK T_KJ
-    float y[kPer];
+    for (int r = 0; r < kPC; ++r) {
+        tc[r] = (r == e ? be : 0.f) - bt[r] * tc[r];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tn + 128 * u;
-        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
-        float acc = 0.f;
+        for (int a4 = (r + 1) >> 2; a4 < kPC / 4; ++a4) {
+            const float4 g4 = reinterpret_cast<const float4 *>(Gs + r * 64)[a4];  // G[4 a4 ..][r]
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-        for (int k = 0; k < d; ++k) {  // K = J + k; G[16I + i][16K + m] = Gs[(16I + i) * 64 + 16K + m]
-            const int K = J + k;
-            acc += dot16_tf(Gs + (16 * I + i) * 64 + 16 * K, Tf, 16 * J + j, 4 * K);
-        }
-        y[u] = acc;
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tn + 128 * u;
-        const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-        Yb[(J * 16 + j) * kYStride + i] = y[u];
-    }
-    solver_sync();
-    // T_IJ = -T_II Y_IJ
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tn + 128 * u;
-        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
-        y[u] = -dot16(Trm + I * 256 + i * 16, Yb + (J * 16 + j) * kYStride);
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tn + 128 * u;
-        const int J = idx >> 8, I = J + d, i = (idx >> 4) & 15, j = idx & 15;
-        Tf[tf_idx(16 * I + i, 16 * J + j)] = y[u];
-        st_timg(sm, 16 * I + i, 16 * J + j, y[u]);
-    }
-    solver_sync();
-}
-
-// T = (I + StrictLower(diag(beta) G))^-1 diag(beta) for a 64-token sub-chunk, by the
-// four solver warps; see the call site.
-__device__ __noinline__ void solve_T(const float *Gs, const float *bt, uint8_t *sm, int warp, int lane)
-{
-    const int tn = ((warp < 4 ? warp - 2 : warp - 4) << 5) + lane;  // 0..127
-    float *Tf = reinterpret_cast<float *>(sm + kPOffTf);
-    float *Trm = reinterpret_cast<float *>(sm + kPOffTrm);
-    float *Yb = reinterpret_cast<float *>(sm + kPOffY);
-    // diagonal tiles: thread (I, e) runs the forward substitution of column e of T_II,
-    // t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r (rows of tile I)
-    if (tn < 64) {
-        const int I = tn >> 4, e = tn & 15, b0 = 16 * I;
-        float tc[16];
-#pragma unroll
-        for (int a = 0; a < 16; ++a) tc[a] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            tc[r] = (r == e ? bt[b0 + e] : 0.f) - bt[b0 + r] * tc[r];
-            const float *gcol = Gs + (b0 + r) * 64 + b0;  // G[b0 + a][b0 + r], a = 0..15
-#pragma unroll
-            for (int a4 = (r + 1) >> 2; a4 < 4; ++a4) {
-                const float4 g4 = reinterpret_cast<const float4 *>(gcol)[a4];
-                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (4 * a4 + j > r) tc[4 * a4 + j] = fmaf(gv[j], tc[r], tc[4 * a4 + j]);
-            }
-        }
-#pragma unroll
-        for (int a4 = 0; a4 < 4; ++a4)
-            reinterpret_cast<float4 *>(Tf + (b0 + e) * 64)[(4 * I + a4) ^ e] =
-                make_float4(tc[4 * a4], tc[4 * a4 + 1], tc[4 * a4 + 2], tc[4 * a4 + 3]);
-#pragma unroll
-        for (int a = 0; a < 16; ++a) {
-            Trm[I * 256 + a * 16 + e] = tc[a];
-            st_timg(sm, b0 + a, b0 + e, a > e ? tc[a] : 0.f);
+            for (int j = 0; j < 4; ++j)
+                if (4 * a4 + j > r) tc[4 * a4 + j] = fmaf(gv[j], tc[r], tc[4 * a4 + j]);
         }
     }
-    solver_sync();
-    // off-diagonal tiles, by distance d = I - J
-    solve_level<1>(Gs, Tf, Trm, Yb, sm, tn);
-    solve_level<2>(Gs, Tf, Trm, Yb, sm, tn);
-    solve_level<3>(Gs, Tf, Trm, Yb, sm, tn);
+    __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + kPOffT);
+#pragma unroll
+    for (int a = 0; a < kPC; ++a) {
+        const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
+        timg[off >> 1] = __float2bfloat16_rn(a > e ? tc[a] : 0.f);
+    }
 }
 
 struct ProdParams {
@@ -352,7 +239,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     } else {
         // ------------------------------------------------------- math warps
         // G is kept column-major (Gs[c * 64 + a] = G[a][c]): lanes store
-        // consecutive words, and the solve reads a column as a broadcast row.
+        // consecutive words; being symmetric, it is row-major as well.
         const int t = threadIdx.x - 64;                  // 0..255
         const int quad = warp & 3, g = (warp - 2) >> 2;  // TMEM lane quadrant, column half
         const int row = quad * 32 + lane;                // TMEM lane (token or pair row)
@@ -434,15 +321,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             p_math_sync();
 
             if (!tok_warp) {
-                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta) on the four warps whose
-                //     TMEM lanes hold no token rows (warps 2, 3, 6, 7), blocked in 16 x 16 tiles:
-                //     the diagonal tiles T_II = (I + L_II)^-1 diag(beta_I) by forward substitution
-                //     (one column per thread), then the off-diagonal tiles by distance from the
-                //     diagonal, T_IJ = -T_II sum_{K=J}^{I-1} G_IK T_KJ (I > J), one element per
-                //     thread and step: the unit-lower system's rows I depend only on tiles of
-                //     smaller distance.  G is symmetric, so its column-major copy Gs is also
-                //     row-major.  The strictly lower part T_off goes to the bf16 image.
-                solve_T(Gs, bt, sm, warp, lane);
+                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta) on warps 2 and 3 (see
+                //     solve_T); warps 6 and 7 have nothing to do in this step.
+                if (warp == 2 || warp == 3) solve_T(Gs, bt, sm, t);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(r_ready);
