@@ -345,14 +345,23 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             tc_fence_after();
             uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
             float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
-            // pass 1: A_f -> bf16 image (shared memory), U_f -> workspace
+            // pass 1: A_f -> bf16 image (shared memory), U_f -> workspace.  TMEM loads
+            // go out two 16-column chunks at a time: each wait costs a full load
+            // latency, which the frame boundary otherwise pays seven times.
 #pragma unroll
-            for (int cc = 0; cc < 7; ++cc) {
+            for (int cp = 0; cp < 7; cp += 2) {
+            uint32_t ra2[2][16], ru2[2][16];
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
+                tmem_ld16(tmem + lane_off + kTmAccA + (cp + hf) * 16, ra2[hf]);
+                tmem_ld16(tmem + lane_off + kTmAccU + (cp + hf) * 16, ru2[hf]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
+                const int cc = cp + hf;
                 const uint32_t col = cc * 16;
-                uint32_t ra[16], ru[16];
-                tmem_ld16(tmem + lane_off + kTmAccA + col, ra);
-                tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
-                tmem_ld_wait();
+                const uint32_t *ra = ra2[hf], *ru = ru2[hf];
                 if (row < kD) {
                     float a[16];
 #pragma unroll
@@ -367,6 +376,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                                                  __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
                 }
             }
+            }
             if (row < kD) {  // key columns 112..127 of the image: zero
                 uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
@@ -376,13 +386,19 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             // touches only its own TMEM lanes, and has read all of them above
             // pass 2: H <- gamma H + U_f, C <- gamma C; A operands -bf16(H_prev), -bf16(C_prev)
 #pragma unroll
-            for (int cc = 0; cc < 7; ++cc) {
-                const uint32_t col = cc * 16;
-                uint32_t ru[16], rh[16], rc[16];
-                tmem_ld16(tmem + lane_off + kTmAccU + col, ru);
-                tmem_ld16(tmem + lane_off + kTmH + col, rh);
-                tmem_ld16(tmem + lane_off + kTmC + col, rc);
-                tmem_ld_wait();
+            for (int cp = 0; cp < 7; cp += 2) {
+            uint32_t ru2[2][16], rh2[2][16], rc2[2][16];
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
+                tmem_ld16(tmem + lane_off + kTmAccU + (cp + hf) * 16, ru2[hf]);
+                tmem_ld16(tmem + lane_off + kTmH + (cp + hf) * 16, rh2[hf]);
+                tmem_ld16(tmem + lane_off + kTmC + (cp + hf) * 16, rc2[hf]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
+                const uint32_t col = (cp + hf) * 16;
+                const uint32_t *ru = ru2[hf], *rh = rh2[hf], *rc = rc2[hf];
                 uint32_t hn0[8], hn1[8], cn0[8], cn1[8], ih[8], ic[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -399,6 +415,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                 tmem_st8(tmem + lane_off + kTmC + col + 8, cn1);
                 tmem_st8(tmem + lane_off + kTmImgH + col / 2, ih);
                 tmem_st8(tmem + lane_off + kTmImgC + col / 2, ic);
+            }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -775,12 +792,15 @@ __global__ void __launch_bounds__(kK2Threads, 1)
             if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 7; ++cc) {
-                uint32_t ra[16];
-                tmem_ld16(tmem + lane_off + cc * 16, ra);
+            for (int cp = 0; cp < 7; cp += 2) {  // two 16-column chunks per TMEM round trip
+                uint32_t ra2[2][16];
+#pragma unroll
+                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) tmem_ld16(tmem + lane_off + (cp + hf) * 16, ra2[hf]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) S[cc * 16 + j] -= __uint_as_float(ra[j]);
+                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) S[(cp + hf) * 16 + j] -= __uint_as_float(ra2[hf][j]);
             }
             tc_fence_before();
             if (p.states && row < kD) {
@@ -860,11 +880,17 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     const int n = t * kTQ + r;  // token of this row
                     uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) +
                                                             (((size_t)bf * p.N + n) * p.H + h) * kD);
+                    // the row in two TMEM round trips (four chunks, then three)
 #pragma unroll
-                    for (int cc = 0; cc < 7; ++cc) {
-                        uint32_t ra[16];
-                        tmem_ld16(acc + cc * 16, ra);
-                        tmem_ld_wait();
+                    for (int cp = 0; cp < 7; cp += 4) {
+                    uint32_t ra4[4][16];
+#pragma unroll
+                    for (int hf = 0; hf < 4 && cp + hf < 7; ++hf) tmem_ld16(acc + (cp + hf) * 16, ra4[hf]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int hf = 0; hf < 4 && cp + hf < 7; ++hf) {
+                        const int cc = cp + hf;
+                        const uint32_t *ra = ra4[hf];
                         float o[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(ra[j]) * rq;
@@ -878,6 +904,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                             orow[c8] = f32x8_to_bf16(o);
                             orow[c8 + 1] = f32x8_to_bf16(o + 8);
                         }
+                    }
                     }
                 }
                 if (kK2OStages > 0) fence_proxy_async_smem();
