@@ -166,6 +166,22 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// Same with an L2 cache-eviction policy for the written lines.
+__device__ __forceinline__ void bulk_s2g_hint(void *dst, const void *src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+// 16-byte global store with an L2 cache-eviction policy.
+__device__ __forceinline__ void st_global_hint(float4 *dst, float4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -53,6 +53,13 @@ namespace gdn {
 #ifndef GDN_K1_LO
 #define GDN_K1_LO 0
 #endif
+#ifndef GDN_WS_L2HINT
+#define GDN_WS_L2HINT 1
+#endif
+// K1 writes the per-frame workspace with an evict-last L2 policy (its k, v reads
+// and K2's q reads are evict-first), so that part of the 190 MB workspace of the
+// 20-head layer is still in the 126 MB L2 when K2 reads it: K2 246 -> 241 us.
+constexpr bool kWsKeepL2 = GDN_WS_L2HINT != 0;
 constexpr int kTS = GDN_K1_TS;                        // tokens per stage (one TMA box height)
 constexpr bool kK1Lo = GDN_K1_LO != 0;                // B as bf16 hi + lo (fp32-accurate U_f)
 constexpr uint32_t kTSPanel = kTS * kRowB;            // one 64-column panel of a stage
@@ -329,6 +336,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             tmem_st8(tmem + lane_off + kTmH + c8 * 8, wz);
         }
         tmem_st_wait();
+        const uint64_t ws_pol = kWsKeepL2 ? policy_evict_last() : 0;  // workspace lines K2 reads next
         // this warp's rows of the A_f image: rows 32*quad.. of each panel
         const int img_rows = quad == 3 ? kD - 96 : 32;
         const uint32_t img_off = quad * 32 * kRowB;
@@ -371,9 +379,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                     *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3) + 1)) = f32x8_to_bf16(a + 8);
                     float4 *u4 = reinterpret_cast<float4 *>(wsU) + (col / 4) * kD + row;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        u4[j * kD] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
-                                                 __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 v4 = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                                      __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+                        if (kWsKeepL2) st_global_hint(u4 + j * kD, v4, ws_pol);
+                        else u4[j * kD] = v4;
+                    }
                 }
             }
             }
@@ -423,8 +434,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(comp_ready);
-                bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
-                bulk_s2g(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off, img_rows * kRowB);
+                if (kWsKeepL2) {
+                    bulk_s2g_hint(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB, ws_pol);
+                    bulk_s2g_hint(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off,
+                                  img_rows * kRowB, ws_pol);
+                } else {
+                    bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
+                    bulk_s2g(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off, img_rows * kRowB);
+                }
                 bulk_commit();
             }
         }
