@@ -85,7 +85,7 @@ static size_t fwd_workspace_size(int B, int H, int F, int N, int D, unsigned fla
     if (D != 112) return (size_t)-1;
     TcPlan plan;
     if (!tc_plan(B, H, F, N, 0, &plan)) return (size_t)-1;
-    return plan.ws_bytes;
+    return (flags & GDN_FWD_PRODUCT) ? product_ws_bytes(plan) : plan.ws_bytes;
 }
 
 size_t gdn_frame_fwd_workspace_size(int B, int H, int F, int N, int D) { return fwd_workspace_size(B, H, F, N, D, 0); }
@@ -125,7 +125,8 @@ static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, 
     const int reverse = (flags & GDN_FWD_REVERSE) ? 1 : 0;
     TcPlan plan;
     if (!tc_plan(B, H, F, N, 0, &plan)) return GDN_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < plan.ws_bytes) return GDN_ERR_WORKSPACE;
+    const size_t need = product ? product_ws_bytes(plan) : plan.ws_bytes;
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
     unsigned *status = device_status_word();
     if (!status) return GDN_ERR_CUDA;

@@ -71,6 +71,9 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
 // token-ordered ("product") reading, D == 112: per-frame transitions by the
 // UT-transform kernel into the plan's frame workspace and their chunk
 // composites (gdn_product.cu), and the whole forward (gdn_tc.cu).
+// Workspace of the product reading: the plan's, then the pre-pass's T_off images.
+size_t product_ws_T_offset(const TcPlan &plan);
+size_t product_ws_bytes(const TcPlan &plan);
 cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *beta, const TcPlan &plan, float c,
                                     int reverse, void *workspace, unsigned *status, cudaStream_t stream);
 cudaError_t launch_chunk_composite_tc(const float *gamma, const TcPlan &plan, int reverse, void *workspace,

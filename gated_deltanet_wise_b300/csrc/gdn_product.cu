@@ -15,15 +15,20 @@
 //     X   = T R = diag(beta) R + T_off R                (T_off = T - diag(beta)),
 //     [Abar ; W] += X^T K^ = (X diag(c/r))^T K         (raw K: an exact operand).
 //
-// One CTA per (frame, chain), sub-chunks in order.  tcgen05 forms G, R~ (the
-// product K^ [Abar ; W]^T, N = 2 x 128), T_off R (accumulated on top of the
-// fp32 diag(beta) R stored into TMEM) and the pair update (fp32 TMEM
-// accumulators, X split hi + lo); CUDA cores solve the 64 x 64 unit-triangular
-// system for T (one column per thread, in registers).  Abar is accumulated
-// transposed, so the accumulator's lanes are Abar's columns: its bf16 image is
-// then directly the B operand the scan kernel multiplies S by, and the kernel
-// writes (Abar_f^T image, W_f) in the per-frame workspace format of the sum
-// reading's frame-statistics kernel.
+// G and T depend only on the sub-chunk's keys and write strengths, never on the
+// running pair, so two kernels split the work:
+//   K1t, over all sub-chunks of all frames at once: G on tcgen05 from the raw
+//     keys, scaled in fp32 by c/r per token, and T by forward substitution on CUDA
+//     cores (one column per thread, in registers); T_off goes to the workspace as
+//     an 8 KB bf16 MMA image per sub-chunk;
+//   K1p, one CTA per (frame, chain), sub-chunks in order: tcgen05 forms R~ (the
+//     product K^ [Abar ; W]^T, N = 2 x 128), T_off R (accumulated on top of the
+//     fp32 diag(beta) R stored into TMEM, T_off loaded with the keys) and the pair
+//     update (fp32 TMEM accumulators, X split hi + lo).
+// Abar is accumulated transposed, so the accumulator's lanes are Abar's columns:
+// its bf16 image is then directly the B operand the scan kernel multiplies S by,
+// and K1p writes (Abar_f^T image, W_f) in the per-frame workspace format of the
+// sum reading's frame-statistics kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -61,36 +66,37 @@ constexpr uint32_t kIdRW = idesc_bf16(128, 128, false, false);  // R~_W = K^ W^T
 constexpr uint32_t kIdX = idesc_bf16(128, 256, false, true);    // X += T_off R
 constexpr uint32_t kIdU = idesc_bf16(128, kD, true, true);      // pair += X'^T K
 
-__device__ __forceinline__ void p_math_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// T = (I + StrictLower(diag(beta) G))^-1 diag(beta) for a 64-token sub-chunk by
-// warps 2 and 3, one column e per thread, by forward substitution in right-looking
-// order: once t_r is final it is added into every later row's sum (independent
-// FMAs, broadcast float4 reads of column r of G);
-//     t_a = [a == e] beta_e - beta_a sum_{r<a} G[a][r] t_r.
-// The strictly lower part T_off goes to the bf16 image (row a, column e).  (Timed
-// alone, one CTA of these two warps per SM: ~6,000 cycles per solve; a
-// left-looking order with four partial sums took ~6,500, and neither a 16 x 16
-// blocked form on four warps nor two lanes per column beat it inside the kernel.)
-__device__ __noinline__ void solve_T(const float *Gs, const float *bt, uint8_t *sm, int e)
+// T = (I + StrictLower(diag(beta) G))^-1 diag(beta) for a 64-token sub-chunk, one
+// column e per thread, by forward substitution in right-looking order.  The
+// caller passes Ls = -diag(beta) G column-major (Ls[r * 64 + a] = -beta_a G[a][r]),
+// so that with t initialised to beta_e e_e each step is only
+//     t_a += Ls[a][r] t_r   for every a > r
+// (t_r is final once the steps before r are done): the loop-carried path is one
+// FMA per step, and the column reads of Ls are broadcast float4s that the fully
+// unrolled steps can issue early.  The strictly lower part T_off goes to the
+// bf16 image `timg` (64 rows of 128 bytes, 128-byte swizzle: row a, column e),
+// the diagonal and above as zeros.  R0 > 0: the caller's columns are all >= R0,
+// whose entries above row R0 vanish, so the substitution starts there.
+template <int R0>
+__device__ __noinline__ void solve_T(const float *Ls, const float *bt, uint8_t *timg_bytes, int e)
 {
     const float be = bt[e];
     float tc[kPC];
 #pragma unroll
-    for (int a = 0; a < kPC; ++a) tc[a] = 0.f;
+    for (int a = 0; a < kPC; ++a) tc[a] = (a == e) ? be : 0.f;
 #pragma unroll
-    for (int r = 0; r < kPC; ++r) {
-        tc[r] = (r == e ? be : 0.f) - bt[r] * tc[r];
+    for (int r = R0; r < kPC; ++r) {
 #pragma unroll
         for (int a4 = (r + 1) >> 2; a4 < kPC / 4; ++a4) {
-            const float4 g4 = reinterpret_cast<const float4 *>(Gs + r * 64)[a4];  // G[4 a4 ..][r]
-            const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+            const float4 l4 = reinterpret_cast<const float4 *>(Ls + r * 64)[a4];  // -beta_a G[a][r], a = 4 a4 ..
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (4 * a4 + j > r) tc[4 * a4 + j] = fmaf(gv[j], tc[r], tc[4 * a4 + j]);
+                if (4 * a4 + j > r) tc[4 * a4 + j] = fmaf(lv[j], tc[r], tc[4 * a4 + j]);
         }
     }
-    __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(sm + kPOffT);
+    __nv_bfloat16 *timg = reinterpret_cast<__nv_bfloat16 *>(timg_bytes);
 #pragma unroll
     for (int a = 0; a < kPC; ++a) {
         const uint32_t off = a * kRowB + ((((uint32_t)e >> 3) ^ (a & 7)) << 4) + (e & 7) * 2;
@@ -98,8 +104,208 @@ __device__ __noinline__ void solve_T(const float *Gs, const float *bt, uint8_t *
     }
 }
 
+// ===================================================================== K1t
+// The UT transform's T of every 64-token sub-chunk, ahead of the pair chain: T
+// depends on the sub-chunk's keys and write strengths only, never on the running
+// pair (Abar, W), so all of them are formed here in parallel and K1p reads them.
+// Persistent CTAs of kTPairs independent warp pairs; a pair takes sub-chunks in
+// turn: TMA the raw key tile, norms r_a, G_raw = K K^T on tcgen05 (exact bf16
+// products, fp32 accumulation), G = (c/r_a)(c/r_b) G_raw while reading it out of
+// TMEM, the solve, and one bulk store of the 8 KB T_off image.  Pairs of warps
+// (2p, 2p + 1) sit in TMEM lane quadrants (0, 1) or (2, 3); a pair of the second
+// kind points its MMA's A operand 64 rows before the tile, so that the tile's
+// rows, and G's, land in lanes 64..127.
+constexpr int kTPairs = 4;
+constexpr int kTThreads = kTPairs * 64;                     // 256
+constexpr uint32_t kTPairBytes = 49152;                     // two key tiles (16 KB each; a consumed one takes
+                                                            // its T_off image), G (16 KB fp32)
+constexpr uint32_t kTOffBar = kTPairs * kTPairBytes;        // 196608
+constexpr uint32_t kTOffArr = kTOffBar + 256;               // per pair: c/r and beta of 64 tokens
+constexpr uint32_t kTSmem = kTOffArr + kTPairs * 512 + 1024;
+static_assert(kTSmem <= kMaxSmem, "T pre-pass shared memory");
+
+struct TParams {
+    const float *beta;
+    uint8_t *ws_T;   // [B*H][F][n_sc] x 8 KB T_off images, by processing position
+    unsigned *status;
+    int B, H, F, N, n_sc;
+    float c;
+    int reverse;
+};
+
+__device__ __forceinline__ void pair_sync(int p) { asm volatile("bar.sync %0, 64;" ::"r"(p + 1) : "memory"); }
+// Barrier over one pair that also ANDs a flag across its 64 threads, so both warps
+// take the same branch after a bounded wait.
+__device__ __forceinline__ bool pair_sync_and(int p, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 64, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(p + 1)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kTThreads, 1)
+    kt_ut_transform_kernel(const __grid_constant__ CUtensorMap mapK, const TParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTOffBar);
+    uint64_t *kfull = bars, *gfull = bars + 2 * kTPairs;  // kfull[pair][buffer], gfull[pair]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * kTPairs);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 3 * kTPairs + 1);
+    const int warp = threadIdx.x >> 5;
+    const int pr = warp >> 1, tn = threadIdx.x & 63;           // pair, thread within the pair
+    const int quad = warp & 3, lg = (quad & 2) * 32;           // TMEM lanes of this pair: lg .. lg + 63
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTPairs; ++i) {
+            mbar_init(&kfull[2 * i], 1);
+            mbar_init(&kfull[2 * i + 1], 1);
+            mbar_init(&gfull[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+    griddep_launch_dependents();
+    griddep_wait();
+
+    uint8_t *pbase = sm + pr * kTPairBytes;                    // key tiles 0, 1; G
+    float *Gs = reinterpret_cast<float *>(pbase + 32768);
+    float *cr = reinterpret_cast<float *>(sm + kTOffArr + pr * 512), *bt = cr + 64;
+    const uint32_t pbase_addr = sbase + pr * kTPairBytes;
+    const uint32_t dcol = tmem + 64u * pr;                     // this pair's 64 accumulator columns
+    const long long items = (long long)p.B * p.H * p.F * p.n_sc;
+    const long long stride = (long long)gridDim.x * kTPairs;
+    const long long first = (long long)blockIdx.x * kTPairs + pr;
+    const uint64_t pol = policy_evict_first();
+    // item -> (chain, processing position, sub-chunk) and the key tile's TMA coordinates
+    auto decode = [&](long long item, int &bh, int &f, int &sc, int &h, int &bf) {
+        sc = (int)(item % p.n_sc);
+        const long long bhf = item / p.n_sc;
+        f = (int)(bhf % p.F);
+        bh = (int)(bhf / p.F);
+        const int b = bh / p.H;
+        h = bh % p.H;
+        bf = b * p.F + frame_at(f, p.F, p.reverse);
+    };
+    auto issue_tile = [&](long long item, int buf) {  // leader only
+        int bh, f, sc, h, bf;
+        decode(item, bh, f, sc, h, bf);
+        uint8_t *dst = pbase + buf * 16384;
+        mbar_arrive_expect_tx(&kfull[2 * pr + buf], 2 * kPPanel);
+        tma_load_4d(dst, &mapK, &kfull[2 * pr + buf], 0, h, sc * kPC, bf, pol);
+        tma_load_4d(dst + kPPanel, &mapK, &kfull[2 * pr + buf], 64, h, sc * kPC, bf, pol);
+    };
+    bool ok = true;
+    int k_issued = 0, k_waited = 0;  // (leader) key-tile loads issued / consumed, per pair
+    bool g_pending = false;          // (leader) a G MMA not yet waited for
+    if (tn == 0 && first < items) {
+        issue_tile(first, 0);
+        ++k_issued;
+    }
+    int use = 0;
+    for (long long item = first; item < items; item += stride, ++use) {
+        int bh, f, sc, h, bf;
+        decode(item, bh, f, sc, h, bf);
+        const int buf = use & 1;
+        uint8_t *kbuf = pbase + buf * 16384;
+        const uint32_t kaddr = pbase_addr + buf * 16384;
+        const int m = min(kPC, p.N - sc * kPC);
+        // (1) the next item's key tile into the other buffer, once the store of the
+        //     T_off image that the item before this one left there has read it
+        if (tn == 0 && item + stride < items) {
+            bulk_wait_read_all();
+            issue_tile(item + stride, buf ^ 1);
+            ++k_issued;
+        }
+        bt[tn] = tn < m ? __ldg(p.beta + ((size_t)bf * p.N + sc * kPC + tn) * p.H + h) : 0.f;
+        ok = mbar_wait_warp(&kfull[2 * pr + buf], (use >> 1) & 1, abort_flag);
+        if (tn == 0 && ok) ++k_waited;
+        // (2) G_raw on the tensor cores; c / ||k_a|| per token meanwhile
+        if (tn == 0 && ok) {
+            tc_fence_after();
+            const uint32_t abase = kaddr - (uint32_t)lg * kRowB;  // tile rows land in lanes lg..lg + 63
+#pragma unroll
+            for (int ks = 0; ks < 7; ++ks) {
+                const uint32_t koff = (ks >> 2) * kPPanel + (ks & 3) * 32;
+                mma_bf16(dcol, sdesc_sw128(abase + koff, 16, 1024), sdesc_sw128(kaddr + koff, 16, 1024), kIdG, ks > 0);
+            }
+            mma_commit(&gfull[pr]);
+            g_pending = true;
+        }
+        if (ok) {
+            float ss = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {  // both panels of token tn's row (columns 112..127 are zero)
+                float f8[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(kbuf + (c8 >> 3) * kPPanel + sw128_off(tn, c8 & 7)), f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
+            }
+            cr[tn] = p.c * rsqrtf(ss + kEps);
+        }
+        if (!(ok = pair_sync_and(pr, ok))) break;
+        // (3) Ls = -diag(beta) G with G = (c/r_a)(c/r_b) G_raw, column-major, from this
+        //     thread's TMEM lane (row a = tn)
+        ok = mbar_wait_warp(&gfull[pr], use & 1, abort_flag);
+        if (tn == 0 && ok) g_pending = false;
+        if (ok) {
+            tc_fence_after();
+            const float ia = -bt[tn] * cr[tn];  // row a = tn of Ls = -beta_a (c/r_a)(c/r_b) G_raw[a][b]
+            const uint32_t lane_addr = dcol + ((uint32_t)(lg + (warp & 1) * 32) << 16);
+            uint32_t rg[4][16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(lane_addr + q4 * 16, rg[q4]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int bcol = q4 * 16 + j;
+                    Gs[bcol * 64 + tn] = __uint_as_float(rg[q4][j]) * ia * cr[bcol];
+                }
+        }
+        tc_fence_before();
+        if (!(ok = pair_sync_and(pr, ok))) break;
+        // (4) the solve (the upper 32 columns start at row 32); the T_off image goes over
+        //     the consumed key tile
+        if (tn < 32) solve_T<0>(Gs, bt, kbuf, tn);
+        else solve_T<32>(Gs, bt, kbuf, tn);
+        fence_proxy_async_smem();
+        pair_sync(pr);
+        if (tn == 0) {
+            bulk_s2g(p.ws_T + (size_t)item * 8192, kbuf, 8192);
+            bulk_commit();
+        }
+    }
+    if (tn == 0) {  // let this pair's copies and MMA in flight land before the CTA exits
+        for (int u = k_waited; u < k_issued; ++u) mbar_wait_drain(&kfull[2 * pr + (u & 1)], (u >> 1) & 1);
+        if (g_pending) mbar_wait_drain(&gfull[pr], use & 1);
+    }
+    if (tn == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 struct ProdParams {
     const float *beta;
+    const uint8_t *ws_T; // [BH][F][n_sc] x 8 KB T_off images from the pre-pass
     uint8_t *ws_frames;  // [BH][F] x kFrameWs, by processing position
     unsigned *status;
     int B, H, F, N;
@@ -114,8 +320,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPOffBar);
-    uint64_t *kv_full = bars + 0, *kv_empty = bars + 2, *prep_done = bars + 4, *g_full = bars + 5;
-    uint64_t *g_read = bars + 6, *simg_ready = bars + 7, *rt_full = bars + 8, *r_ready = bars + 9;
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 2, *prep_done = bars + 4;
+    uint64_t *simg_ready = bars + 7, *rt_full = bars + 8, *r_ready = bars + 9;
     uint64_t *x_full = bars + 10, *x_ready = bars + 11, *upd_done = bars + 12, *drain = bars + 13;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 15);
@@ -135,8 +341,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(&kv_empty[i], 1);
         }
         mbar_init(prep_done, 8);
-        mbar_init(g_full, 1);
-        mbar_init(g_read, 4);
         mbar_init(simg_ready, 8);
         mbar_init(rt_full, 1);
         mbar_init(r_ready, 8);
@@ -166,11 +370,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int kb = sc & 1;
                 if (sc >= 2 && !mbar_wait(&kv_empty[kb], ((sc >> 1) - 1) & 1, abort_flag)) break;
                 uint8_t *kd = sm + kPOffK + kb * 2 * kPPanel, *vd = sm + kPOffV + kb * 2 * kPPanel;
-                mbar_arrive_expect_tx(&kv_full[kb], 4 * kPPanel);
+                mbar_arrive_expect_tx(&kv_full[kb], 4 * kPPanel + 8192);
                 tma_load_4d(kd, &mapK, &kv_full[kb], 0, h, sc * kPC, bf, pol);
                 tma_load_4d(kd + kPPanel, &mapK, &kv_full[kb], 64, h, sc * kPC, bf, pol);
                 tma_load_4d(vd, &mapV, &kv_full[kb], 0, h, sc * kPC, bf, pol);
                 tma_load_4d(vd + kPPanel, &mapV, &kv_full[kb], 64, h, sc * kPC, bf, pol);
+                bulk_g2s(sm + kPOffT + kb * 8192, p.ws_T + ((size_t)(bh * p.F + f) * n_sc + sc) * 8192, 8192,
+                         &kv_full[kb]);
                 ++issued;
             }
             if (*abort_flag)  // let loads already in flight land before the CTA exits
@@ -187,17 +393,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int kb = sc & 1, ph = sc & 1;
                 const uint32_t kraw = sbase + kPOffK + kb * 2 * kPPanel, kh = sbase + kPOffKh;
                 if (!(ok = mbar_wait(prep_done, ph, abort_flag))) break;
-                tc_fence_after();
-                // G = K^ K^^T (64 x 64, lanes = tokens)
-#pragma unroll
-                for (int ks = 0; ks < 7; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kPPanel + (ks & 3) * 32;
-                    mma_bf16(tmem + kPTmX, sdesc_sw128(kh + koff, 16, 1024), sdesc_sw128(kh + koff, 16, 1024), kIdG,
-                             ks > 0);
-                }
-                mma_commit(g_full);
-                // R~ = K^ [Abar ; W]^T once G is read out and the pair image is current
-                if (!(ok = mbar_wait(g_read, ph, abort_flag))) break;
+                // R~ = K^ [Abar ; W]^T once the pair image is current
                 if (!(ok = mbar_wait(simg_ready, ph, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
@@ -212,8 +408,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (!(ok = mbar_wait(r_ready, ph, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < kPC / 16; ++ks)
-                    mma_bf16(tmem + kPTmX, sdesc_sw128(sbase + kPOffT + ks * 32, 16, 1024),
+                for (int ks = 0; ks < kPC / 16; ++ks)  // T_off of this sub-chunk from the pre-pass (rows 64.. unused)
+                    mma_bf16(tmem + kPTmX, sdesc_sw128(sbase + kPOffT + kb * 8192 + ks * 32, 16, 1024),
                              sdesc_sw128(sbase + kPOffR + ks * 2048, kPPanel, 1024), kIdX, 1u);
                 mma_commit(x_full);
                 // pair update (X' = X c/r as hi + lo; all operands token-row tiles, MN-major):
@@ -238,22 +434,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else {
         // ------------------------------------------------------- math warps
-        // G is kept column-major (Gs[c * 64 + a] = G[a][c]): lanes store
-        // consecutive words; being symmetric, it is row-major as well.
         const int t = threadIdx.x - 64;                  // 0..255
         const int quad = warp & 3, g = (warp - 2) >> 2;  // TMEM lane quadrant, column half
         const int row = quad * 32 + lane;                // TMEM lane (token or pair row)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const bool tok_warp = quad < 2;                  // lanes 0..63 hold the token-indexed results
-        float *Gs = reinterpret_cast<float *>(sm + kPOffXlo);
         bool ok = true;
 
-        // the pair starts at zero: zero image; the T_off image's tiles above the
-        // diagonal are never written by the solve and stay zero
+        // the pair starts at zero: zero image
         for (int e = t; e < (int)(4 * kPSPanel / 16); e += 256)
             reinterpret_cast<uint4 *>(sm + kPOffSA)[e] = make_uint4(0, 0, 0, 0);
-        for (int e = t; e < (int)(kPC * kRowB / 16); e += 256)
-            reinterpret_cast<uint4 *>(sm + kPOffT)[e] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(simg_ready);
@@ -300,31 +490,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (lane == 0) mbar_arrive(prep_done);
             }
 
-            // (2) G out of TMEM into shared memory (token warps), visible to all math warps
-            if (tok_warp) {
-                if (ok) ok = mbar_wait_warp(g_full, ph, abort_flag);
-                tc_fence_after();
-                if (ok) {
-                    uint32_t rg[16];
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        tmem_ld16(tmem + lane_off + kPTmX + g * 32 + cc * 16, rg);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) Gs[(g * 32 + cc * 16 + j) * 64 + row] = __uint_as_float(rg[j]);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(g_read);
-            }
-            p_math_sync();
-
             if (!tok_warp) {
-                // (3) T = (I + StrictLower(diag(beta) G))^-1 diag(beta) on warps 2 and 3 (see
-                //     solve_T); warps 6 and 7 have nothing to do in this step.
-                if (warp == 2 || warp == 3) solve_T(Gs, bt, sm, t);
-                fence_proxy_async_smem();
+                // (3) T_off comes from the pre-pass with the sub-chunk's keys; these warps have
+                //     nothing to do in this step
                 __syncwarp();
                 if (lane == 0) mbar_arrive(r_ready);
             } else if (tok_warp) {
@@ -670,9 +838,19 @@ __global__ void __launch_bounds__(kCThreads, 1) kc_chunk_composite_kernel(const 
     }
 }
 
+// The product reading's T_off images (8 KB per 64-token sub-chunk of every frame
+// and chain) follow the plan's workspace.
+size_t product_ws_T_offset(const TcPlan &pl) { return (pl.ws_bytes + 255) / 256 * 256; }
+size_t product_ws_bytes(const TcPlan &pl)
+{
+    const size_t n_sc = ((size_t)pl.N + kPC - 1) / kPC;
+    return product_ws_T_offset(pl) + (size_t)pl.B * pl.H * pl.F * n_sc * 8192;
+}
+
 namespace {
 constexpr int kMaxDevP = 64;
 bool g_p_attr[kMaxDevP];
+bool g_t_attr[kMaxDevP];
 bool g_c_attr[kMaxDevP];
 }  // namespace
 
@@ -691,8 +869,35 @@ cudaError_t launch_frame_product_tc(const void *k, const void *v, const float *b
     CUtensorMap mk, mv;
     if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kPC) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kPC))
         return cudaErrorInvalidValue;
+    // the pre-pass: T_off of every sub-chunk
+    const int n_sc = (pl.N + kPC - 1) / kPC;
+    uint8_t *ws_T = static_cast<uint8_t *>(workspace) + product_ws_T_offset(pl);
+    {
+        if (!g_t_attr[dev]) {
+            e = cudaFuncSetAttribute(kt_ut_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTSmem);
+            if (e != cudaSuccess) return e;
+            g_t_attr[dev] = true;
+        }
+        TParams tp;
+        tp.beta = beta;
+        tp.ws_T = ws_T;
+        tp.status = status;
+        tp.B = pl.B;
+        tp.H = pl.H;
+        tp.F = pl.F;
+        tp.N = pl.N;
+        tp.n_sc = n_sc;
+        tp.c = c;
+        tp.reverse = reverse;
+        const long long items = (long long)pl.B * pl.H * pl.F * n_sc;
+        const long long ctas = (items + kTPairs - 1) / kTPairs;
+        const int grid = (int)(ctas < kSms ? ctas : kSms);
+        kt_ut_transform_kernel<<<grid, kTThreads, kTSmem, stream>>>(mk, tp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     ProdParams p;
     p.beta = beta;
+    p.ws_T = ws_T;
     p.ws_frames = static_cast<uint8_t *>(workspace) + pl.off_frames;
     p.status = status;
     p.B = pl.B;

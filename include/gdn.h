@@ -108,7 +108,9 @@ gdn_status_t gdn_frame_fwd(const void *q, const void *k, const void *v,
  * The two readings differ at order (c_k^2 ||k^||^2)^2 per token pair: at the
  * default key_scale they agree to about 1e-8; with unit keys (key_scale = 1)
  * they differ at first order.  Arguments, layouts, ownership and status codes
- * are those of gdn_frame_fwd; the workspace size has its own query.  Results
+ * are those of gdn_frame_fwd; the workspace size has its own query (larger than
+ * gdn_frame_fwd's: it also holds the UT transform's T of every 64-token
+ * sub-chunk, 8 KB each, formed by a pre-pass over all sub-chunks).  Results
  * match the fp64 definition within 5e-3 relative Frobenius error on o and
  * S_out for inputs drawn as in the tests, key_scale up to 1.
  */

@@ -25,7 +25,12 @@ int main(void)
     const size_t err = (size_t)-1;
     size_t ws = gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112);
     CHECK(ws != err && ws > (size_t)20 * 121 * 78848);
-    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_PRODUCT | GDN_FWD_REVERSE) == ws);
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_REVERSE) == ws);
+    /* the token-ordered reading adds one 8 KB T_off image per 64-token sub-chunk */
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_PRODUCT | GDN_FWD_REVERSE) >=
+          ws + (size_t)20 * 121 * 14 * 8192);
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_PRODUCT) ==
+          gdn_frame_fwd_product_workspace_size(1, 20, 121, 880, 112));
     CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 4u) == err);
     CHECK(gdn_frame_fwd_workspace_size(1, 1, 2, 8, 64) == err);
     CHECK(gdn_frame_step_workspace_size(1, 20, 880, 112) == 0);
