@@ -130,24 +130,50 @@ __global__ void __launch_bounds__(256) kb_frame_grad(const float *S_in, const fl
 
 // ------------------------------------------------ token-row gradient kernels
 // One CTA per (frame, chain), 128-token tiles of the frame's rows through TMA
-// into tcgen05 GEMMs against per-frame fp32 matrices given as hi + lo bf16
-// images (image row j = column j of the matrix, K-major); the epilogue (thread
-// = token row) applies the chain rule through the normalisations and writes
-// the final fp32 gradients.
+// into tcgen05 GEMMs against per-frame fp32 matrices given as bf16 images
+// (image row j = column j of the matrix, K-major), hi only or hi + lo; the
+// epilogue (thread = token row) applies the chain rule through the
+// normalisations and writes the final fp32 gradients.
 //   kMode 0: acc = dO W (W = S_f)  ->  dq^ = S_f^T do;  dq = (dq^ - q (q.dq^)/rho^2) / rho
-//            two stages of (dO, q) tiles, two accumulator slots.
 //   kMode 1: acc0 = k Dsym, acc1 = v G, acc2 = k G^T (the G image read MN-major:
 //            row j, column i holds G[i][j], which is B[n = i][k = j] = G[i][j]);
 //            with k^ = (c/r) k: dk^ = beta ((c/r) acc0 + acc1),
 //            dk = (c/r)(dk^ - k (k.dk^)/r^2),  dv = beta (c/r) acc2,
-//            dbeta = 1/2 (c/r)^2 k.acc0 + (c/r) k.acc1;  one stage of (k, v).
-constexpr int kGThreads = 320;                    // producer, MMA, 4 image warps, 4 output warps
-constexpr uint32_t kGOffImg = 0;  // W0 hi, W0 lo (, W1 hi, W1 lo), 32 KB each; then the (x0, x1) tile stages
-// mode 0: 2 images + 2 stages x 2 tiles; mode 1: 4 images + 1 stage x 2 tiles: both 196,608 B
-constexpr uint32_t kGOffBar = 6 * kImgBytes;
+//            dbeta = 1/2 (c/r)^2 k.acc0 + (c/r) k.acc1.
+// Shared memory is seven 32 KB slots: the images first, then as many stages
+// of the two token tiles as fit, the last slot staging the gradient rows for
+// TMA stores (per output warp two 32-row x 16-column boxes of each output,
+// 64-byte swizzle).  TMEM holds one accumulator set per stage in mode 0 and a
+// single set of three in mode 1.
+#ifndef GDN_BWD_LO0
+#define GDN_BWD_LO0 1  // mode 0 keeps the lo image of S_f
+#endif
+#ifndef GDN_BWD_LO1
+#define GDN_BWD_LO1 0  // mode 1 keeps the lo images of Dsym_f and G_f
+#endif
+#ifndef GDN_BWD_TMA_ST
+#define GDN_BWD_TMA_ST 1  // gradient rows leave through shared memory and TMA stores
+#endif
+constexpr int kGThreads = 320;  // producer, MMA, 4 image warps, 4 output warps
+constexpr int kGSlots = 7;
+constexpr uint32_t kGOffImg = 0;
+constexpr uint32_t kGOffBar = kGSlots * kImgBytes;
+constexpr uint32_t kGOffStg = (kGSlots - 1) * kImgBytes;  // staging slot: 8 KB per output warp
 constexpr uint32_t kGSmem = kGOffBar + 256 + 1024;
 static_assert(kGSmem <= kMaxSmem, "token-gradient kernel shared memory");
 constexpr uint32_t kIdescKMN = idesc_bf16(128, kD, false, true);
+
+template <int kMode> struct TokGradShape {
+    static constexpr int kLo = kMode == 0 ? GDN_BWD_LO0 : GDN_BWD_LO1;
+    static constexpr int kMats = kMode == 0 ? 1 : 2;
+    static constexpr int kImgPer = kLo ? 2 : 1;                     // images per matrix
+    static constexpr int kImgs = kMats * kImgPer;
+    static constexpr int kStages = (kGSlots - GDN_BWD_TMA_ST - kImgs) / 2;   // (x0, x1) tile stages
+    static constexpr int kAcc = kMode == 0 ? 1 : 3;                 // accumulators per tile
+    static constexpr int kAccSets = kMode == 0 ? (kStages < 4 ? kStages : 4) : 1;
+    static_assert(kStages >= 1 && kStages <= 4, "token-gradient stages");
+    static_assert(kAcc * kAccSets * 128 <= 512, "token-gradient TMEM");
+};
 
 struct TokGradParams {
     const float *W0, *W1;   // mode 0: S states [BH][F]; mode 1: Dsym [BH][F], G states [BH][F+1] (G_f at F-1-f)
@@ -161,35 +187,42 @@ struct TokGradParams {
 template <int kMode>
 __global__ void __launch_bounds__(kGThreads, 1)
     kg_token_grad_kernel(const __grid_constant__ CUtensorMap mapX0, const __grid_constant__ CUtensorMap mapX1,
+                         const __grid_constant__ CUtensorMap mapG0, const __grid_constant__ CUtensorMap mapG1,
                          const TokGradParams p)
 {
-    constexpr int kStages = kMode == 0 ? 2 : 1;
-    constexpr int kAcc = kMode == 0 ? 1 : 3;       // accumulators per tile
-    constexpr uint32_t kOffBar = kGOffBar;
-    constexpr uint32_t kOffX = kMode == 0 ? 2 * kImgBytes : 4 * kImgBytes;
+    using Sh = TokGradShape<kMode>;
+    constexpr int kStages = Sh::kStages, kAccSets = Sh::kAccSets, kAcc = Sh::kAcc;
+    constexpr uint32_t kOffX = Sh::kImgs * kImgBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-    uint64_t *x_full = bars + 0, *x_empty = bars + 2, *acc_full = bars + 4, *acc_free = bars + 6;
-    uint64_t *img_ready = bars + 8, *drain = bars + 9;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 11);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kGOffBar);
+    uint64_t *x_full = bars + 0, *x_empty = bars + 4, *acc_full = bars + 8, *acc_free = bars + 12;
+    uint64_t *img_ready = bars + 16, *img_free = bars + 17, *drain = bars + 18;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 19);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 20);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = p.B * p.H;
-    const int f = blockIdx.x / BH, bh = blockIdx.x % BH;
-    const int b = bh / p.H, h = bh % p.H;
-    const int bf = b * p.F + f;
+    const int n_items = BH * p.F;  // item = (frame f, chain bh), f major
     const int n_tiles = (p.N + 127) / 128;
+    // the frame's matrices: W0 of item it; W1 (mode 1) G_f at slot F-1-f
+    auto mat = [&](int w, int it) {
+        const int f = it / BH, bh = it % BH;
+        return w == 0 ? p.W0 + ((size_t)bh * p.F + f) * kStateFloats
+                      : p.W1 + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kStateFloats;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 5);  // the tile's MMAs + the four output warps (epilogue reads x1 / x0)
+        }
+        for (int i = 0; i < kAccSets; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_free[i], 4);
         }
         mbar_init(img_ready, 4);
+        mbar_init(img_free, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -208,199 +241,298 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int issued = 0;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % kStages, u = t / kStages;
-                if (u >= 1 && !mbar_wait(&x_empty[s], (u - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&x_full[s], 2 * kImgBytes);
-                for (int w = 0; w < 2; ++w) {
-                    uint8_t *dst = sm + xtile(s, w);
-                    const CUtensorMap *m = w ? &mapX1 : &mapX0;
-                    tma_load_4d(dst, m, &x_full[s], 0, h, t * 128, bf, pol);
-                    tma_load_4d(dst + kImgPanel, m, &x_full[s], 64, h, t * 128, bf, pol);
+            int g = 0;  // tiles issued by this CTA
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const int f = it / BH, bh = it % BH;
+                const int b = bh / p.H, h = bh % p.H, bf = b * p.F + f;
+                for (int t = 0; t < n_tiles; ++t, ++g) {
+                    const int s = g % kStages, u = g / kStages;
+                    if (u >= 1 && !(ok = mbar_wait(&x_empty[s], (u - 1) & 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(&x_full[s], 2 * kImgBytes);
+                    for (int w = 0; w < 2; ++w) {
+                        uint8_t *dst = sm + xtile(s, w);
+                        const CUtensorMap *m = w ? &mapX1 : &mapX0;
+                        tma_load_4d(dst, m, &x_full[s], 0, h, t * 128, bf, pol);
+                        tma_load_4d(dst + kImgPanel, m, &x_full[s], 64, h, t * 128, bf, pol);
+                    }
                 }
-                ++issued;
             }
             if (*abort_flag)
-                for (int s = 0; s < kStages && s < issued; ++s) {
-                    const int last = ((issued - 1 - s) / kStages) * kStages + s;
+                for (int s = 0; s < kStages && s < g; ++s) {
+                    const int last = ((g - 1 - s) / kStages) * kStages + s;
                     mbar_wait_drain(&x_full[s], (last / kStages) & 1);
                 }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(img_ready, 0, abort_flag);
-            tc_fence_after();
-            for (int t = 0; t < n_tiles && ok; ++t) {
-                const int s = t % kStages, u = t / kStages;
-                if (!(ok = mbar_wait(&x_full[s], u & 1, abort_flag))) break;
-                if (u >= 1 && !(ok = mbar_wait(&acc_free[s], (u - 1) & 1, abort_flag))) break;
+            bool ok = true;
+            int g = 0, i = 0;  // tiles, items of this CTA
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++i) {
+                if (!(ok = mbar_wait(img_ready, i & 1, abort_flag))) break;
                 tc_fence_after();
-                const uint32_t x0 = sbase + xtile(s, 0), x1 = sbase + xtile(s, 1);
-                const uint32_t acc = tmem + 128 * kAcc * s;
+                for (int t = 0; t < n_tiles; ++t, ++g) {
+                    const int s = g % kStages, u = g / kStages;
+                    const int a = g % kAccSets, ua = g / kAccSets;
+                    if (!(ok = mbar_wait(&x_full[s], u & 1, abort_flag))) break;
+                    if (ua >= 1 && !(ok = mbar_wait(&acc_free[a], (ua - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t x0 = sbase + xtile(s, 0), x1 = sbase + xtile(s, 1);
+                    const uint32_t acc = tmem + 128 * kAcc * a;
 #pragma unroll
-                for (int ks = 0; ks < 7; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
-                    const uint32_t w0 = sbase + kGOffImg + koff, w1 = sbase + kGOffImg + 2 * kImgBytes + koff;
-                    const uint64_t a0 = sdesc_sw128(x0 + koff, 16, 1024);
-                    mma_bf16(acc, a0, sdesc_sw128(w0, 16, 1024), kIdescK, ks > 0);
-                    mma_bf16(acc, a0, sdesc_sw128(w0 + kImgBytes, 16, 1024), kIdescK, 1u);
-                    if (kMode == 1) {
-                        const uint64_t a1 = sdesc_sw128(x1 + koff, 16, 1024);
-                        mma_bf16(acc + 128, a1, sdesc_sw128(w1, 16, 1024), kIdescK, ks > 0);
-                        mma_bf16(acc + 128, a1, sdesc_sw128(w1 + kImgBytes, 16, 1024), kIdescK, 1u);
-                        // k G^T: the G image as an MN-major B operand, 16 image rows (K) per step
-                        const uint32_t wm = sbase + kGOffImg + 2 * kImgBytes + ks * 2048;
-                        mma_bf16(acc + 256, a0, sdesc_sw128(wm, kImgPanel, 1024), kIdescKMN, ks > 0);
-                        mma_bf16(acc + 256, a0, sdesc_sw128(wm + kImgBytes, kImgPanel, 1024), kIdescKMN, 1u);
+                    for (int ks = 0; ks < 7; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                        const uint32_t w0 = sbase + kGOffImg + koff;
+                        const uint32_t w1 = sbase + kGOffImg + Sh::kImgPer * kImgBytes + koff;
+                        const uint64_t a0 = sdesc_sw128(x0 + koff, 16, 1024);
+                        mma_bf16(acc, a0, sdesc_sw128(w0, 16, 1024), kIdescK, ks > 0);
+                        if (Sh::kLo) mma_bf16(acc, a0, sdesc_sw128(w0 + kImgBytes, 16, 1024), kIdescK, 1u);
+                        if (kMode == 1) {
+                            const uint64_t a1 = sdesc_sw128(x1 + koff, 16, 1024);
+                            mma_bf16(acc + 128, a1, sdesc_sw128(w1, 16, 1024), kIdescK, ks > 0);
+                            if (Sh::kLo)
+                                mma_bf16(acc + 128, a1, sdesc_sw128(w1 + kImgBytes, 16, 1024), kIdescK, 1u);
+                            // k G^T: the G image as an MN-major B operand, 16 image rows (K) per step
+                            const uint32_t wm = sbase + kGOffImg + Sh::kImgPer * kImgBytes + ks * 2048;
+                            mma_bf16(acc + 256, a0, sdesc_sw128(wm, kImgPanel, 1024), kIdescKMN, ks > 0);
+                            if (Sh::kLo)
+                                mma_bf16(acc + 256, a0, sdesc_sw128(wm + kImgBytes, kImgPanel, 1024), kIdescKMN,
+                                         1u);
+                        }
                     }
+                    mma_commit(&acc_full[a]);
+                    mma_commit(&x_empty[s]);
                 }
-                mma_commit(&acc_full[s]);
-                mma_commit(&x_empty[s]);
+                mma_commit(img_free);  // the item's MMAs have read the images
             }
             mma_commit(drain);
             mbar_wait_drain(drain, 0);
         }
     } else if (warp < 6) {
-        // images: row j = column j of W (W0 then W1), hi + lo bf16; rows and
-        // columns 112..127 zero
+        // images: row j = column j of W (W0 then W1), bf16 hi (+ lo); rows and
+        // columns 112..127 zero.  Four groups of 32 matrix rows, every load of a
+        // group issued before the first conversion.  The next item's matrices are
+        // prefetched into L2 while this item's tiles run.
         const int j = (warp & 3) * 32 + lane;
-        for (int w = 0; w < (kMode == 1 ? 2 : 1); ++w) {
-            const float *W = w == 0 ? p.W0 + ((size_t)bh * p.F + f) * kStateFloats
-                                    : p.W1 + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kStateFloats;
-            uint8_t *img = sm + kGOffImg + w * 2 * kImgBytes;
-#pragma unroll 1
-            for (int c8 = 0; c8 < 16; ++c8) {
-                float x[8];
+        bool ok = true;
+        int i = 0;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++i) {
+            if (warp == 2 && lane < Sh::kMats && it + (int)gridDim.x < n_items)
+                bulk_prefetch_l2(mat(lane, it + gridDim.x), kStateBytes);
+            if (i >= 1 && !(ok = mbar_wait_warp(img_free, (i - 1) & 1, abort_flag))) break;
+            const float *Wm[Sh::kMats];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = c8 * 8 + e;
-                    x[e] = (j < kD && i < kD) ? W[i * kD + j] : 0.f;
+            for (int w = 0; w < Sh::kMats; ++w) Wm[w] = mat(w, it);
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                float x[Sh::kMats][32];
+#pragma unroll
+                for (int w = 0; w < Sh::kMats; ++w)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int r = g4 * 32 + e;
+                        x[w][e] = (j < kD && r < kD) ? __ldg(Wm[w] + r * kD + j) : 0.f;
+                    }
+#pragma unroll
+                for (int w = 0; w < Sh::kMats; ++w) {
+                    uint8_t *img = sm + kGOffImg + w * Sh::kImgPer * kImgBytes;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int c8 = g4 * 4 + c;
+                        const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(j, c8 & 7);
+                        if (Sh::kLo) {
+                            uint4 hi, lo;
+                            split_bf16x8(&x[w][8 * c], hi, lo);
+                            *reinterpret_cast<uint4 *>(img + off) = hi;
+                            *reinterpret_cast<uint4 *>(img + kImgBytes + off) = lo;
+                        } else {
+                            *reinterpret_cast<uint4 *>(img + off) = f32x8_to_bf16(&x[w][8 * c]);
+                        }
+                    }
                 }
-                uint4 hi, lo;
-                split_bf16x8(x, hi, lo);
-                const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(j, c8 & 7);
-                *reinterpret_cast<uint4 *>(img + off) = hi;
-                *reinterpret_cast<uint4 *>(img + kImgBytes + off) = lo;
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(img_ready);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(img_ready);
     } else {
         // output warps: thread = token row r of the tile
         const int quad = warp & 3, r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        bool ok = true;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % kStages, u = t / kStages;
-            // the row the normalisation applies to: q (x1) in mode 0, k (x0) in mode 1
-            const uint8_t *xr = sm + xtile(s, kMode == 0 ? 1 : 0);
-            if (ok) ok = mbar_wait_warp(&acc_full[s], u & 1, abort_flag);
-            tc_fence_after();
-            const int tok = t * 128 + r;
-            const bool live = ok && tok < p.N;
-            const size_t rowi = ((size_t)bf * p.N + tok) * p.H + h;
-            const uint32_t acc = tmem + 128 * kAcc * s + lane_off;
-            auto xrow = [&](int cc, float *o16) {  // 16 bf16 values of this thread's row, columns 16 cc..
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc) >> 3) * kImgPanel +
-                                                               sw128_off(r, (2 * cc) & 7)), o16);
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc + 1) >> 3) * kImgPanel +
-                                                               sw128_off(r, (2 * cc + 1) & 7)), o16 + 8);
-            };
-            if (kMode == 0) {
-                float sqq = 0.f, sqd = 0.f;
-#pragma unroll 1
-                for (int cc = 0; cc < 7; ++cc) {
-                    uint32_t ra[16];
-                    tmem_ld16(acc + cc * 16, ra);
-                    tmem_ld_wait();
-                    float xq[16];
-                    xrow(cc, xq);
+        uint8_t *stg = sm + kGOffStg + quad * 8192;  // two buffers: output 0 at +0, output 1 at +2048
+        int nst = 0;                                  // boxes staged by this warp
+        // this thread's row of a 32 x 16 fp32 box, 64-byte swizzle
+        auto put16 = [&](uint8_t *box, const float *v) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        sqq = fmaf(xq[e], xq[e], sqq);
-                        sqd = fmaf(xq[e], __uint_as_float(ra[e]), sqd);
-                    }
-                }
-                const float p2 = sqq + kEps, pinv = rsqrtf(p2), corr = sqd / p2;
-                float *dq = p.g0 + rowi * kD;
-#pragma unroll 1
-                for (int cc = 0; cc < 7; ++cc) {
-                    uint32_t ra[16];
-                    tmem_ld16(acc + cc * 16, ra);
-                    tmem_ld_wait();
-                    float xq[16];
-                    xrow(cc, xq);
-                    if (live) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dq + cc * 16);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float o[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                o[e] = pinv * (__uint_as_float(ra[4 * q4 + e]) - xq[4 * q4 + e] * corr);
-                            d4[q4] = make_float4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                }
-            } else {
-                float skk = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll 1
-                for (int cc = 0; cc < 7; ++cc) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(acc + cc * 16, r0);
-                    tmem_ld16(acc + 128 + cc * 16, r1);
-                    tmem_ld_wait();
-                    float xk[16];
-                    xrow(cc, xk);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        skk = fmaf(xk[e], xk[e], skk);
-                        s2 = fmaf(xk[e], __uint_as_float(r0[e]), s2);
-                        s3 = fmaf(xk[e], __uint_as_float(r1[e]), s3);
-                    }
-                }
-                const float r2 = skk + kEps, kh = p.c * rsqrtf(r2);   // c / r
-                const float bt = live ? __ldg(p.beta + rowi) : 0.f;
-                const float kdk = bt * (kh * s2 + s3);                 // k . dk^
-                if (live) p.g_beta[rowi] = 0.5f * kh * kh * s2 + kh * s3;
-                float *dk = p.g0 + rowi * kD, *dv = p.g1 + rowi * kD;
-#pragma unroll 1
-                for (int cc = 0; cc < 7; ++cc) {
-                    uint32_t r0[16], r1[16], r2v[16];
-                    tmem_ld16(acc + cc * 16, r0);
-                    tmem_ld16(acc + 128 + cc * 16, r1);
-                    tmem_ld16(acc + 256 + cc * 16, r2v);
-                    tmem_ld_wait();
-                    float xk[16];
-                    xrow(cc, xk);
-                    if (live) {
-                        float4 *k4 = reinterpret_cast<float4 *>(dk + cc * 16);
-                        float4 *v4 = reinterpret_cast<float4 *>(dv + cc * 16);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float ok4[4], ov4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int i = 4 * q4 + e;
-                                const float dkh = bt * (kh * __uint_as_float(r0[i]) + __uint_as_float(r1[i]));
-                                ok4[e] = kh * (dkh - xk[i] * kdk / r2);
-                                ov4[e] = bt * kh * __uint_as_float(r2v[i]);
-                            }
-                            k4[q4] = make_float4(ok4[0], ok4[1], ok4[2], ok4[3]);
-                            v4[q4] = make_float4(ov4[0], ov4[1], ov4[2], ov4[3]);
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<float4 *>(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        };
+        auto stage_begin = [&]() -> uint8_t * {  // the buffer used two boxes ago has been read by its store
+            if (lane == 0) bulk_wait_read_le1();
             __syncwarp();
-            if (ok && lane == 0) {
-                mbar_arrive(&acc_free[s]);
-                mbar_arrive(&x_empty[s]);
+            return stg + (nst & 1) * 4096;
+        };
+        bool ok = true;
+        int g = 0;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const int f = it / BH, bh = it % BH;
+            const int b = bh / p.H, h = bh % p.H, bf = b * p.F + f;
+            for (int t = 0; t < n_tiles; ++t, ++g) {
+                const int s = g % kStages;
+                const int a = g % kAccSets, ua = g / kAccSets;
+                // the row the normalisation applies to: q (x1) in mode 0, k (x0) in mode 1
+                const uint8_t *xr = sm + xtile(s, kMode == 0 ? 1 : 0);
+                if (ok) ok = mbar_wait_warp(&acc_full[a], ua & 1, abort_flag);
+                tc_fence_after();
+                const int tok = t * 128 + r;
+                const bool live = ok && tok < p.N;
+                const bool wlive = ok && t * 128 + quad * 32 < p.N;  // any row of this warp in range
+                const size_t rowi = ((size_t)bf * p.N + tok) * p.H + h;
+                const uint32_t acc = tmem + 128 * kAcc * a + lane_off;
+                auto xrow = [&](int cc, float *o16) {  // 16 bf16 values of this thread's row, columns 16 cc..
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc) >> 3) * kImgPanel +
+                                                                   sw128_off(r, (2 * cc) & 7)), o16);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + ((2 * cc + 1) >> 3) * kImgPanel +
+                                                                   sw128_off(r, (2 * cc + 1) & 7)), o16 + 8);
+                };
+                auto stage_end = [&](uint8_t *box, int cc) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&mapG0, box, cc * 16, h, t * 128 + quad * 32, bf);
+                        if (kMode == 1) tma_store_4d(&mapG1, box + 2048, cc * 16, h, t * 128 + quad * 32, bf);
+                        bulk_commit();
+                    }
+                    ++nst;
+                };
+                if (kMode == 0) {
+                    // the whole accumulator row in registers: TMEM is free before the stores
+                    uint32_t ra[7][16];
+#pragma unroll
+                    for (int cc = 0; cc < 7; ++cc) tmem_ld16(acc + cc * 16, ra[cc]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (ok && lane == 0) mbar_arrive(&acc_free[a]);
+                    float sqq = 0.f, sqd = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < 7; ++cc) {
+                        float xq[16];
+                        xrow(cc, xq);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            sqq = fmaf(xq[e], xq[e], sqq);
+                            sqd = fmaf(xq[e], __uint_as_float(ra[cc][e]), sqd);
+                        }
+                    }
+                    const float p2 = sqq + kEps, pinv = rsqrtf(p2), corr = sqd / p2;
+                    float *dq = p.g0 + rowi * kD;
+#pragma unroll
+                    for (int cc = 0; cc < 7; ++cc) {
+                        float xq[16];
+                        xrow(cc, xq);
+                        float *o = reinterpret_cast<float *>(ra[cc]);  // dq over its accumulator row
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = pinv * (__uint_as_float(ra[cc][e]) - xq[e] * corr);
+                        if (GDN_BWD_TMA_ST) {
+                            if (wlive) {
+                                uint8_t *box = stage_begin();
+                                put16(box, o);
+                                stage_end(box, cc);
+                            }
+                        } else if (live) {
+                            float4 *d4 = reinterpret_cast<float4 *>(dq + cc * 16);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                d4[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+                        }
+                    }
+                    __syncwarp();
+                    if (ok && lane == 0) mbar_arrive(&x_empty[s]);
+                } else {
+                    // two 16-column chunks per TMEM wait; chunk 7 (columns 112..127) is loaded and ignored
+                    float skk = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 1
+                    for (int cc = 0; cc < 7; cc += 2) {
+                        uint32_t r0[2][16], r1[2][16];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            tmem_ld16(acc + (cc + q) * 16, r0[q]);
+                            tmem_ld16(acc + 128 + (cc + q) * 16, r1[q]);
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            if (cc + q >= 7) break;
+                            float xk[16];
+                            xrow(cc + q, xk);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                skk = fmaf(xk[e], xk[e], skk);
+                                s2 = fmaf(xk[e], __uint_as_float(r0[q][e]), s2);
+                                s3 = fmaf(xk[e], __uint_as_float(r1[q][e]), s3);
+                            }
+                        }
+                    }
+                    const float r2 = skk + kEps, kh = p.c * rsqrtf(r2);  // c / r
+                    const float bt = live ? __ldg(p.beta + rowi) : 0.f;
+                    const float kdk = bt * (kh * s2 + s3);                // k . dk^
+                    const float kc = kdk / r2, btkh = bt * kh;
+                    if (live) p.g_beta[rowi] = 0.5f * kh * kh * s2 + kh * s3;
+                    float *dk = p.g0 + rowi * kD, *dv = p.g1 + rowi * kD;
+#pragma unroll 1
+                    for (int cc = 0; cc < 7; cc += 2) {
+                        uint32_t r0[2][16], r1[2][16], r2v[2][16];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            tmem_ld16(acc + (cc + q) * 16, r0[q]);
+                            tmem_ld16(acc + 128 + (cc + q) * 16, r1[q]);
+                            tmem_ld16(acc + 256 + (cc + q) * 16, r2v[q]);
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            if (cc + q >= 7) break;
+                            float xk[16], okv[16], ovv[16];
+                            xrow(cc + q, xk);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float dkh =
+                                    bt * fmaf(kh, __uint_as_float(r0[q][e]), __uint_as_float(r1[q][e]));
+                                okv[e] = kh * fmaf(-xk[e], kc, dkh);
+                                ovv[e] = btkh * __uint_as_float(r2v[q][e]);
+                            }
+                            if (GDN_BWD_TMA_ST) {
+                                if (wlive) {
+                                    uint8_t *box = stage_begin();
+                                    put16(box, okv);
+                                    put16(box + 2048, ovv);
+                                    stage_end(box, cc + q);
+                                }
+                            } else if (live) {
+                                float4 *k4 = reinterpret_cast<float4 *>(dk + (cc + q) * 16);
+                                float4 *v4 = reinterpret_cast<float4 *>(dv + (cc + q) * 16);
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    k4[q4] = make_float4(okv[4 * q4], okv[4 * q4 + 1], okv[4 * q4 + 2],
+                                                         okv[4 * q4 + 3]);
+                                    v4[q4] = make_float4(ovv[4 * q4], ovv[4 * q4 + 1], ovv[4 * q4 + 2],
+                                                         ovv[4 * q4 + 3]);
+                                }
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (ok && lane == 0) {
+                        mbar_arrive(&acc_free[a]);
+                        mbar_arrive(&x_empty[s]);
+                    }
+                }
             }
         }
+        if (lane == 0) bulk_wait_all();  // the staged boxes have been read and written
     }
     tc_fence_before();
     __syncthreads();
@@ -462,9 +594,11 @@ cudaError_t token_grads(const void *dO, const void *q, const void *k, const void
                         const float *Sst, const float *Dsym, const float *Gst, float *dq, float *dk, float *dv,
                         float *dbeta, int B, int H, int F, int N, float c, unsigned *status, cudaStream_t stream)
 {
-    CUtensorMap mdo, mq, mk, mv;
+    CUtensorMap mdo, mq, mk, mv, mdq, mdk, mdv;
     if (!make_token_map(&mdo, dO, B, H, F, N, 128) || !make_token_map(&mq, q, B, H, F, N, 128) ||
-        !make_token_map(&mk, k, B, H, F, N, 128) || !make_token_map(&mv, v, B, H, F, N, 128))
+        !make_token_map(&mk, k, B, H, F, N, 128) || !make_token_map(&mv, v, B, H, F, N, 128) ||
+        !make_f32_row_map(&mdq, dq, B, H, F, N, 32) || !make_f32_row_map(&mdk, dk, B, H, F, N, 32) ||
+        !make_f32_row_map(&mdv, dv, B, H, F, N, 32))
         return cudaErrorInvalidValue;
     TokGradParams p;
     p.beta = beta;
@@ -479,7 +613,8 @@ cudaError_t token_grads(const void *dO, const void *q, const void *k, const void
     p.g0 = dq;
     p.g1 = nullptr;
     p.g_beta = nullptr;
-    kg_token_grad_kernel<0><<<B * H * F, kGThreads, kGSmem, stream>>>(mdo, mq, p);
+    const int grid = B * H * F < kSms ? B * H * F : kSms;  // persistent: items strided over the CTAs
+    kg_token_grad_kernel<0><<<grid, kGThreads, kGSmem, stream>>>(mdo, mq, mdq, mdq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.W0 = Dsym;
@@ -487,7 +622,7 @@ cudaError_t token_grads(const void *dO, const void *q, const void *k, const void
     p.g0 = dk;
     p.g1 = dv;
     p.g_beta = dbeta;
-    kg_token_grad_kernel<1><<<B * H * F, kGThreads, kGSmem, stream>>>(mk, mv, p);
+    kg_token_grad_kernel<1><<<grid, kGThreads, kGSmem, stream>>>(mk, mv, mdk, mdv, p);
     return cudaGetLastError();
 }
 }  // namespace

@@ -26,6 +26,9 @@ bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N
 // 2-D view of a bf16 row-major [rows][cols] matrix, 128-byte swizzle, boxes of
 // 64 columns x `box_rows` rows (gdn_tc.cu).
 bool make_matrix_map(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
+// Same 4-D view of an fp32 token tensor for TMA stores, 64-byte swizzle, boxes
+// of 16 head-dim elements x `rows` tokens (gdn_tc.cu).
+bool make_f32_row_map(CUtensorMap *m, void *base, int B, int H, int F, int N, int rows);
 
 // Block projections (gdn_proj.cu), tcgen05 GEMMs C = A W^T with bf16 A [M][K]
 // and W [N][K]: the plain form (C bf16 [M][N]) and the input projection of the

@@ -984,6 +984,23 @@ bool make_token_map(CUtensorMap *m, const void *base, int B, int H, int F, int N
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D view [B*F][N][H][D] of an fp32 [B][F*N][H][D] tensor for TMA stores:
+// 64-byte swizzle, boxes of 16 head-dim elements x `rows` tokens of one head
+// of one frame (the smem box is `rows` rows of 64 bytes, 16-byte chunk c of
+// row r at chunk position c ^ ((r >> 1) & 3)).
+bool make_f32_row_map(CUtensorMap *m, void *base, int B, int H, int F, int N, int rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B * F};
+    cuuint64_t strides[3] = {(cuuint64_t)kD * 4, (cuuint64_t)H * kD * 4, (cuuint64_t)N * H * kD * 4};
+    cuuint32_t box[4] = {16, 1, (cuuint32_t)rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D view of a bf16 row-major [rows][cols] matrix, 128B swizzle, boxes of
 // 64 columns (one swizzled 128-byte row) x `box_rows` rows.  cols must be a
 // multiple of 8 (16-byte row stride); out-of-range elements load as zero.
