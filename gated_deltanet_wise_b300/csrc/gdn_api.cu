@@ -80,7 +80,8 @@ const char *gdn_status_string(gdn_status_t s)
 static size_t fwd_workspace_size(int B, int H, int F, int N, int D, unsigned flags)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return (size_t)-1;
-    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE)) return (size_t)-1;
+    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE | GDN_FWD_FUSED)) return (size_t)-1;
+    if ((flags & GDN_FWD_PRODUCT) && (flags & GDN_FWD_FUSED)) return (size_t)-1;
     if (B == 0 || H == 0 || F == 0 || N == 0) return 0;
     if (D != 112) return (size_t)-1;
     TcPlan plan;
@@ -107,9 +108,10 @@ static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, 
                                    int withhold_loads = 0)
 {
     if (B < 0 || H < 0 || F < 0 || N < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE)) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(GDN_FWD_PRODUCT | GDN_FWD_REVERSE | GDN_FWD_FUSED)) return GDN_ERR_INVALID_ARG;
     if (B == 0 || H == 0) return GDN_OK;
     if (D != 112) return GDN_ERR_UNSUPPORTED;
+    if ((flags & GDN_FWD_PRODUCT) && (flags & GDN_FWD_FUSED)) return GDN_ERR_UNSUPPORTED;
     if ((S_in && !aligned(S_in, 16)) || (S_out && !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (F == 0 || N == 0) {  // no tokens: every reading and direction gives S_out = (prod gamma) S_in
@@ -132,6 +134,12 @@ static gdn_status_t frame_fwd_impl(const void *q, const void *k, const void *v, 
     if (!status) return GDN_ERR_CUDA;
     plan.withhold_loads = withhold_loads;
     const float c = default_key_scale(key_scale, D, N);
+    if (flags & GDN_FWD_FUSED) {
+        const cudaError_t ef =
+            launch_frame_fwd_fused_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse, workspace, status, st);
+        if (ef != cudaErrorCooperativeLaunchTooLarge) return ef == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+        (void)cudaGetLastError();  // too many CTAs to be resident at once: the three-launch path
+    }
     cudaError_t e = product ? launch_frame_fwd_product_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse,
                                                           workspace, status, st)
                             : launch_frame_fwd_tc(q, k, v, beta, gamma, S_in, S_out, o, plan, c, reverse, workspace,

@@ -43,10 +43,11 @@ cudaError_t launch_in_proj_tc(const void *x, const void *W_in, void *q, void *k,
 // tensor-core path (gdn_tc.cu); D == 112.
 struct TcPlan {
     int B, H, F, N;
-    int chunk;       // frames per chunk (K1 / K2 work unit)
+    int chunk;       // frames of the longest chunk (K1 / K2 work unit; chunk_frames gives each range)
     int n_chunks;    // chunks per chain
     size_t ws_bytes; // total workspace
     size_t off_frames, off_comp, off_start;  // workspace sections
+    size_t off_flags;                         // chunk-hop flags of the fused chained scan
     // Failure-detection test only: the frame-statistics kernel issues no loads,
     // so its first bounded wait expires and the status word records a timeout.
     int withhold_loads = 0;
@@ -65,6 +66,12 @@ cudaError_t launch_fwd_resume_tc(const void *q, const float *gamma, const float 
 // S_out = S C + H per chain (S may be null: zero), fp32.
 cudaError_t launch_state_compose_tc(const float *S, const float *C, const float *H, float *S_out, int BH,
                                     unsigned *status, cudaStream_t stream);
+// The fused chained scan: the forward in one cooperative launch (statistics,
+// chunk-boundary hops and scan); cudaErrorCooperativeLaunchTooLarge (nothing
+// launched) when the plan's CTAs cannot all be resident.
+cudaError_t launch_frame_fwd_fused_tc(const void *q, const void *k, const void *v, const float *beta,
+                                      const float *gamma, const float *S_in, float *S_out, void *o, const TcPlan &plan,
+                                      float c, int reverse, void *workspace, unsigned *status, cudaStream_t stream);
 // reverse = 1 visits the frames from the last to the first (reverse-direction scan).
 cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, const float *beta, const float *gamma,
                                 const float *S_in, float *S_out, void *o, const TcPlan &plan, float c, int reverse,

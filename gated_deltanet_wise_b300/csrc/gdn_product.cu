@@ -686,8 +686,8 @@ __global__ void __launch_bounds__(kCThreads, 1) kc_chunk_composite_kernel(const 
     const int BH = p.B * p.H;
     const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
     const int b = bh / p.H, h = bh % p.H;
-    const int f_begin = chunk_idx * p.chunk;
-    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+    int f_begin, nf;
+    chunk_frames(chunk_idx, p.F, p.n_chunks, f_begin, nf);
 
     if (threadIdx.x == 0) {
         mbar_init(a_full, 1);

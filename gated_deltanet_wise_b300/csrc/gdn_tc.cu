@@ -93,7 +93,11 @@ constexpr int kK2SBuf = GDN_K2_SBUF;                  // S image sets (2: the ne
                                                       // written while the previous frame's outputs run)
 static_assert(kK2QStages >= 2 && kK2QStages <= 4 && kK2OStages >= 0 && kK2OStages <= 2, "K2 rings");
 static_assert(kK2SBuf == 1 || kK2SBuf == 2, "K2 S image sets");
-constexpr int kK2Threads = 320;                       // producers, MMA, 4 state warps, 4 output warps
+#ifndef GDN_K2_SW8
+#define GDN_K2_SW8 0
+#endif
+constexpr int kK2StateWarps = GDN_K2_SW8 ? 8 : 4;     // 8: every state row split over two warps
+constexpr int kK2Threads = kK2StateWarps == 8 ? 448 : 320;  // producers, MMA, state warps, 4 output warps
 constexpr uint32_t kK2OffO = kK2QStages * kImgBytes;       // output staging tiles
 constexpr uint32_t kK2OffA = kK2OffO + kK2OStages * kImgBytes;
 constexpr uint32_t kK2SetBytes = (kK2Lo ? 2 : 1) * kImgBytes;  // one S image set: hi [, lo]
@@ -126,12 +130,14 @@ struct K1Params {
 //   [384,512) T_H: chunk input composite H (state reached from zero)
 constexpr uint32_t kTmAccA = 0, kTmAccU = 128, kTmC = 256, kTmH = 384, kTmImgC = 0, kTmImgH = 56;
 
-__global__ void __launch_bounds__(kK1Threads, 1)
-    k1_frame_stats_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                          const K1Params p)
+// The kernel body, shared by the standalone launch and the fused chained scan.
+// With kKeepTmem the CTA's 512 TMEM columns stay allocated on return (the chunk
+// composites C and H still in them) and their address is returned; *aborted
+// receives the role abort flag.
+template <bool kKeepTmem>
+__device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUtensorMap &mapV, const K1Params &p,
+                                            uint8_t *sm, int *aborted)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK1OffBar);
     uint64_t *st_full = bars + 0, *st_prep = bars + kK1Stages, *st_empty = bars + 2 * kK1Stages;
     uint64_t *acc_full = bars + 3 * kK1Stages, *comp_ready = acc_full + 1, *comp_done = acc_full + 2;
@@ -143,8 +149,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const int BH = p.B * p.H;
     const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
     const int b = bh / p.H, h = bh % p.H;
-    const int f_begin = chunk_idx * p.chunk;
-    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+    int f_begin, nf;
+    chunk_frames(chunk_idx, p.F, p.n_chunks, f_begin, nf);
     const int n_st = (p.N + kTS - 1) / kTS;
 
     if (threadIdx.x == 0) {
@@ -473,11 +479,23 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    *aborted = *abort_flag;
     if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
-    if (warp == 1) {
+    if (!kKeepTmem && warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    return tmem;
+}
+
+__global__ void __launch_bounds__(kK1Threads, 1)
+    k1_frame_stats_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                          const K1Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int aborted;
+    k1_body<false>(mapK, mapV, p, sm, &aborted);
 }
 
 // ===================================================================== K1b
@@ -588,16 +606,145 @@ struct K2Params {
     int states_only;  // 1: no outputs (the state chain alone)
 };
 
+// K2's state role over columns [kC0, kC0 + kCols) of every row: thread = row
+// of S (fp32 registers), one warp per TMEM lane quadrant.  The standalone
+// kernel runs it on four warps with all 112 columns; the fused chained scan,
+// whose 448 threads allow 128 registers each, on eight warps with 56 columns.
+// As soon as S_f's images are written, S <- gamma_f S + U_f (U_f read from
+// global memory, where it was prefetched into L2 a frame ahead, quad-major: a
+// warp's lanes read 512 contiguous bytes), overlapping the S A_f GEMM; when
+// that lands, S <- S - S_f A_f.
+template <int kCols, int kC0>
+__device__ __forceinline__ void k2_state_role(const K2Params &p, uint8_t *sm, uint32_t tmem, uint64_t *s_ready,
+                                              uint64_t *accS_full, uint64_t *o_done, volatile int *abort_flag,
+                                              int bh, int b, int h, int chunk_idx, int f_begin, int nf,
+                                              const uint8_t *ws_chain)
+{
+    static_assert(kCols % 8 == 0 && kC0 % 8 == 0 && kC0 + kCols <= kD, "state column range");
+    constexpr int kCh = kCols / 8;                 // 8-column chunks
+    constexpr int kCs = kC0 & ~15, kSkip = kC0 - kCs;
+    constexpr int kNld = (kSkip + kCols + 15) / 16;  // 16-column TMEM loads covering the range
+    const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3, row = quad * 32 + lane;
+    const int urow = row < kD ? row : 0;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    float S[kCols];
+    const float *s0 = p.ws_start + ((size_t)bh * p.n_chunks + chunk_idx) * kStateFloats;
+#pragma unroll
+    for (int j = 0; j < kCols; j += 4) {
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < kD) v4 = __ldcg(reinterpret_cast<const float4 *>(s0 + row * kD + kC0 + j));  // L2: may come from
+                                                                                                // another CTA
+        S[j] = v4.x;
+        S[j + 1] = v4.y;
+        S[j + 2] = v4.z;
+        S[j + 3] = v4.w;
+    }
+    auto write_images = [&](int set) {
+        if (row < kD) {
+            const uint32_t sset = (uint32_t)set * kK2SetBytes;
+#pragma unroll
+            for (int c8 = 0; c8 < kCh; ++c8) {
+                const int g8 = kC0 / 8 + c8;
+                const uint32_t off = sset + (g8 >> 3) * kImgPanel + sw128_off(row, g8 & 7);
+                if (kK2Lo) {
+                    uint4 hi, lo;
+                    split_bf16x8(S + 8 * c8, hi, lo);
+                    *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + kK2OffSlo + off) = lo;
+                } else {
+                    *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = f32x8_to_bf16(S + 8 * c8);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_ready);
+    };
+    write_images(0);
+    const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
+    float g_next = __ldg(gam + (size_t)frame_at(f_begin, p.F, p.reverse) * p.H);
+    for (int it = 0; it < nf; ++it) {
+        const float g = g_next;
+        if (it + 1 < nf) g_next = __ldg(gam + (size_t)frame_at(f_begin + it + 1, p.F, p.reverse) * p.H);
+        const float4 *U4 = reinterpret_cast<const float4 *>(ws_chain + (size_t)it * kFrameWs + kAimgBytes) + urow;
+        constexpr int kW = 4;  // 8-column chunks of U_f loaded ahead of their use
+        float4 ub[kW][2];
+#pragma unroll
+        for (int c = 0; c < kW && c < kCh; ++c)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ub[c][j] = __ldg(U4 + (kC0 / 4 + 2 * c + j) * kD);
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float4 u4 = ub[c % kW][j];
+                const int k0 = c * 8 + 4 * j;
+                S[k0] = fmaf(g, S[k0], u4.x);
+                S[k0 + 1] = fmaf(g, S[k0 + 1], u4.y);
+                S[k0 + 2] = fmaf(g, S[k0 + 2], u4.z);
+                S[k0 + 3] = fmaf(g, S[k0 + 3], u4.w);
+            }
+            if (c + kW < kCh)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) ub[c % kW][j] = __ldg(U4 + (kC0 / 4 + 2 * (c + kW) + j) * kD);
+        }
+        if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cp = 0; cp < kNld; cp += 2) {  // two 16-column chunks per TMEM round trip
+            uint32_t ra2[2][16];
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < kNld; ++hf)
+                tmem_ld16(tmem + lane_off + kCs + (cp + hf) * 16, ra2[hf]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hf = 0; hf < 2 && cp + hf < kNld; ++hf)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int k = (cp + hf) * 16 + j - kSkip;
+                    if (k >= 0 && k < kCols) S[k] -= __uint_as_float(ra2[hf][j]);
+                }
+        }
+        tc_fence_before();
+        if (p.states && row < kD) {
+            float4 *dst = reinterpret_cast<float4 *>(p.states + ((size_t)bh * p.F + f_begin + it) * kStateFloats +
+                                                     row * kD + kC0);
+#pragma unroll
+            for (int j = 0; j < kCols / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        }
+        // S_it goes into image set (it + 1) % kK2SBuf, which MMA iteration it + 1 - kK2SBuf
+        // read last: with one set, wait for this iteration's outputs (frame it - 1); with
+        // two, for the previous iteration's (frame it - 2), whose images are the other set.
+        {
+            // MMA iteration j commits o_done[j % kK2SBuf], whose phase (j - 1) / kK2SBuf it completes;
+            // the next commit there (iteration j + kK2SBuf = it + 1) needs this iteration's images,
+            // so the phase waited for is always the latest one of that barrier.
+            const int j = it + 1 - kK2SBuf;
+            if (j >= 1 && !mbar_wait_warp(&o_done[j % kK2SBuf], ((j - 1) / kK2SBuf) & 1, abort_flag)) break;
+        }
+        write_images((it + 1) % kK2SBuf);
+    }
+    if (p.S_out && chunk_idx + 1 == p.n_chunks && row < kD) {
+        float *dst = p.S_out + (size_t)bh * kStateFloats + row * kD + kC0;
+#pragma unroll
+        for (int j = 0; j < kCols; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+}
+
 // Named barrier over K2's four output warps (id 0 is __syncthreads).
 __device__ __forceinline__ void out_warps_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kK2Threads, 1)
-    k2_scan_output_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO,
-                          const K2Params p)
+// The kernel body, shared by the standalone launch (kStateWarps = 4, TMEM
+// allocated here) and the fused chained scan (kStateWarps = 8: warps 10..13 take
+// the second half of every state row; tmem_given = the fused kernel's TMEM).
+template <int kStateWarps>
+__device__ __forceinline__ void k2_body(const CUtensorMap &mapQ, const CUtensorMap &mapO, const K2Params &p,
+                                        uint8_t *sm, uint8_t *bar_area, bool own_tmem, uint32_t tmem_given)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kK2OffBar);
+    static_assert(kStateWarps == 4 || kStateWarps == 8, "K2 state warps");
+    uint64_t *bars = reinterpret_cast<uint64_t *>(bar_area);
     uint64_t *q_full = bars + 0, *q_empty = bars + kK2QStages;
     uint64_t *a_full = bars + 2 * kK2QStages, *a_empty = a_full + 1;
     // o_done[m]: the MMAs of iteration j (outputs of frame j - 1) have completed, for j % kK2SBuf == m
@@ -610,8 +757,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     const int BH = p.B * p.H;
     const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
     const int b = bh / p.H, h = bh % p.H;
-    const int f_begin = chunk_idx * p.chunk;
-    const int nf = min(p.F, f_begin + p.chunk) - f_begin;
+    int f_begin, nf;
+    chunk_frames(chunk_idx, p.F, p.n_chunks, f_begin, nf);
     const int n_tiles = p.states_only ? 0 : (p.N + kTQ - 1) / kTQ;
 
     if (threadIdx.x == 0) {
@@ -622,7 +769,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         mbar_init(drain, 1);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
-        mbar_init(s_ready, 4);
+        mbar_init(s_ready, kStateWarps);
         mbar_init(accS_full, 1);
         for (int i = 0; i < kK2SBuf; ++i) mbar_init(&o_done[i], 1);
         for (int i = 0; i < 3; ++i) {
@@ -632,18 +779,18 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (own_tmem && warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
     // zero the S images (rows 112..127 and key columns 112..127 stay zero)
-    for (int o = threadIdx.x * 16; o < kK2SBuf * (int)kK2SetBytes; o += kK2Threads * 16)
+    for (int o = threadIdx.x * 16; o < kK2SBuf * (int)kK2SetBytes; o += blockDim.x * 16)
         *reinterpret_cast<uint4 *>(sm + kK2OffShi + o) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = own_tmem ? *tmem_slot : tmem_given;
     const uint32_t sbase = smem_u32(sm);
     griddep_launch_dependents();
     griddep_wait();
@@ -739,111 +886,16 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         }
     } else if (warp < 6) {
         // ------------------------------------------------- state warps (rows)
-        // Thread = row of S, held in fp32 registers.  As soon as S_f's images
-        // are written, S <- gamma_f S + U_f (U_f read from global memory, where
-        // it was prefetched into L2 a frame ahead, quad-major: a warp's lanes
-        // read 512 contiguous bytes), overlapping the S A_f GEMM; when that
-        // lands, S <- S - S_f A_f.
-        const int quad = warp & 3, row = quad * 32 + lane;
-        const int urow = row < kD ? row : 0;
-        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        float S[kD];
-        const float *s0 = p.ws_start + ((size_t)bh * p.n_chunks + chunk_idx) * kStateFloats;
-#pragma unroll
-        for (int j = 0; j < kD; j += 4) {
-            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (row < kD) v4 = *reinterpret_cast<const float4 *>(s0 + row * kD + j);
-            S[j] = v4.x;
-            S[j + 1] = v4.y;
-            S[j + 2] = v4.z;
-            S[j + 3] = v4.w;
-        }
-        auto write_images = [&](int set) {
-            if (row < kD) {
-                const uint32_t sset = (uint32_t)set * kK2SetBytes;
-#pragma unroll
-                for (int c8 = 0; c8 < kD / 8; ++c8) {
-                    const uint32_t off = sset + (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
-                    if (kK2Lo) {
-                        uint4 hi, lo;
-                        split_bf16x8(S + 8 * c8, hi, lo);
-                        *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = hi;
-                        *reinterpret_cast<uint4 *>(sm + kK2OffSlo + off) = lo;
-                    } else {
-                        *reinterpret_cast<uint4 *>(sm + kK2OffShi + off) = f32x8_to_bf16(S + 8 * c8);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_ready);
-        };
-        write_images(0);
-        const float *gam = p.gamma + (size_t)b * p.F * p.H + h;
-        float g_next = __ldg(gam + (size_t)frame_at(f_begin, p.F, p.reverse) * p.H);
-        for (int it = 0; it < nf; ++it) {
-            const float g = g_next;
-            if (it + 1 < nf) g_next = __ldg(gam + (size_t)frame_at(f_begin + it + 1, p.F, p.reverse) * p.H);
-            const float4 *U4 = reinterpret_cast<const float4 *>(ws_chain + (size_t)it * kFrameWs + kAimgBytes) + urow;
-            float4 ub[2][4];  // 16-column chunks of U_f, loaded two ahead of their use
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) ub[c][j] = __ldg(U4 + (c * 4 + j) * kD);
-#pragma unroll
-            for (int cc = 0; cc < 7; ++cc) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 u4 = ub[cc & 1][j];
-                    const int c0 = cc * 16 + 4 * j;
-                    S[c0] = fmaf(g, S[c0], u4.x);
-                    S[c0 + 1] = fmaf(g, S[c0 + 1], u4.y);
-                    S[c0 + 2] = fmaf(g, S[c0 + 2], u4.z);
-                    S[c0 + 3] = fmaf(g, S[c0 + 3], u4.w);
-                }
-                if (cc + 2 < 7)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) ub[cc & 1][j] = __ldg(U4 + ((cc + 2) * 4 + j) * kD);
-            }
-            if (!mbar_wait_warp(accS_full, it & 1, abort_flag)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int cp = 0; cp < 7; cp += 2) {  // two 16-column chunks per TMEM round trip
-                uint32_t ra2[2][16];
-#pragma unroll
-                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) tmem_ld16(tmem + lane_off + (cp + hf) * 16, ra2[hf]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf)
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) S[(cp + hf) * 16 + j] -= __uint_as_float(ra2[hf][j]);
-            }
-            tc_fence_before();
-            if (p.states && row < kD) {
-                float4 *dst = reinterpret_cast<float4 *>(p.states + ((size_t)bh * p.F + f_begin + it) * kStateFloats +
-                                                         row * kD);
-#pragma unroll
-                for (int j = 0; j < kD / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-            }
-            // S_it goes into image set (it + 1) % kK2SBuf, which MMA iteration it + 1 - kK2SBuf
-            // read last: with one set, wait for this iteration's outputs (frame it - 1); with
-            // two, for the previous iteration's (frame it - 2), whose images are the other set.
-            {
-                // MMA iteration j commits o_done[j % kK2SBuf], whose phase (j - 1) / kK2SBuf it completes;
-                // the next commit there (iteration j + kK2SBuf = it + 1) needs this iteration's images,
-                // so the phase waited for is always the latest one of that barrier.
-                const int j = it + 1 - kK2SBuf;
-                if (j >= 1 && !mbar_wait_warp(&o_done[j % kK2SBuf], ((j - 1) / kK2SBuf) & 1, abort_flag)) break;
-            }
-            write_images((it + 1) % kK2SBuf);
-        }
-        if (p.S_out && chunk_idx + 1 == p.n_chunks && row < kD) {
-            float *dst = p.S_out + (size_t)bh * kStateFloats + row * kD;
-#pragma unroll
-            for (int j = 0; j < kD; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        }
+        if (kStateWarps == 4)
+            k2_state_role<kD, 0>(p, sm, tmem, s_ready, accS_full, o_done, abort_flag, bh, b, h, chunk_idx, f_begin, nf,
+                                 ws_chain);
+        else
+            k2_state_role<kD / 2, 0>(p, sm, tmem, s_ready, accS_full, o_done, abort_flag, bh, b, h, chunk_idx,
+                                     f_begin, nf, ws_chain);
+    } else if (warp >= 10) {
+        if (kStateWarps == 8)
+            k2_state_role<kD / 2, kD / 2>(p, sm, tmem, s_ready, accS_full, o_done, abort_flag, bh, b, h, chunk_idx,
+                                          f_begin, nf, ws_chain);
     } else {
         // ------------------------------------------------ output warps (tokens)
         // Each warp owns 32 token rows of a tile.  It computes their 1/||q||
@@ -942,7 +994,223 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
-    if (warp == 1) {
+    if (own_tmem && warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+__global__ void __launch_bounds__(kK2Threads, 1)
+    k2_scan_output_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO,
+                          const K2Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    k2_body<kK2StateWarps>(mapQ, mapO, p, sm, sm + kK2OffBar, true, 0u);
+}
+
+// ===================================================================== K5
+// Fused chained scan: K1, the chunk-boundary step and K2 in one cooperative
+// launch, one CTA per (chunk, chain), all CTAs resident at once.  After its
+// frame statistics the CTA still holds its chunk composites C_c and H_c in
+// TMEM; it waits for the chunk's start state S_start(c) (published by the
+// CTA of chunk c-1; S_in for chunk 0), forms S_start(c+1) = H_c + S_start(c) C_c
+// on tcgen05 in place of H_c (S and C as bf16 hi + lo, three MMAs per k-step),
+// publishes it with a release flag and runs its own scan and outputs from
+// S_start(c).  The chain of start states is the decoupled look-back of the
+// chunk aggregates (C_p, H_p composites of the summary page, section
+// 技术新颖性), with one hop per chunk instead of a separate launch; every flag
+// wait is bounded and sets the timeout status when it runs out.
+constexpr uint32_t kK5OffHopS = 0;                     // S_start images: hi, lo (K-major A, row = state row)
+constexpr uint32_t kK5OffHopC = 2 * kImgBytes;         // C_c images: hi, lo (MN-major B, row = k index)
+constexpr uint32_t kK5OffK2Bar = kK1OffBar + 256;      // K2's barriers (K1's stay at kK1OffBar)
+constexpr uint32_t kK5OffHopBar = kK1OffBar + 512;     // hop: MMA barrier + state word
+constexpr uint32_t kK5Smem = kK1OffBar + 768 + 1024;
+constexpr uint32_t kIdescKMN5 = idesc_bf16(128, kD, false, true);  // A K-major, B MN-major
+static_assert(kK5OffHopC + 2 * kImgBytes <= kK2OffBar && kK5Smem <= kMaxSmem, "K5 shared memory");
+
+// Warps 10..13 (the statistics epilogue warps: TMEM lane quadrant = warp & 3).
+__device__ __forceinline__ void hop_warps_sync() { asm volatile("bar.sync 5, 128;" ::: "memory"); }
+
+// Returns (to every thread) whether the CTA may run its scan: false after a
+// timeout here or in the statistics phase.
+__device__ __forceinline__ bool k5_chunk_hop(const K1Params &p1, const K2Params &p2, const float *S_in,
+                                             unsigned *flags, uint8_t *sm, uint32_t tmem, int aborted)
+{
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kK5OffHopBar);
+    volatile int *hop_abort = reinterpret_cast<volatile int *>(bar + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p1.B * p1.H, nch = p1.n_chunks;
+    const int chunk_idx = blockIdx.x / BH, bh = blockIdx.x % BH;
+    const bool need_next = chunk_idx + 1 < nch;
+    float *ws_start = const_cast<float *>(p2.ws_start);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *hop_abort = aborted ? 1 : 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp >= 10 && !*hop_abort) {
+        const int quad = warp & 3, row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        // C_c -> bf16 hi/lo images, row = row of C (rows 112.. are zero in TMEM), columns 112..127 zero
+        if (need_next) {
+#pragma unroll
+            for (int cp = 0; cp < 7; cp += 2) {
+                uint32_t rc2[2][16];
+#pragma unroll
+                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) tmem_ld16(tmem + lane_off + kTmC + (cp + hf) * 16, rc2[hf]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int hf = 0; hf < 2 && cp + hf < 7; ++hf)
+#pragma unroll
+                    for (int e8 = 0; e8 < 2; ++e8) {
+                        const int c8 = 2 * (cp + hf) + e8;
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(rc2[hf][8 * e8 + e]);
+                        uint4 hi, lo;
+                        split_bf16x8(x, hi, lo);
+                        const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(row, c8 & 7);
+                        *reinterpret_cast<uint4 *>(sm + kK5OffHopC + off) = hi;
+                        *reinterpret_cast<uint4 *>(sm + kK5OffHopC + kImgBytes + off) = lo;
+                    }
+            }
+#pragma unroll
+            for (int c8 = 14; c8 < 16; ++c8) {
+                const uint32_t off = kImgPanel + sw128_off(row, c8 & 7);
+                *reinterpret_cast<uint4 *>(sm + kK5OffHopC + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(sm + kK5OffHopC + kImgBytes + off) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        // the chunk's start state: S_in for chunk 0, else published by chunk c-1
+        if (chunk_idx > 0 && warp == 10 && lane == 0) {
+            const unsigned *fl = flags + (size_t)bh * nch + chunk_idx;
+            const long long t0 = clock64();
+            while (ld_acquire_u32(fl) == 0) {
+                if (clock64() - t0 > kSpinLimitCycles) {
+                    *hop_abort = 1;
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+    }
+    // every thread loads a part of S_start (one L2 round trip) into the S images;
+    // chunk 0 also leaves its copy of S_in where the scan reads its start state
+    __syncthreads();
+    if (!*hop_abort && (chunk_idx == 0 || need_next)) {
+        const float *src = chunk_idx == 0 ? (S_in ? S_in + (size_t)bh * kStateFloats : nullptr)
+                                          : ws_start + ((size_t)bh * nch + chunk_idx) * kStateFloats;
+        float *own = ws_start + ((size_t)bh * nch + chunk_idx) * kStateFloats;
+        constexpr int kItems = 128 * 16;  // (row, 8-column group) of the 128 x 128 images
+        constexpr int kPer = (kItems + kK1Threads - 1) / kK1Threads;
+        float x[kPer][8];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = threadIdx.x + u * kK1Threads, r = e >> 4, c8 = e & 15;
+            if (e < kItems && src && r < kD && c8 < 14) {
+                const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src + r * kD + 8 * c8));
+                const float4 b4 = __ldcg(reinterpret_cast<const float4 *>(src + r * kD + 8 * c8 + 4));
+                x[u][0] = a4.x; x[u][1] = a4.y; x[u][2] = a4.z; x[u][3] = a4.w;
+                x[u][4] = b4.x; x[u][5] = b4.y; x[u][6] = b4.z; x[u][7] = b4.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[u][i] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = threadIdx.x + u * kK1Threads, r = e >> 4, c8 = e & 15;
+            if (e >= kItems) continue;
+            if (chunk_idx == 0 && r < kD && c8 < 14) {
+                *reinterpret_cast<float4 *>(own + r * kD + 8 * c8) = make_float4(x[u][0], x[u][1], x[u][2], x[u][3]);
+                *reinterpret_cast<float4 *>(own + r * kD + 8 * c8 + 4) =
+                    make_float4(x[u][4], x[u][5], x[u][6], x[u][7]);
+            }
+            if (need_next) {
+                uint4 hi, lo;
+                split_bf16x8(x[u], hi, lo);
+                const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7);
+                *reinterpret_cast<uint4 *>(sm + kK5OffHopS + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + kK5OffHopS + kImgBytes + off) = lo;
+            }
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp >= 10) {
+        const int quad = warp & 3, row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        if (need_next && !*hop_abort) {
+            if (warp == 10 && lane == 0) {
+                tc_fence_after();
+                const uint32_t sbase = smem_u32(sm);
+#pragma unroll
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint32_t koff = (ks >> 2) * kImgPanel + (ks & 3) * 32;
+                    const uint64_t a_hi = sdesc_sw128(sbase + kK5OffHopS + koff, 16, 1024);
+                    const uint64_t a_lo = sdesc_sw128(sbase + kK5OffHopS + kImgBytes + koff, 16, 1024);
+                    const uint64_t b_hi = sdesc_sw128(sbase + kK5OffHopC + ks * 2048, kImgPanel, 1024);
+                    const uint64_t b_lo = sdesc_sw128(sbase + kK5OffHopC + kImgBytes + ks * 2048, kImgPanel, 1024);
+                    mma_bf16(tmem + kTmH, a_hi, b_hi, kIdescKMN5, 1u);
+                    mma_bf16(tmem + kTmH, a_lo, b_hi, kIdescKMN5, 1u);
+                    mma_bf16(tmem + kTmH, a_hi, b_lo, kIdescKMN5, 1u);
+                }
+                mma_commit(bar);
+            }
+            if (mbar_wait_warp(bar, 0, hop_abort)) {
+                tc_fence_after();
+                float *dst = ws_start + ((size_t)bh * nch + chunk_idx + 1) * kStateFloats;
+#pragma unroll
+                for (int cp = 0; cp < 7; cp += 4) {
+                    uint32_t rh4[4][16];
+#pragma unroll
+                    for (int hf = 0; hf < 4 && cp + hf < 7; ++hf)
+                        tmem_ld16(tmem + lane_off + kTmH + (cp + hf) * 16, rh4[hf]);
+                    tmem_ld_wait();
+                    if (row < kD)
+#pragma unroll
+                        for (int hf = 0; hf < 4 && cp + hf < 7; ++hf)
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4 *>(dst + row * kD + (cp + hf) * 16 + j) =
+                                    make_float4(__uint_as_float(rh4[hf][j]), __uint_as_float(rh4[hf][j + 1]),
+                                                __uint_as_float(rh4[hf][j + 2]), __uint_as_float(rh4[hf][j + 3]));
+                }
+                __threadfence();
+                tc_fence_before();
+                hop_warps_sync();
+                if (warp == 10 && lane == 0) st_release_u32(flags + (size_t)bh * nch + chunk_idx + 1, 1u);
+            } else if (warp == 10 && lane == 0) {
+                // let the hop's MMAs land before the CTA moves on
+                mbar_wait_drain(bar, 0);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool ok = *hop_abort == 0;
+    if (!ok && threadIdx.x == 0 && !aborted) raise_status(p1.status);
+    return ok;
+}
+
+__global__ void __launch_bounds__(kK1Threads, 1)
+    k5_fused_scan_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                         const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO,
+                         const K1Params p1, const K2Params p2, const float *S_in, unsigned *flags)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int aborted = 0;
+    const uint32_t tmem = k1_body<true>(mapK, mapV, p1, sm, &aborted);
+    if (k5_chunk_hop(p1, p2, S_in, flags, sm, tmem, aborted))
+        k2_body<8>(mapQ, mapO, p2, sm, sm + kK5OffK2Bar, false, tmem);
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1049,7 +1317,8 @@ bool tc_plan(int B, int H, int F, int N, int force_chunks, TcPlan *plan)
     plan->off_frames = 0;
     plan->off_comp = align_up((size_t)BH * F * kFrameWs, 256);
     plan->off_start = align_up(plan->off_comp + (size_t)BH * plan->n_chunks * 2 * kStateBytes, 256);
-    plan->ws_bytes = align_up(plan->off_start + (size_t)BH * plan->n_chunks * kStateBytes, 256);
+    plan->off_flags = align_up(plan->off_start + (size_t)BH * plan->n_chunks * kStateBytes, 256);
+    plan->ws_bytes = align_up(plan->off_flags + (size_t)BH * plan->n_chunks * sizeof(unsigned), 256);
     return true;
 }
 
@@ -1090,6 +1359,8 @@ cudaError_t prepare_tc_kernels()
     e = cudaFuncSetAttribute(k2_scan_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK2Smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k1b_chunk_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1bSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k5_fused_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK5Smem);
     if (e != cudaSuccess) return e;
     g_tc_attrs[dev] = true;
     return cudaSuccess;
@@ -1278,6 +1549,63 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     return launch_scan_output_tc(q, gamma, S_in, S_out, o, pl, reverse, ws, status, stream, events);
+}
+
+// The fused chained scan (K5) in one cooperative launch.  Every CTA must be
+// resident at once (the chunk hops wait on one another): when the plan's
+// chunk x chain count exceeds the device's SMs, cudaErrorCooperativeLaunchTooLarge
+// comes back and nothing is launched.  The hop flags are cleared on the stream
+// first.
+cudaError_t launch_frame_fwd_fused_tc(const void *q, const void *k, const void *v, const float *beta,
+                                      const float *gamma, const float *S_in, float *S_out, void *o, const TcPlan &pl,
+                                      float c, int reverse, void *workspace, unsigned *status, cudaStream_t stream)
+{
+    CUtensorMap mk, mv, mq, mo;
+    if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS) ||
+        !make_token_map(&mq, q, pl.B, pl.H, pl.F, pl.N, kTQ) || !make_token_map(&mo, o, pl.B, pl.H, pl.F, pl.N, kTQ))
+        return cudaErrorInvalidValue;
+    cudaError_t e = prepare_tc_kernels();
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k5_fused_scan_kernel, kK1Threads, kK5Smem)) !=
+        cudaSuccess)
+        return e;
+    const int grid = pl.B * pl.H * pl.n_chunks;
+    if ((long long)grid > (long long)sms * per_sm) return cudaErrorCooperativeLaunchTooLarge;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    unsigned *flags = reinterpret_cast<unsigned *>(ws + pl.off_flags);
+    if ((e = cudaMemsetAsync(flags, 0, (size_t)pl.B * pl.H * pl.n_chunks * sizeof(unsigned), stream)) != cudaSuccess)
+        return e;
+    const K1Params p1 = k1_params(beta, gamma, pl, c, reverse, ws, status);
+    K2Params p2;
+    p2.o = o;
+    p2.gamma = gamma;
+    p2.ws_frames = ws + pl.off_frames;
+    p2.ws_start = reinterpret_cast<const float *>(ws + pl.off_start);
+    p2.S_out = S_out;
+    p2.states = nullptr;
+    p2.states_only = 0;
+    p2.status = status;
+    p2.B = pl.B;
+    p2.H = pl.H;
+    p2.F = pl.F;
+    p2.N = pl.N;
+    p2.chunk = pl.chunk;
+    p2.n_chunks = pl.n_chunks;
+    p2.reverse = reverse;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kK1Threads);
+    cfg.dynamicSmemBytes = kK5Smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k5_fused_scan_kernel, mk, mv, mq, mo, p1, p2, S_in, flags);
 }
 
 // Token-ordered reading: per-frame transitions from the UT-transform kernel

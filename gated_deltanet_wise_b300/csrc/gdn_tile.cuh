@@ -35,6 +35,17 @@ constexpr uint32_t kIdescK = idesc_bf16(128, kD, false, false);   // D-contracti
 // to the first.  Per-frame workspace slots are indexed by processing position.
 __host__ __device__ __forceinline__ int frame_at(int p, int F, int reverse) { return reverse ? F - 1 - p : p; }
 
+// Frames [f_begin, f_begin + nf) of chunk c when F frames are cut into n chunks
+// as evenly as possible, the longer chunks first (lengths differ by at most one):
+// chunks that start their scan later, after more boundary steps, get no more
+// frames than earlier ones.
+__host__ __device__ __forceinline__ void chunk_frames(int c, int F, int n, int &f_begin, int &nf)
+{
+    const int base = F / n, rem = F % n;
+    nf = base + (c < rem ? 1 : 0);
+    f_begin = c * base + (c < rem ? c : rem);
+}
+
 __device__ __forceinline__ void raise_status(unsigned *status)
 {
     if (status) atomicOr(status, kStatusTimeout);

@@ -41,6 +41,7 @@ EXPORTED = [
 
 GDN_FWD_PRODUCT = 1
 GDN_FWD_REVERSE = 2
+GDN_FWD_FUSED = 4
 
 _lib = None
 
@@ -363,8 +364,10 @@ def frame_fwd_product(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0
 
 
 def frame_fwd_ex(q, k, v, beta, gamma, S_in=None, *, product: bool = False, reverse: bool = False,
-                 key_scale: float = 0.0, o=None, S_out=None, workspace: Optional[Workspace] = None, stream=None):
-    """gdn_frame_fwd_ex: the sum or product reading, forward or reverse frame order."""
+                 fused: bool = False, key_scale: float = 0.0, o=None, S_out=None,
+                 workspace: Optional[Workspace] = None, stream=None):
+    """gdn_frame_fwd_ex: the sum or product reading, forward or reverse frame order, the sum
+    reading optionally as the fused chained-scan launch."""
     B, H, F, N, D = _shape(q, gamma)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, torch.bfloat16, n)
@@ -372,7 +375,8 @@ def frame_fwd_ex(q, k, v, beta, gamma, S_in=None, *, product: bool = False, reve
     _check(gamma, torch.float32, "gamma")
     if S_in is not None:
         _check(S_in, torch.float32, "S_in")
-    flags = (GDN_FWD_PRODUCT if product else 0) | (GDN_FWD_REVERSE if reverse else 0)
+    flags = (GDN_FWD_PRODUCT if product else 0) | (GDN_FWD_REVERSE if reverse else 0) | \
+        (GDN_FWD_FUSED if fused else 0)
     o = torch.empty_like(q) if o is None else o
     S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=q.device) if S_out is None else S_out
     nbytes = gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags)

@@ -135,6 +135,17 @@ gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v,
  *     This equals gdn_frame_fwd on the frame-reversed sequence with its
  *     outputs put back in frame order.  How the two directions' outputs are
  *     combined is not stated on the pages and is left to the caller.
+ *   GDN_FWD_FUSED - the sum reading as one fused chained-scan launch
+ *     (statistics, chunk-boundary states and scan/output in one cooperative
+ *     grid, one CTA per (frame chunk, chain); each chunk's CTA forms the next
+ *     chunk's start state from its own composites, S_start(c+1) =
+ *     S_start(c) C_c + H_c, the C_p / H_p prefix of the summary page, section
+ *     技术新颖性, and passes it on through a flag in the workspace).  Same
+ *     results as the three-launch path up to fp32 rounding of the start states
+ *     (bf16 hi + lo products instead of fp32 FMAs).  When the chunks x chains
+ *     cannot all be resident at once it runs the three-launch path instead.
+ *     With GDN_FWD_PRODUCT: GDN_ERR_UNSUPPORTED ((size_t)-1 from the size
+ *     query).
  * flags == 0 is gdn_frame_fwd.  Unknown bits return GDN_ERR_INVALID_ARG (and
  * (size_t)-1 from the size query).  Arguments, layouts, ownership and the
  * other status codes are those of gdn_frame_fwd; the workspace must hold
@@ -142,6 +153,7 @@ gdn_status_t gdn_frame_fwd_product(const void *q, const void *k, const void *v,
  */
 #define GDN_FWD_PRODUCT 1u
 #define GDN_FWD_REVERSE 2u
+#define GDN_FWD_FUSED 4u
 size_t gdn_frame_fwd_ex_workspace_size(int B, int H, int F, int N, int D, unsigned flags);
 gdn_status_t gdn_frame_fwd_ex(const void *q, const void *k, const void *v,
                               const float *beta, const float *gamma,

@@ -31,7 +31,9 @@ int main(void)
           ws + (size_t)20 * 121 * 14 * 8192);
     CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_PRODUCT) ==
           gdn_frame_fwd_product_workspace_size(1, 20, 121, 880, 112));
-    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 4u) == err);
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_FUSED) == ws);
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, GDN_FWD_FUSED | GDN_FWD_PRODUCT) == err);
+    CHECK(gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 8u) == err);
     CHECK(gdn_frame_fwd_workspace_size(1, 1, 2, 8, 64) == err);
     CHECK(gdn_frame_step_workspace_size(1, 20, 880, 112) == 0);
     CHECK(gdn_frame_bwd_workspace_size(1, 20, 121, 880, 112) != err);

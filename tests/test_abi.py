@@ -59,7 +59,11 @@ def test_workspace_sizes(L):
         gdn.gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112)
     assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, gdn.GDN_FWD_PRODUCT) == \
         gdn.gdn_frame_fwd_product_workspace_size(1, 20, 121, 880, 112)
-    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 4) == SZ_ERR
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, gdn.GDN_FWD_FUSED) == \
+        gdn.gdn_frame_fwd_workspace_size(1, 20, 121, 880, 112)
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, gdn.GDN_FWD_FUSED | gdn.GDN_FWD_PRODUCT) == \
+        SZ_ERR
+    assert gdn.gdn_frame_fwd_ex_workspace_size(1, 20, 121, 880, 112, 8) == SZ_ERR
     # the workspace grows linearly in frames (per-frame images dominate)
     a = gdn.gdn_frame_fwd_workspace_size(1, 4, 10, 880, 112)
     b = gdn.gdn_frame_fwd_workspace_size(1, 4, 20, 880, 112)
@@ -88,9 +92,13 @@ def test_host_side_validation_without_gpu(L):
     need = gdn.gdn_frame_fwd_workspace_size(1, 1, 2, 8, 112)
     assert fwd(1, 1, 2, 8, 112, ws=fake, nbytes=need - 16) == gdn.GDN_ERR_WORKSPACE
     a = args
-    for flags in (4, 8, 0x80000000):
+    for flags in (8, 16, 0x80000000):
         assert L.gdn_frame_fwd_ex(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"],
                                   1, 1, 2, 8, 112, 0.0, flags, fake, need, None) == gdn.GDN_ERR_INVALID_ARG
+    # the fused chained scan is the sum reading only
+    assert L.gdn_frame_fwd_ex(a["q"], a["k"], a["v"], a["beta"], a["gamma"], a["S_in"], a["S_out"], a["o"],
+                              1, 1, 2, 8, 112, 0.0, gdn.GDN_FWD_FUSED | gdn.GDN_FWD_PRODUCT, fake, need,
+                              None) == gdn.GDN_ERR_UNSUPPORTED
     assert fwd(1, 1, 2, 8, 112, ws=P(0x10008), nbytes=need) == gdn.GDN_ERR_INVALID_ARG
     def step(B, H, N, D, **over):
         a = dict(args, **over)

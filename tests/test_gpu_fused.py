@@ -1,0 +1,86 @@
+"""The fused chained scan (gdn_frame_fwd_ex with GDN_FWD_FUSED) on the GPU.
+
+One cooperative launch computes the frame statistics, hands each chunk's start
+state to the next chunk's CTA (S_start(c+1) = S_start(c) C_c + H_c, formed on
+tcgen05 from bf16 hi + lo splits) and runs the scan and outputs.  It must
+match the fp64 oracle within the bf16 path's 5e-3 relative Frobenius error on
+every chain, agree with the three-launch path to within the rounding of the
+start states, be deterministic, and fall back to the three-launch path when
+the chunks x chains cannot all be resident at once."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_wise_b300 import gdn
+from gated_deltanet_wise_b300.inputs import make_inputs, make_workload
+from tests.conftest import check_every_chain, rel_fro
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    gdn.lib()
+    yield
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def _fused(x, **kw):
+    o, S = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, fused=True, **kw)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    return o, S
+
+
+@pytest.mark.parametrize("B,H,F,N,s0", [(1, 1, 1, 1, 0.1), (2, 3, 5, 15, 0.1), (1, 2, 9, 65, 0.1),
+                                        (2, 1, 3, 130, 0.0), (1, 3, 4, 200, 0.1), (1, 1, 40, 16, 0.1)])
+def test_fused_ragged_shapes_match_oracle(B, H, F, N, s0):
+    """Several chunks per chain (each hop exercised), token tails, with and without S_0."""
+    x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=11 * F + N, device=DEV, s0_std=s0)
+    o, S = _fused(x)
+    o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_fro(S.cpu().numpy(), S_ref) <= TOL
+
+
+def test_fused_layer_every_chain_and_three_launch_agreement():
+    """B=1, H=20, D=112, F=121, N=880: all 20 chains against the oracle; against the
+    three-launch path the only difference is the start states' products (bf16
+    hi + lo on tcgen05 instead of fp32 FMAs)."""
+    x = make_workload("layer_60s_720p", device=DEV)
+    o, S = _fused(x)
+    w = check_every_chain(x, o, S, lambda *a: oracle.frame_fwd(*a), TOL)
+    print(f"fused layer: worst chain rel_fro {w:.3e}")
+    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    torch.cuda.synchronize()
+    d_o = rel_fro(o.float().cpu().numpy(), o3.float().cpu().numpy().astype(np.float64))
+    d_s = rel_fro(S.cpu().numpy(), S3.cpu().numpy().astype(np.float64))
+    print(f"fused vs three launches: o {d_o:.2e}, S {d_s:.2e}")
+    assert d_o < 1e-3 and d_s < 1e-4
+
+
+def test_fused_is_deterministic_and_reverse_matches_oracle():
+    x = make_inputs(1, 4, 30, 200, 112, dtype="bf16", seed=5, device=DEV, s0_std=0.1)
+    o1, S1 = _fused(x)
+    o2, S2 = _fused(x)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    o, S = _fused(x, reverse=True)
+    o3, S3 = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, reverse=True)
+    torch.cuda.synchronize()
+    assert rel_fro(o.float().cpu().numpy(), o3.float().cpu().numpy().astype(np.float64)) < 1e-3
+    assert rel_fro(S.cpu().numpy(), S3.cpu().numpy().astype(np.float64)) < 1e-4
+
+
+def test_fused_falls_back_when_not_all_resident():
+    """160 chains: one chunk each, 160 CTAs > 148 SMs, so the three-launch path runs
+    (bit-identical to gdn_frame_fwd)."""
+    x = make_inputs(1, 160, 2, 64, 112, dtype="bf16", seed=3, device=DEV, s0_std=0.1)
+    o, S = _fused(x)
+    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o3) and torch.equal(S, S3)
