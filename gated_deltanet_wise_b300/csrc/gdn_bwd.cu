@@ -21,7 +21,7 @@
 //      its chunk composites (K1c), the chunk-boundary kernel and the scan
 //      kernel without outputs, from dS_out, visit G_{F-1}, ..., G_0 and end at
 //      dS_in.
-//   4. kb_frame_grad: dM_f = S_{f-1}^T G_f (fp32 CUDA cores), dgamma_f, and
+//   4. kb_frame_grad_tc: dM_f = S_{f-1}^T G_f (tcgen05, hi + lo bf16), dgamma_f, and
 //      Dsym_f = dA_f + dA_f^T.
 //   5. kg_token_grad_kernel (tcgen05), twice: dO S_f, with q's normalisation
 //      Jacobian in the epilogue, gives dq; k Dsym_f, v G_f and k G_f^T (one G
@@ -65,67 +65,216 @@ __global__ void kb_build_reverse_ws(const uint8_t *ws_fwd, const uint8_t *ws_E, 
         gamma_G[((size_t)b * (F + 1) + p) * H + h] = p >= 1 ? gamma[((size_t)b * F + (F - p)) * H + h] : 1.f;
 }
 
-// dM = S_{f-1}^T G_f, dgamma_f = trace(dM), Dsym_f = -(dM + dM^T).  One block of
-// 256 threads per (chain, frame); thread (ty, tx) owns the 7 x 7 block of rows
-// 7 ty.., columns 7 tx...
-constexpr uint32_t kFgSmem = 2 * (uint32_t)kStateBytes + 16;
-__global__ void __launch_bounds__(256) kb_frame_grad(const float *S_in, const float *Sst, const float *Gst,
-                                                     float *dgamma, float *Dsym, int B, int H, int F)
+// dM_f = S_{f-1}^T G_f, dgamma_f = trace(dM_f), Dsym_f = -(dM_f + dM_f^T), on
+// tcgen05.  Persistent: one CTA per SM walks (frame, chain) items.  With
+// m = i, n = j, k = l, dM[i][j] = sum_l S[l][i] G[l][j] takes both operands
+// MN-major, so the images are plain row-major copies of S_{f-1} and G_f (image
+// row l = matrix row l), each as bf16 hi + lo; three MMAs per 16-row k-step
+// (S_hi G_hi + S_lo G_hi + S_hi G_lo) keep the product near fp32.  Warps:
+// 1 issues the MMAs, 2..5 build the images (the next item's matrices are
+// prefetched into L2 first), 6..9 read dM out of TMEM (two accumulator sets,
+// so the next item's MMAs run meanwhile) into a padded fp32 tile in shared
+// memory, from which the trace and the symmetrised Dsym are written with
+// coalesced stores.
+constexpr int kFgThreads = 320;
+constexpr uint32_t kFgDMStride = kD + 1;  // odd row stride: row writes and column reads are conflict-free
+constexpr uint32_t kFgOffDM = 4 * kImgBytes;
+constexpr uint32_t kFgOffBar = kFgOffDM + ((kD * kFgDMStride * 4 + 1023) / 1024) * 1024;
+constexpr uint32_t kFgSmem = kFgOffBar + 256 + 1024;
+static_assert(kFgSmem <= kMaxSmem, "frame-gradient kernel shared memory");
+
+struct FrameGradParams {
+    const float *S_in;  // [BH] states or null (zero)
+    const float *Sst;   // S_f after every frame, [BH][F]
+    const float *Gst;   // G_f, [BH][F+1] (G_f at slot F-1-f)
+    float *dgamma;      // [B][F][H]
+    float *Dsym;        // [BH][F]
+    unsigned *status;
+    int B, H, F;
+};
+
+// Epilogue warps 6..9 (id 0 is __syncthreads).
+__device__ __forceinline__ void fg_epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGradParams p)
 {
-    extern __shared__ __align__(16) float fg_smem[];
-    float *Sp = fg_smem, *Gf = fg_smem + kStateFloats;
-    float *tr = fg_smem + 2 * kStateFloats;
-    const int bh = blockIdx.x, f = blockIdx.y;
-    const int b = bh / H, h = bh % H;
-    const float *sp = f == 0 ? (S_in ? S_in + (size_t)bh * kStateFloats : nullptr)
-                             : Sst + ((size_t)bh * F + f - 1) * kStateFloats;
-    const float *gf = Gst + ((size_t)bh * (F + 1) + (F - 1 - f)) * kStateFloats;
-    for (int e = threadIdx.x; e < (int)kStateFloats / 4; e += 256) {
-        reinterpret_cast<float4 *>(Sp)[e] = sp ? reinterpret_cast<const float4 *>(sp)[e] : make_float4(0, 0, 0, 0);
-        reinterpret_cast<float4 *>(Gf)[e] = reinterpret_cast<const float4 *>(gf)[e];
-    }
-    if (threadIdx.x == 0) *tr = 0.f;
-    __syncthreads();
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-    const int i0 = ty * 7, j0 = tx * 7;
-    float acc[7][7];
-#pragma unroll
-    for (int a = 0; a < 7; ++a)
-#pragma unroll
-        for (int c = 0; c < 7; ++c) acc[a][c] = 0.f;
-    for (int l = 0; l < kD; ++l) {
-        float sv[7], gv[7];
-#pragma unroll
-        for (int a = 0; a < 7; ++a) {
-            sv[a] = Sp[l * kD + i0 + a];
-            gv[a] = Gf[l * kD + j0 + a];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *dM = reinterpret_cast<float *>(sm + kFgOffDM);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kFgOffBar);
+    uint64_t *acc_full = bars + 0, *acc_free = bars + 2, *img_ready = bars + 4, *img_free = bars + 5;
+    uint64_t *drain = bars + 6;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 7);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = p.B * p.H;
+    const int n_items = BH * p.F;  // item = (frame f, chain bh), f major
+    // the item's two matrices: S_{f-1} (null: zero) and G_f
+    auto mat = [&](int w, int it) -> const float * {
+        const int f = it / BH, bh = it % BH;
+        if (w == 1) return p.Gst + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kStateFloats;
+        if (f == 0) return p.S_in ? p.S_in + (size_t)bh * kStateFloats : nullptr;
+        return p.Sst + ((size_t)bh * p.F + f - 1) * kStateFloats;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_free[i], 4);
         }
-#pragma unroll
-        for (int a = 0; a < 7; ++a)
-#pragma unroll
-            for (int c = 0; c < 7; ++c) acc[a][c] = fmaf(sv[a], gv[c], acc[a][c]);
+        mbar_init(img_ready, 4);
+        mbar_init(img_free, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
     }
-    __syncthreads();  // Sp is reused for dM
-#pragma unroll
-    for (int a = 0; a < 7; ++a)
-#pragma unroll
-        for (int c = 0; c < 7; ++c) Sp[(i0 + a) * kD + j0 + c] = acc[a][c];
-    if (ty == tx) {
-        float d = 0.f;
-#pragma unroll
-        for (int a = 0; a < 7; ++a) d += acc[a][a];
-        atomicAdd(tr, d);
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
     }
+    tc_fence_before();
     __syncthreads();
-    float *ds = Dsym + ((size_t)bh * F + f) * kStateFloats;
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            int i = 0;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++i) {
+                const int a = i & 1, ua = i >> 1;
+                if (!(ok = mbar_wait(img_ready, i & 1, abort_flag))) break;
+                if (ua >= 1 && !(ok = mbar_wait(&acc_free[a], (ua - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + 128 * a;
 #pragma unroll
-    for (int a = 0; a < 7; ++a)
-#pragma unroll
-        for (int c = 0; c < 7; ++c) {
-            const int i = i0 + a, j = j0 + c;
-            ds[i * kD + j] = -(Sp[i * kD + j] + Sp[j * kD + i]);
+                for (int ks = 0; ks < 7; ++ks) {
+                    const uint32_t o = ks * 2048;  // image rows 16 ks .. 16 ks + 15 (k = l)
+                    const uint64_t s_hi = sdesc_sw128(sbase + o, kImgPanel, 1024);
+                    const uint64_t s_lo = sdesc_sw128(sbase + kImgBytes + o, kImgPanel, 1024);
+                    const uint64_t g_hi = sdesc_sw128(sbase + 2 * kImgBytes + o, kImgPanel, 1024);
+                    const uint64_t g_lo = sdesc_sw128(sbase + 3 * kImgBytes + o, kImgPanel, 1024);
+                    mma_bf16(acc, s_hi, g_hi, kIdescMN, ks > 0);
+                    mma_bf16(acc, s_lo, g_hi, kIdescMN, 1u);
+                    mma_bf16(acc, s_hi, g_lo, kIdescMN, 1u);
+                }
+                mma_commit(&acc_full[a]);
+                mma_commit(img_free);  // the images may be rebuilt once these MMAs have read them
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
         }
-    if (threadIdx.x == 0) dgamma[((size_t)b * F + f) * H + h] = *tr;
+    } else if (warp >= 2 && warp < 6) {
+        // images: thread = matrix row l (0..127; rows 112.. and columns 112.. zero)
+        const int l = (warp - 2) * 32 + lane;
+        bool ok = true;
+        int i = 0;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++i) {
+            if (warp == 2 && lane < 2 && it + (int)gridDim.x < n_items) {
+                const float *nxt = mat(lane, it + gridDim.x);
+                if (nxt) bulk_prefetch_l2(nxt, kStateBytes);
+            }
+            if (i >= 1 && !(ok = mbar_wait_warp(img_free, (i - 1) & 1, abort_flag))) break;
+            const float *W[2] = {mat(0, it), mat(1, it)};
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {  // 8-column groups 7 half .. 7 half + 6, both matrices in flight
+                float x[2][7][8];
+#pragma unroll
+                for (int w = 0; w < 2; ++w)
+#pragma unroll
+                    for (int g = 0; g < 7; ++g) {
+                        const int c8 = 7 * half + g;
+                        if (W[w] && l < kD) {
+                            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(W[w] + l * kD + 8 * c8));
+                            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(W[w] + l * kD + 8 * c8 + 4));
+                            x[w][g][0] = a4.x; x[w][g][1] = a4.y; x[w][g][2] = a4.z; x[w][g][3] = a4.w;
+                            x[w][g][4] = b4.x; x[w][g][5] = b4.y; x[w][g][6] = b4.z; x[w][g][7] = b4.w;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[w][g][e] = 0.f;
+                        }
+                    }
+#pragma unroll
+                for (int w = 0; w < 2; ++w)
+#pragma unroll
+                    for (int g = 0; g < 7; ++g) {
+                        const int c8 = 7 * half + g;
+                        const uint32_t off = (c8 >> 3) * kImgPanel + sw128_off(l, c8 & 7);
+                        uint4 hi, lo;
+                        split_bf16x8(x[w][g], hi, lo);
+                        *reinterpret_cast<uint4 *>(sm + 2 * w * kImgBytes + off) = hi;
+                        *reinterpret_cast<uint4 *>(sm + (2 * w + 1) * kImgBytes + off) = lo;
+                    }
+            }
+#pragma unroll
+            for (int c8 = 14; c8 < 16; ++c8) {
+                const uint32_t off = kImgPanel + sw128_off(l, c8 & 7);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4 *>(sm + m * kImgBytes + off) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(img_ready);
+        }
+    } else if (warp >= 6) {
+        // epilogue: thread = row i of dM
+        const int quad = warp & 3, row = quad * 32 + lane, t = threadIdx.x - 192;  // t: 0..127
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        // every warp runs every item and both named barriers; after a timeout the
+        // work is skipped (the abort flag makes the other warps' waits return)
+        bool ok = true;
+        int i = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++i) {
+            const int a = i & 1, ua = i >> 1;
+            const int f = it / BH, bh = it % BH, b = bh / p.H, h = bh % p.H;
+            if (ok) ok = mbar_wait_warp(&acc_full[a], ua & 1, abort_flag);
+            tc_fence_after();
+            if (ok) {
+#pragma unroll
+                for (int cp = 0; cp < 7; cp += 4) {
+                    uint32_t r4[4][16];
+#pragma unroll
+                    for (int hf = 0; hf < 4 && cp + hf < 7; ++hf)
+                        tmem_ld16(tmem + 128 * a + lane_off + (cp + hf) * 16, r4[hf]);
+                    tmem_ld_wait();
+                    if (row < kD)
+#pragma unroll
+                        for (int hf = 0; hf < 4 && cp + hf < 7; ++hf)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                dM[row * kFgDMStride + (cp + hf) * 16 + j] = __uint_as_float(r4[hf][j]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&acc_free[a]);
+            fg_epi_sync();  // dM complete in shared memory
+            if (ok && !*abort_flag) {
+                if (warp == 6) {
+                    float d = 0.f;
+                    for (int r = lane; r < kD; r += 32) d += dM[r * kFgDMStride + r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                    if (lane == 0) p.dgamma[((size_t)b * p.F + f) * p.H + h] = d;
+                }
+                float *ds = p.Dsym + ((size_t)bh * p.F + f) * kStateFloats;
+                for (int e = t; e < (int)kStateFloats; e += 128) {
+                    const int r = e / kD, c = e - r * kD;
+                    ds[e] = -(dM[r * kFgDMStride + c] + dM[c * kFgDMStride + r]);
+                }
+            }
+            fg_epi_sync();  // dM may be overwritten by the next item
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) raise_status(p.status);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
 }
 
 // ------------------------------------------------ token-row gradient kernels
@@ -583,7 +732,7 @@ cudaError_t prepare_bwd_kernels()
     if ((e = cudaFuncSetAttribute(kg_token_grad_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kGSmem)) != cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(kb_frame_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFgSmem)) !=
+    if ((e = cudaFuncSetAttribute(kb_frame_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFgSmem)) !=
         cudaSuccess)
         return e;
     g_b_attr[dev] = true;
@@ -669,7 +818,20 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     if ((e = launch_states_tc(q, gamma_G, dS_out, dS_in, Gst, L.plan_G, ws + L.ws_G, status, stream)) != cudaSuccess)
         return e;
     // 4. per-frame dgamma and Dsym = dA + dA^T
-    kb_frame_grad<<<dim3(BH, F), 256, kFgSmem, stream>>>(S_in, Sst, Gst, dgamma, Dsym, B, H, F);
+    {
+        FrameGradParams fp;
+        fp.S_in = S_in;
+        fp.Sst = Sst;
+        fp.Gst = Gst;
+        fp.dgamma = dgamma;
+        fp.Dsym = Dsym;
+        fp.status = status;
+        fp.B = B;
+        fp.H = H;
+        fp.F = F;
+        const int items = BH * F;
+        kb_frame_grad_tc<<<items < kSms ? items : kSms, kFgThreads, kFgSmem, stream>>>(fp);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 5. token gradients: dq from dO S_f; dk, dv, dbeta from k Dsym_f, v G_f, k G_f^T
     if ((e = token_grads(dO, q, k, v, beta, Sst, Dsym, Gst, dq, dk, dv, dbeta, B, H, F, N, c, status, stream)) !=
