@@ -84,3 +84,23 @@ def test_fused_falls_back_when_not_all_resident():
     o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
     torch.cuda.synchronize()
     assert torch.equal(o, o3) and torch.equal(S, S3)
+
+
+def test_fused_reads_no_stale_start_state():
+    """The workspace filled with NaN bytes before the call: every chunk's start state
+    must come from the hop that publishes it in this launch, never from memory left
+    by an earlier call (a read before the flag would turn the outputs into NaN)."""
+    x = make_workload("layer_60s_720p", device=DEV)
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    nb = gdn.gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, gdn.GDN_FWD_FUSED)
+    ws = gdn.Workspace()
+    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    for _ in range(3):
+        buf = ws.get(nb, DEV)
+        buf.fill_(0xFF)
+        o, S = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, fused=True, workspace=ws)
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+        assert rel_fro(o.float().cpu().numpy(), o3.float().cpu().numpy().astype(np.float64)) < 1e-3
+        assert rel_fro(S.cpu().numpy(), S3.cpu().numpy().astype(np.float64)) < 1e-4
