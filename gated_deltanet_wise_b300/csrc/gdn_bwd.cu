@@ -22,7 +22,7 @@
 //      kernel without outputs, from dS_out, visit G_{F-1}, ..., G_0 and end at
 //      dS_in.
 //   4. kb_frame_grad_tc: dM_f = S_{f-1}^T G_f (tcgen05, hi + lo bf16), dgamma_f, and
-//      Dsym_f = dA_f + dA_f^T.
+//      Dsym_f = dA_f + dA_f^T and G_f as bf16 MMA-operand images for step 5.
 //   5. kg_token_grad_kernel (tcgen05), twice: dO S_f, with q's normalisation
 //      Jacobian in the epilogue, gives dq; k Dsym_f, v G_f and k G_f^T (one G
 //      image read K-major and MN-major), with k's, give dk, dv and dbeta.
@@ -74,8 +74,11 @@ __global__ void kb_build_reverse_ws(const uint8_t *ws_fwd, const uint8_t *ws_E, 
 // 1 issues the MMAs, 2..5 build the images (the next item's matrices are
 // prefetched into L2 first), 6..9 read dM out of TMEM (two accumulator sets,
 // so the next item's MMAs run meanwhile) into a padded fp32 tile in shared
-// memory, from which the trace and the symmetrised Dsym are written with
-// coalesced stores.
+// memory, from which the trace and the symmetrised Dsym are written.  The
+// token-gradient kernel reads Dsym_f and G_f as bf16 MMA operands, so both
+// leave as ready images (row-major, 128 rows x two 128B-swizzled 64-column
+// panels, rows and columns 112.. zero): Dsym_f built here with coalesced
+// 16-byte stores, G_f bulk-copied from this kernel's own hi image.
 constexpr int kFgThreads = 320;
 constexpr uint32_t kFgDMStride = kD + 1;  // odd row stride: row writes and column reads are conflict-free
 constexpr uint32_t kFgOffDM = 4 * kImgBytes;
@@ -88,7 +91,7 @@ struct FrameGradParams {
     const float *Sst;   // S_f after every frame, [BH][F]
     const float *Gst;   // G_f, [BH][F+1] (G_f at slot F-1-f)
     float *dgamma;      // [B][F][H]
-    float *Dsym;        // [BH][F]
+    uint8_t *img_out;   // [BH][F] x (Dsym_f image, G_f image), kImgBytes each
     unsigned *status;
     int B, H, F;
 };
@@ -177,6 +180,8 @@ __global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGra
                 if (nxt) bulk_prefetch_l2(nxt, kStateBytes);
             }
             if (i >= 1 && !(ok = mbar_wait_warp(img_free, (i - 1) & 1, abort_flag))) break;
+            if (lane == 0) bulk_wait_read_all();  // the previous item's G image export has read these rows
+            __syncwarp();
             const float *W[2] = {mat(0, it), mat(1, it)};
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {  // 8-column groups 7 half .. 7 half + 6, both matrices in flight
@@ -216,8 +221,18 @@ __global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGra
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(img_ready);
+            if (lane == 0) {
+                mbar_arrive(img_ready);
+                // this warp's 32 rows of the G_f hi image, both panels, to the token-gradient kernel
+                const int f = it / BH, bh = it % BH;
+                uint8_t *gi = p.img_out + ((size_t)bh * p.F + f) * 2 * kImgBytes + kImgBytes;
+                const uint32_t ro = (uint32_t)(warp - 2) * 32 * kRowB;
+                bulk_s2g(gi + ro, sm + 2 * kImgBytes + ro, 32 * kRowB);
+                bulk_s2g(gi + kImgPanel + ro, sm + 2 * kImgBytes + kImgPanel + ro, 32 * kRowB);
+                bulk_commit();
+            }
         }
+        if (lane == 0) bulk_wait_all();
     } else if (warp >= 6) {
         // epilogue: thread = row i of dM
         const int quad = warp & 3, row = quad * 32 + lane, t = threadIdx.x - 192;  // t: 0..127
@@ -259,10 +274,17 @@ __global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGra
                     for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
                     if (lane == 0) p.dgamma[((size_t)b * p.F + f) * p.H + h] = d;
                 }
-                float *ds = p.Dsym + ((size_t)bh * p.F + f) * kStateFloats;
-                for (int e = t; e < (int)kStateFloats; e += 128) {
-                    const int r = e / kD, c = e - r * kD;
-                    ds[e] = -(dM[r * kFgDMStride + c] + dM[c * kFgDMStride + r]);
+                // Dsym_f image: thread = (row r, 8-column group c8), 16-byte stores along each row
+                uint8_t *di = p.img_out + ((size_t)bh * p.F + f) * 2 * kImgBytes;
+                for (int e = t; e < 128 * 16; e += 128) {
+                    const int r = e >> 4, c8 = e & 15;
+                    float x[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int c = 8 * c8 + k;
+                        x[k] = (r < kD && c < kD) ? -(dM[r * kFgDMStride + c] + dM[c * kFgDMStride + r]) : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(di + (c8 >> 3) * kImgPanel + sw128_off(r, c8 & 7)) = f32x8_to_bf16(x);
                 }
             }
             fg_epi_sync();  // dM may be overwritten by the next item
@@ -284,8 +306,10 @@ __global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGra
 // epilogue (thread = token row) applies the chain rule through the
 // normalisations and writes the final fp32 gradients.
 //   kMode 0: acc = dO W (W = S_f)  ->  dq^ = S_f^T do;  dq = (dq^ - q (q.dq^)/rho^2) / rho
-//   kMode 1: acc0 = k Dsym, acc1 = v G, acc2 = k G^T (the G image read MN-major:
-//            row j, column i holds G[i][j], which is B[n = i][k = j] = G[i][j]);
+//   kMode 1: acc0 = k Dsym, acc1 = v G, acc2 = k G^T from the frame-gradient
+//            kernel's row-major images (image row l = matrix row l): v G reads
+//            the G image MN-major (B[n = j][k = i] = G[i][j]), k G^T K-major
+//            (B[n][k] = G[n][k]), Dsym is symmetric;
 //            with k^ = (c/r) k: dk^ = beta ((c/r) acc0 + acc1),
 //            dk = (c/r)(dk^ - k (k.dk^)/r^2),  dv = beta (c/r) acc2,
 //            dbeta = 1/2 (c/r)^2 k.acc0 + (c/r) k.acc1.
@@ -296,9 +320,6 @@ __global__ void __launch_bounds__(kFgThreads, 1) kb_frame_grad_tc(const FrameGra
 // single set of three in mode 1.
 #ifndef GDN_BWD_LO0
 #define GDN_BWD_LO0 1  // mode 0 keeps the lo image of S_f
-#endif
-#ifndef GDN_BWD_LO1
-#define GDN_BWD_LO1 0  // mode 1 keeps the lo images of Dsym_f and G_f
 #endif
 #ifndef GDN_BWD_TMA_ST
 #define GDN_BWD_TMA_ST 1  // gradient rows leave through shared memory and TMA stores
@@ -313,7 +334,7 @@ static_assert(kGSmem <= kMaxSmem, "token-gradient kernel shared memory");
 constexpr uint32_t kIdescKMN = idesc_bf16(128, kD, false, true);
 
 template <int kMode> struct TokGradShape {
-    static constexpr int kLo = kMode == 0 ? GDN_BWD_LO0 : GDN_BWD_LO1;
+    static constexpr int kLo = kMode == 0 ? GDN_BWD_LO0 : 0;       // mode 1: hi images (bulk-loaded)
     static constexpr int kMats = kMode == 0 ? 1 : 2;
     static constexpr int kImgPer = kLo ? 2 : 1;                     // images per matrix
     static constexpr int kImgs = kMats * kImgPer;
@@ -325,7 +346,8 @@ template <int kMode> struct TokGradShape {
 };
 
 struct TokGradParams {
-    const float *W0, *W1;   // mode 0: S states [BH][F]; mode 1: Dsym [BH][F], G states [BH][F+1] (G_f at F-1-f)
+    const float *W0;        // mode 0: S states [BH][F]
+    const uint8_t *img1;    // mode 1: (Dsym_f, G_f) images [BH][F], kImgBytes each
     const float *beta;
     float *g0, *g1, *g_beta;  // mode 0: dq; mode 1: dk, dv, dbeta
     unsigned *status;
@@ -354,11 +376,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int BH = p.B * p.H;
     const int n_items = BH * p.F;  // item = (frame f, chain bh), f major
     const int n_tiles = (p.N + 127) / 128;
-    // the frame's matrices: W0 of item it; W1 (mode 1) G_f at slot F-1-f
-    auto mat = [&](int w, int it) {
+    // mode 0: the frame's state S_f; mode 1: the item's two images
+    auto mat = [&](int, int it) {
         const int f = it / BH, bh = it % BH;
-        return w == 0 ? p.W0 + ((size_t)bh * p.F + f) * kStateFloats
-                      : p.W1 + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kStateFloats;
+        return p.W0 + ((size_t)bh * p.F + f) * kStateFloats;
+    };
+    auto imgs = [&](int it) {
+        const int f = it / BH, bh = it % BH;
+        return p.img1 + ((size_t)bh * p.F + f) * 2 * kImgBytes;
     };
 
     if (threadIdx.x == 0) {
@@ -370,7 +395,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_free[i], 4);
         }
-        mbar_init(img_ready, 4);
+        mbar_init(img_ready, kMode == 0 ? 4 : 1);
         mbar_init(img_free, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -437,16 +462,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         mma_bf16(acc, a0, sdesc_sw128(w0, 16, 1024), kIdescK, ks > 0);
                         if (Sh::kLo) mma_bf16(acc, a0, sdesc_sw128(w0 + kImgBytes, 16, 1024), kIdescK, 1u);
                         if (kMode == 1) {
+                            // v G: the row-major G image as an MN-major B operand, 16 image rows (K) per step
                             const uint64_t a1 = sdesc_sw128(x1 + koff, 16, 1024);
-                            mma_bf16(acc + 128, a1, sdesc_sw128(w1, 16, 1024), kIdescK, ks > 0);
-                            if (Sh::kLo)
-                                mma_bf16(acc + 128, a1, sdesc_sw128(w1 + kImgBytes, 16, 1024), kIdescK, 1u);
-                            // k G^T: the G image as an MN-major B operand, 16 image rows (K) per step
-                            const uint32_t wm = sbase + kGOffImg + Sh::kImgPer * kImgBytes + ks * 2048;
-                            mma_bf16(acc + 256, a0, sdesc_sw128(wm, kImgPanel, 1024), kIdescKMN, ks > 0);
-                            if (Sh::kLo)
-                                mma_bf16(acc + 256, a0, sdesc_sw128(wm + kImgBytes, kImgPanel, 1024), kIdescKMN,
-                                         1u);
+                            const uint32_t wm = sbase + kGOffImg + kImgBytes + ks * 2048;
+                            mma_bf16(acc + 128, a1, sdesc_sw128(wm, kImgPanel, 1024), kIdescKMN, ks > 0);
+                            // k G^T: the same image K-major
+                            mma_bf16(acc + 256, a0, sdesc_sw128(w1, 16, 1024), kIdescK, ks > 0);
                         }
                     }
                     mma_commit(&acc_full[a]);
@@ -457,10 +478,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mma_commit(drain);
             mbar_wait_drain(drain, 0);
         }
+    } else if (warp < 6 && kMode == 1) {
+        // the item's Dsym_f and G_f images, ready-made by the frame-gradient
+        // kernel: two bulk copies once the previous item's MMAs have read the
+        // slots (the next item's images are prefetched into L2 meanwhile)
+        if (warp == 2 && lane == 0) {
+            bool ok = true;
+            int i = 0, issued = 0;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++i) {
+                if (i >= 1 && !(ok = mbar_wait(img_free, (i - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(img_ready, 2 * kImgBytes);
+                bulk_g2s(sm + kGOffImg, imgs(it), kImgBytes, img_ready);
+                bulk_g2s(sm + kGOffImg + kImgBytes, imgs(it) + kImgBytes, kImgBytes, img_ready);
+                ++issued;
+                if (it + (int)gridDim.x < n_items) bulk_prefetch_l2(imgs(it + gridDim.x), 2 * kImgBytes);
+            }
+            if (*abort_flag && issued) mbar_wait_drain(img_ready, (issued - 1) & 1);
+        }
     } else if (warp < 6) {
-        // images: row j = column j of W (W0 then W1), bf16 hi (+ lo); rows and
-        // columns 112..127 zero.  Four groups of 32 matrix rows, every load of a
-        // group issued before the first conversion.  The next item's matrices are
+        // images: row j = column j of S_f, bf16 hi (+ lo); rows and columns
+        // 112..127 zero.  Four groups of 32 matrix rows, every load of a group
+        // issued before the first conversion.  The next item's matrix is
         // prefetched into L2 while this item's tiles run.
         const int j = (warp & 3) * 32 + lane;
         bool ok = true;
@@ -696,7 +734,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 namespace {
 struct BwdLayout {
     TcPlan plan, plan_G;  // F frames; the reverse scan's F + 1 slots
-    size_t ws_fwd, ws_E, ones, ws_G, gamma_G, Sst, Gst, Dsym, total;
+    size_t ws_fwd, ws_E, ones, ws_G, gamma_G, Sst, Gst, Img1, total;
 };
 
 bool bwd_layout(int B, int H, int F, int N, BwdLayout *L)
@@ -711,7 +749,7 @@ bool bwd_layout(int B, int H, int F, int N, BwdLayout *L)
     L->gamma_G = o; o = up256(o + (size_t)B * (F + 1) * H * 4);
     L->Sst = o; o = up256(o + BH * F * kStateBytes);
     L->Gst = o; o = up256(o + BH * (F + 1) * kStateBytes);
-    L->Dsym = o; o = up256(o + BH * F * kStateBytes);
+    L->Img1 = o; o = up256(o + BH * F * 2 * (size_t)kImgBytes);
     L->total = o;
     return true;
 }
@@ -740,7 +778,7 @@ cudaError_t prepare_bwd_kernels()
 }
 
 cudaError_t token_grads(const void *dO, const void *q, const void *k, const void *v, const float *beta,
-                        const float *Sst, const float *Dsym, const float *Gst, float *dq, float *dk, float *dv,
+                        const float *Sst, const uint8_t *img1, float *dq, float *dk, float *dv,
                         float *dbeta, int B, int H, int F, int N, float c, unsigned *status, cudaStream_t stream)
 {
     CUtensorMap mdo, mq, mk, mv, mdq, mdk, mdv;
@@ -758,7 +796,7 @@ cudaError_t token_grads(const void *dO, const void *q, const void *k, const void
     p.N = N;
     p.c = c;
     p.W0 = Sst;
-    p.W1 = nullptr;
+    p.img1 = img1;
     p.g0 = dq;
     p.g1 = nullptr;
     p.g_beta = nullptr;
@@ -766,8 +804,7 @@ cudaError_t token_grads(const void *dO, const void *q, const void *k, const void
     kg_token_grad_kernel<0><<<grid, kGThreads, kGSmem, stream>>>(mdo, mq, mdq, mdq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    p.W0 = Dsym;
-    p.W1 = Gst;
+    p.W0 = nullptr;
     p.g0 = dk;
     p.g1 = dv;
     p.g_beta = dbeta;
@@ -797,7 +834,7 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     float *ones = reinterpret_cast<float *>(ws + L.ones);
     float *gamma_G = reinterpret_cast<float *>(ws + L.gamma_G);
     float *Sst = reinterpret_cast<float *>(ws + L.Sst), *Gst = reinterpret_cast<float *>(ws + L.Gst);
-    float *Dsym = reinterpret_cast<float *>(ws + L.Dsym);
+    uint8_t *img1 = ws + L.Img1;
     // 1. forward statistics and every state S_f
     if ((e = launch_frame_stats_tc(k, v, beta, gamma, L.plan, c, 0, ws + L.ws_fwd, status, stream)) != cudaSuccess)
         return e;
@@ -817,14 +854,14 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     if ((e = launch_chunk_composite_tc(gamma_G, L.plan_G, 0, ws + L.ws_G, status, stream)) != cudaSuccess) return e;
     if ((e = launch_states_tc(q, gamma_G, dS_out, dS_in, Gst, L.plan_G, ws + L.ws_G, status, stream)) != cudaSuccess)
         return e;
-    // 4. per-frame dgamma and Dsym = dA + dA^T
+    // 4. per-frame dgamma, and Dsym = dA + dA^T and G_f as bf16 images for step 5
     {
         FrameGradParams fp;
         fp.S_in = S_in;
         fp.Sst = Sst;
         fp.Gst = Gst;
         fp.dgamma = dgamma;
-        fp.Dsym = Dsym;
+        fp.img_out = img1;
         fp.status = status;
         fp.B = B;
         fp.H = H;
@@ -834,7 +871,7 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 5. token gradients: dq from dO S_f; dk, dv, dbeta from k Dsym_f, v G_f, k G_f^T
-    if ((e = token_grads(dO, q, k, v, beta, Sst, Dsym, Gst, dq, dk, dv, dbeta, B, H, F, N, c, status, stream)) !=
+    if ((e = token_grads(dO, q, k, v, beta, Sst, img1, dq, dk, dv, dbeta, B, H, F, N, c, status, stream)) !=
         cudaSuccess)
         return e;
     return cudaSuccess;  // dS_in: written by the reverse scan as its final state
