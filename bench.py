@@ -468,15 +468,17 @@ def run_ours(args):
 
 
 def measure_variants(x, K, stream, alg, peaks):
-    """The same layer through gdn_frame_fwd_ex: the token-ordered (product) reading
-    and the reverse-direction scan, K back-to-back calls each after 3 warm-ups."""
+    """The same layer through gdn_frame_fwd_ex: the token-ordered (product) reading,
+    the reverse-direction scan and the fused chained scan (one cooperative launch
+    after a memset of its hop flags), K back-to-back calls each after 3 warm-ups."""
     import torch
     from gated_deltanet_wise_b300 import gdn
     B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
     o = torch.empty_like(x.q)
     S_out = torch.empty(B, H, D, D, dtype=torch.float32, device=x.q.device)
     out = {}
-    for name, flags, launches in (("product", gdn.GDN_FWD_PRODUCT, 4), ("reverse", gdn.GDN_FWD_REVERSE, 3)):
+    for name, flags, launches in (("product", gdn.GDN_FWD_PRODUCT, 5), ("reverse", gdn.GDN_FWD_REVERSE, 3),
+                                  ("fused", gdn.GDN_FWD_FUSED, 1)):
         nb = gdn.gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, flags)
         ws = torch.empty(nb, dtype=torch.uint8, device=x.q.device)
 

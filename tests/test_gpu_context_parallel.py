@@ -88,12 +88,12 @@ def test_split_runs_equal_one_forward(world):
 
 
 def test_resume_equals_forward_and_reads_no_keys():
-    """gdn_frame_fwd_resume after gdn_frame_composite on the same frames equals gdn_frame_fwd
+    """gdn_frame_fwd_resume after gdn_frame_composite on the same frames equals the three-launch forward
     (several chunks, a random start state); k, v and beta are not read again (they are
     overwritten with NaN before the resume)."""
     B, H, F, N = 2, 3, 23, 150
     x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=77, device=DEV, s0_std=0.1)
-    o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0)  # three launches
     ws = gdn.Workspace()
     C, Hc = gdn.frame_composite(x.k, x.v, x.beta, x.gamma, workspace=ws)
     for t in (x.k, x.v, x.beta):

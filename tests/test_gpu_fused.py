@@ -1,4 +1,5 @@
-"""The fused chained scan (gdn_frame_fwd_ex with GDN_FWD_FUSED) on the GPU.
+"""The fused chained scan (gdn_frame_fwd_ex with GDN_FWD_FUSED) and the
+three-launch sum reading (flags 0, which gdn_frame_fwd runs) on the GPU.
 
 One cooperative launch computes the frame statistics, hands each chunk's start
 state to the next chunk's CTA (S_start(c+1) = S_start(c) C_c + H_c, formed on
@@ -30,19 +31,25 @@ def _lib():
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
 
-def _fused(x, **kw):
-    o, S = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, fused=True, **kw)
+def _fused(x, fused=True, **kw):
+    o, S = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0, fused=fused, **kw)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
     return o, S
 
 
+def _three(x, **kw):
+    return _fused(x, fused=False, **kw)
+
+
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("B,H,F,N,s0", [(1, 1, 1, 1, 0.1), (2, 3, 5, 15, 0.1), (1, 2, 9, 65, 0.1),
                                         (2, 1, 3, 130, 0.0), (1, 3, 4, 200, 0.1), (1, 1, 40, 16, 0.1)])
-def test_fused_ragged_shapes_match_oracle(B, H, F, N, s0):
-    """Several chunks per chain (each hop exercised), token tails, with and without S_0."""
+def test_fused_ragged_shapes_match_oracle(B, H, F, N, s0, fused):
+    """Several chunks per chain (each hop exercised), token tails, with and without S_0;
+    the fused launch and the three-launch path."""
     x = make_inputs(B, H, F, N, 112, dtype="bf16", seed=11 * F + N, device=DEV, s0_std=s0)
-    o, S = _fused(x)
+    o, S = _fused(x, fused=fused)
     o_ref, S_ref = oracle.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
     assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL
     assert rel_fro(S.cpu().numpy(), S_ref) <= TOL
@@ -56,8 +63,12 @@ def test_fused_layer_every_chain_and_three_launch_agreement():
     o, S = _fused(x)
     w = check_every_chain(x, o, S, lambda *a: oracle.frame_fwd(*a), TOL)
     print(f"fused layer: worst chain rel_fro {w:.3e}")
-    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o3, S3 = _three(x)
+    w3 = check_every_chain(x, o3, S3, lambda *a: oracle.frame_fwd(*a), TOL)
+    print(f"three launches: worst chain rel_fro {w3:.3e}")
+    od, Sd = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)  # gdn_frame_fwd is the three-launch path
     torch.cuda.synchronize()
+    assert torch.equal(od, o3) and torch.equal(Sd, S3)
     d_o = rel_fro(o.float().cpu().numpy(), o3.float().cpu().numpy().astype(np.float64))
     d_s = rel_fro(S.cpu().numpy(), S3.cpu().numpy().astype(np.float64))
     print(f"fused vs three launches: o {d_o:.2e}, S {d_s:.2e}")
@@ -77,12 +88,11 @@ def test_fused_is_deterministic_and_reverse_matches_oracle():
 
 
 def test_fused_falls_back_when_not_all_resident():
-    """160 chains: one chunk each, 160 CTAs > 148 SMs, so the three-launch path runs
-    (bit-identical to gdn_frame_fwd)."""
+    """160 chains: at least 160 CTAs > 148 SMs, so the three-launch path runs
+    (bit-identical to gdn_frame_fwd_ex with flags 0)."""
     x = make_inputs(1, 160, 2, 64, 112, dtype="bf16", seed=3, device=DEV, s0_std=0.1)
     o, S = _fused(x)
-    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
-    torch.cuda.synchronize()
+    o3, S3 = _three(x)
     assert torch.equal(o, o3) and torch.equal(S, S3)
 
 
@@ -94,7 +104,7 @@ def test_fused_reads_no_stale_start_state():
     B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
     nb = gdn.gdn_frame_fwd_ex_workspace_size(B, H, F, N, D, gdn.GDN_FWD_FUSED)
     ws = gdn.Workspace()
-    o3, S3 = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o3, S3 = _three(x)
     for _ in range(3):
         buf = ws.get(nb, DEV)
         buf.fill_(0xFF)

@@ -196,7 +196,7 @@ def test_device_status_clean():
 def test_profiled_entry_records_stage_events():
     x = make_inputs(1, 4, 6, 300, 112, dtype="bf16", seed=4, device=DEV, s0_std=0.1)
     B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
-    o_ref, S_ref = gdn.frame_fwd(x.q, x.k, x.v, x.beta, x.gamma, x.S0)
+    o_ref, S_ref = gdn.frame_fwd_ex(x.q, x.k, x.v, x.beta, x.gamma, x.S0)  # the three-launch path
     o = torch.empty_like(x.q)
     S = torch.empty_like(S_ref)
     nb = gdn.gdn_frame_fwd_workspace_size(B, H, F, N, D)
