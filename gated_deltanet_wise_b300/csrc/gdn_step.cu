@@ -487,17 +487,25 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
 
         // 5. owned rows: S_out = gamma S_in + the peers' deltas; to global memory,
-        //    and as hi/lo image rows into this CTA and, by bulk copies, the others
+        //    and as hi/lo image rows into this CTA and, by bulk copies, the others.
+        //    The S_in values of this thread's first item and gamma are loaded
+        //    while the deltas are still arriving.
+        const int n8 = (r1 - r0) * 14;
+        float4 pre0 = make_float4(0.f, 0.f, 0.f, 0.f), pre1 = pre0;
+        if (sin && t < n8) {
+            const int rw = r0 + t / 14, c8 = t % 14;
+            pre0 = __ldg(reinterpret_cast<const float4 *>(sin + rw * kD + c8 * 8));
+            pre1 = __ldg(reinterpret_cast<const float4 *>(sin + rw * kD + c8 * 8 + 4));
+        }
+        const float gam = __ldg(p.gamma + (size_t)b * p.H + h);
         if (ok) ok = mbar_wait_warp(recv_full, 0, abort_flag);
         {
-            const float gam = __ldg(p.gamma + (size_t)b * p.H + h);
             float *sout = p.S_out ? p.S_out + (size_t)bh * kStateFloats : nullptr;
             const float *recv = reinterpret_cast<const float *>(sm + kSOffRecv);
-            const int n8 = (r1 - r0) * 14;
             for (int e = t; e < n8; e += 256) {
                 const int lr = e / 14, c8 = e % 14, rw = r0 + lr;
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-                if (sin) {
+                float4 a0 = pre0, a1 = pre1;
+                if (sin && e != t) {
                     a0 = __ldg(reinterpret_cast<const float4 *>(sin + rw * kD + c8 * 8));
                     a1 = __ldg(reinterpret_cast<const float4 *>(sin + rw * kD + c8 * 8 + 4));
                 }
