@@ -15,12 +15,13 @@
 //   1. K1 on (k, v): A_f images, U_f and chunk composites in a workspace; the
 //      chunk-boundary kernel and the scan kernel without outputs, from S_in,
 //      store every S_f.
-//   2. K1 on (k := q, v := dO, beta := 1, c := 1): its U_f slots are E_f.
-//   3. kb_build_reverse_ws lays out the reverse scan: slot p holds A of frame
-//      F - p (none for p = 0) and E_{F-1-p} (none for p = F), gamma likewise;
-//      its chunk composites (K1c), the chunk-boundary kernel and the scan
-//      kernel without outputs, from dS_out, visit G_{F-1}, ..., G_0 and end at
-//      dS_in.
+//   2. K1 on (k := q, v := dO, beta := 1, c := 1) in its E mode forms only the
+//      U_f slots, which are E_f.
+//   3. The reverse scan: slot p holds A of frame F - p (none for p = 0) and
+//      E_{F-1-p} (none for p = F), gamma likewise; the two K1 passes write
+//      those slots directly and kb_reverse_edges fills the empty ends; its chunk
+//      composites (K1c), the chunk-boundary kernel and the scan kernel without
+//      outputs, from dS_out, visit G_{F-1}, ..., G_0 and end at dS_in.
 //   4. kb_frame_grad_tc: dM_f = S_{f-1}^T G_f (tcgen05, hi + lo bf16), dgamma_f, and
 //      Dsym_f = dA_f + dA_f^T and G_f as bf16 MMA-operand images for step 5.
 //   5. kg_token_grad_kernel (tcgen05), twice: dO S_f, with q's normalisation
@@ -40,29 +41,20 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
 
 // ------------------------------------------------------------------ helpers
-__global__ void kb_fill(float *p, size_t n, float value)
+// The reverse scan's workspace: slot p of a chain holds A of frame F - p and E
+// of frame F - 1 - p, written there by the two statistics passes; this kernel
+// fills the two empty ends (no A in slot 0, no E in slot F) with zeros and lays
+// out gamma in slot order (1 for slot 0).  One block per chain.
+__global__ void kb_reverse_edges(uint8_t *ws_G, const float *gamma, float *gamma_G, int B, int H, int F)
 {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        p[i] = value;
-}
-
-// Reverse-scan workspace, one block per (chain, slot p = 0..F).
-__global__ void kb_build_reverse_ws(const uint8_t *ws_fwd, const uint8_t *ws_E, uint8_t *ws_G, const float *gamma,
-                                    float *gamma_G, int B, int H, int F)
-{
-    const int bh = blockIdx.x, p = blockIdx.y;
+    const int bh = blockIdx.x;
     const int b = bh / H, h = bh % H;
-    uint4 *dst = reinterpret_cast<uint4 *>(ws_G + ((size_t)bh * (F + 1) + p) * kFrameWs);
-    const uint4 *srcA = p >= 1 ? reinterpret_cast<const uint4 *>(ws_fwd + ((size_t)bh * F + (F - p)) * kFrameWs)
-                               : nullptr;
-    const uint4 *srcU =
-        p <= F - 1 ? reinterpret_cast<const uint4 *>(ws_E + ((size_t)bh * F + (F - 1 - p)) * kFrameWs + kAimgBytes)
-                   : nullptr;
-    constexpr int nA = kAimgBytes / 16, nU = kUBytes / 16;
-    for (int i = threadIdx.x; i < nA; i += blockDim.x) dst[i] = srcA ? srcA[i] : make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < nU; i += blockDim.x) dst[nA + i] = srcU ? srcU[i] : make_uint4(0, 0, 0, 0);
-    if (threadIdx.x == 0)
-        gamma_G[((size_t)b * (F + 1) + p) * H + h] = p >= 1 ? gamma[((size_t)b * F + (F - p)) * H + h] : 1.f;
+    uint4 *a0 = reinterpret_cast<uint4 *>(ws_G + (size_t)bh * (F + 1) * kFrameWs);
+    uint4 *uF = reinterpret_cast<uint4 *>(ws_G + ((size_t)bh * (F + 1) + F) * kFrameWs + kAimgBytes);
+    for (int i = threadIdx.x; i < (int)(kAimgBytes / 16); i += blockDim.x) a0[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < (int)(kUBytes / 16); i += blockDim.x) uF[i] = make_uint4(0, 0, 0, 0);
+    for (int q = threadIdx.x; q <= F; q += blockDim.x)
+        gamma_G[((size_t)b * (F + 1) + q) * H + h] = q >= 1 ? gamma[((size_t)b * F + (F - q)) * H + h] : 1.f;
 }
 
 // dM_f = S_{f-1}^T G_f, dgamma_f = trace(dM_f), Dsym_f = -(dM_f + dM_f^T), on
@@ -734,7 +726,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 namespace {
 struct BwdLayout {
     TcPlan plan, plan_G;  // F frames; the reverse scan's F + 1 slots
-    size_t ws_fwd, ws_E, ones, ws_G, gamma_G, Sst, Gst, Img1, total;
+    size_t ws_fwd, ws_G, gamma_G, Sst, Gst, Img1, total;
 };
 
 bool bwd_layout(int B, int H, int F, int N, BwdLayout *L)
@@ -743,8 +735,6 @@ bool bwd_layout(int B, int H, int F, int N, BwdLayout *L)
     const size_t BH = (size_t)B * H;
     size_t o = 0;
     L->ws_fwd = o; o = up256(o + L->plan.ws_bytes);
-    L->ws_E = o; o = up256(o + L->plan.ws_bytes);
-    L->ones = o; o = up256(o + (size_t)B * F * N * H * 4);
     L->ws_G = o; o = up256(o + L->plan_G.ws_bytes);
     L->gamma_G = o; o = up256(o + (size_t)B * (F + 1) * H * 4);
     L->Sst = o; o = up256(o + BH * F * kStateBytes);
@@ -830,26 +820,23 @@ cudaError_t launch_frame_bwd_tc(const void *q, const void *k, const void *v, con
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = B * H;
-    const size_t rows = (size_t)B * F * N * H;  // token rows (beta entries)
-    float *ones = reinterpret_cast<float *>(ws + L.ones);
     float *gamma_G = reinterpret_cast<float *>(ws + L.gamma_G);
     float *Sst = reinterpret_cast<float *>(ws + L.Sst), *Gst = reinterpret_cast<float *>(ws + L.Gst);
     uint8_t *img1 = ws + L.Img1;
-    // 1. forward statistics and every state S_f
-    if ((e = launch_frame_stats_tc(k, v, beta, gamma, L.plan, c, 0, ws + L.ws_fwd, status, stream)) != cudaSuccess)
+    uint8_t *ws_rev = ws + L.ws_G + L.plan_G.off_frames;
+    // 1. forward statistics (A_f images also into the reverse scan's slots) and every state S_f
+    if ((e = launch_frame_stats_tc(k, v, beta, gamma, L.plan, c, 0, ws + L.ws_fwd, status, stream, ws_rev, 0)) !=
+        cudaSuccess)
         return e;
     if ((e = launch_states_tc(q, gamma, S_in, nullptr, Sst, L.plan, ws + L.ws_fwd, status, stream)) != cudaSuccess)
         return e;
-    // 2. E_f = dO^T q^ through the statistics kernel (k := q, v := dO, beta := 1, c := 1)
-    kb_fill<<<296, 256, 0, stream>>>(ones, rows, 1.f);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_frame_stats_tc(q, dO, ones, gamma, L.plan, 1.f, 0, ws + L.ws_E, status, stream)) != cudaSuccess)
+    // 2. E_f = dO^T q^ through the statistics kernel in its E mode (k := q, v := dO, beta := 1,
+    //    c := 1), straight into the reverse scan's slots
+    if ((e = launch_frame_stats_tc(q, dO, nullptr, gamma, L.plan, 1.f, 0, ws + L.ws_fwd, status, stream, ws_rev,
+                                   1)) != cudaSuccess)
         return e;
     // 3. reverse scan G_{F-1} .. G_0, ending at dS_in
-    kb_build_reverse_ws<<<dim3(BH, F + 1), 256, 0, stream>>>(ws + L.ws_fwd + L.plan.off_frames,
-                                                              ws + L.ws_E + L.plan.off_frames,
-                                                              ws + L.ws_G + L.plan_G.off_frames, gamma, gamma_G, B, H,
-                                                              F);
+    kb_reverse_edges<<<BH, 256, 0, stream>>>(ws_rev, gamma, gamma_G, B, H, F);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_chunk_composite_tc(gamma_G, L.plan_G, 0, ws + L.ws_G, status, stream)) != cudaSuccess) return e;
     if ((e = launch_states_tc(q, gamma_G, dS_out, dS_in, Gst, L.plan_G, ws + L.ws_G, status, stream)) != cudaSuccess)

@@ -96,7 +96,7 @@ cudaError_t launch_frame_fwd_product_tc(const void *q, const void *k, const void
 // K1 alone (per-frame statistics into the plan's workspace).
 cudaError_t launch_frame_stats_tc(const void *k, const void *v, const float *beta, const float *gamma,
                                   const TcPlan &plan, float c, int reverse, void *workspace, unsigned *status,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, uint8_t *ws_rev = nullptr, int e_mode = 0);
 // The state chain alone (K1b + K2 without outputs) over a plan whose workspace
 // holds statistics and chunk composites; every state to states (gdn_tc.cu).
 cudaError_t launch_states_tc(const void *q, const float *gamma, const float *S_in, float *S_out, float *states,

@@ -119,7 +119,16 @@ struct K1Params {
     float c;
     int reverse;  // 1: frames are visited from the last to the first
     int withhold_loads;  // failure-detection test: the producer issues nothing
+    // Backward use: the reverse scan's workspace (F + 1 slots per chain), written by the
+    // kK1RevA and kK1E instantiations.  beta == null means beta = 1 for every token.
+    uint8_t *ws_rev;
 };
+
+// K1 instantiations: the forward's; one that also writes each A_f image into slot F - f
+// of the reverse scan's workspace; and the E mode, which forms only U_f (the backward's
+// E_f = dO^T q^: no A_f MMA, no A_f image, no composites) and writes it to the U area of
+// slot F - 1 - f, nothing to the forward workspace.
+constexpr int kK1Fwd = 0, kK1RevA = 1, kK1E = 2;
 
 // Tensor memory of K1 (512 columns, fp32 unless noted):
 //   [  0,128) acc_A: A_f = X^T K; after read-out it holds the composite MMAs'
@@ -134,7 +143,7 @@ constexpr uint32_t kTmAccA = 0, kTmAccU = 128, kTmC = 256, kTmH = 384, kTmImgC =
 // With kKeepTmem the CTA's 512 TMEM columns stay allocated on return (the chunk
 // composites C and H still in them) and their address is returned; *aborted
 // receives the role abort flag.
-template <bool kKeepTmem>
+template <bool kKeepTmem, int kMode = kK1Fwd>
 __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUtensorMap &mapV, const K1Params &p,
                                             uint8_t *sm, int *aborted)
 {
@@ -224,7 +233,9 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
                         const uint64_t blo = sdesc_sw128(stg + kOffBlo + o, kTSPanel, 1024);
                         const uint64_t av = sdesc_sw128(stg + kOffV + o, kTSPanel, 1024);
                         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
-                        mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffK + o, kTSPanel, 1024), bhi, kIdescMN, acc);
+                        if (!(kMode == kK1E))
+                            mma_bf16(tmem + kTmAccA, sdesc_sw128(stg + kOffK + o, kTSPanel, 1024), bhi, kIdescMN,
+                                     acc);
                         mma_bf16(tmem + kTmAccU, av, bhi, kIdescMN, acc);
                         if (kK1Lo) mma_bf16(tmem + kTmAccU, av, blo, kIdescMN, 1u);
                     }
@@ -232,17 +243,20 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
                 }
                 if (!ok) break;
                 mma_commit(acc_full);
-                // composite: T_C += (-C) A_f, T_H += (-H) A_f (T_C, T_H pre-scaled by gamma, T_H += U_f)
+                // composite: T_C += (-C) A_f, T_H += (-H) A_f (T_C, T_H pre-scaled by gamma, T_H += U_f);
+                // comp_ready also says the epilogue has read this frame's accumulators
                 if (!(ok = mbar_wait(comp_ready, fl & 1, abort_flag))) break;
                 tc_fence_after();
+                if (kMode != kK1E) {
 #pragma unroll
-                for (int ks = 0; ks < 7; ++ks) {
-                    const uint64_t bdesc =
-                        sdesc_sw128(sbase + kK1OffAimg + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
-                    mma_bf16_tmem_a(tmem + kTmC, tmem + kTmImgC + ks * 8, bdesc, kIdescK, 1u);
-                    mma_bf16_tmem_a(tmem + kTmH, tmem + kTmImgH + ks * 8, bdesc, kIdescK, 1u);
+                    for (int ks = 0; ks < 7; ++ks) {
+                        const uint64_t bdesc =
+                            sdesc_sw128(sbase + kK1OffAimg + (ks >> 2) * kAimgPanel + (ks & 3) * 32, 16, 1024);
+                        mma_bf16_tmem_a(tmem + kTmC, tmem + kTmImgC + ks * 8, bdesc, kIdescK, 1u);
+                        mma_bf16_tmem_a(tmem + kTmH, tmem + kTmImgH + ks * 8, bdesc, kIdescK, 1u);
+                    }
+                    mma_commit(comp_done);
                 }
-                mma_commit(comp_done);
             }
             mma_commit(drain);  // every MMA issued above has completed once this phase lands
             mbar_wait_drain(drain, 0);
@@ -261,6 +275,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
         const int total = nf * n_st;
         auto load_beta = [&](int itx, int r) -> float {
             if (itx >= total) return 0.f;
+            if (!p.beta) return 1.f;
             const int fl = itx / n_st, n = (itx - fl * n_st) * kTS + r;
             if (n >= p.N) return 0.f;
             return __ldg(p.beta + ((size_t)b * FN + (size_t)frame_at(f_begin + fl, p.F, p.reverse) * p.N + n) * p.H + h);
@@ -357,8 +372,10 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
             __syncwarp();
             if (!(ok = mbar_wait_warp(acc_full, fe & 1, abort_flag))) break;
             tc_fence_after();
-            uint8_t *ws = p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
-            float *wsU = reinterpret_cast<float *>(ws + kAimgBytes);
+            uint8_t *ws = (kMode == kK1E) ? nullptr : p.ws_frames + ((size_t)bh * p.F + f) * kFrameWs;
+            float *wsU = reinterpret_cast<float *>(
+                (kMode == kK1E) ? p.ws_rev + ((size_t)bh * (p.F + 1) + (p.F - 1 - f)) * kFrameWs + kAimgBytes
+                         : ws + kAimgBytes);
             // pass 1: A_f -> bf16 image (shared memory), U_f -> workspace.  TMEM loads
             // go out two 16-column chunks at a time: each wait costs a full load
             // latency, which the frame boundary otherwise pays seven times.
@@ -367,7 +384,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
             uint32_t ra2[2][16], ru2[2][16];
 #pragma unroll
             for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
-                tmem_ld16(tmem + lane_off + kTmAccA + (cp + hf) * 16, ra2[hf]);
+                if (!(kMode == kK1E)) tmem_ld16(tmem + lane_off + kTmAccA + (cp + hf) * 16, ra2[hf]);
                 tmem_ld16(tmem + lane_off + kTmAccU + (cp + hf) * 16, ru2[hf]);
             }
             tmem_ld_wait();
@@ -377,12 +394,14 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
                 const uint32_t col = cc * 16;
                 const uint32_t *ra = ra2[hf], *ru = ru2[hf];
                 if (row < kD) {
-                    float a[16];
+                    if (!(kMode == kK1E)) {
+                        float a[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) a[j] = __uint_as_float(ra[j]);
-                    uint8_t *dst = sm + kK1OffAimg + (cc >> 2) * kAimgPanel;
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3))) = f32x8_to_bf16(a);
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3) + 1)) = f32x8_to_bf16(a + 8);
+                        for (int j = 0; j < 16; ++j) a[j] = __uint_as_float(ra[j]);
+                        uint8_t *dst = sm + kK1OffAimg + (cc >> 2) * kAimgPanel;
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3))) = f32x8_to_bf16(a);
+                        *reinterpret_cast<uint4 *>(dst + sw128_off(row, 2 * (cc & 3) + 1)) = f32x8_to_bf16(a + 8);
+                    }
                     float4 *u4 = reinterpret_cast<float4 *>(wsU) + (col / 4) * kD + row;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -394,7 +413,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
                 }
             }
             }
-            if (row < kD) {  // key columns 112..127 of the image: zero
+            if (row < kD && !(kMode == kK1E)) {  // key columns 112..127 of the image: zero
                 uint8_t *dst = sm + kK1OffAimg + kAimgPanel;
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 6)) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(dst + sw128_off(row, 7)) = make_uint4(0, 0, 0, 0);
@@ -403,7 +422,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
             // touches only its own TMEM lanes, and has read all of them above
             // pass 2: H <- gamma H + U_f, C <- gamma C; A operands -bf16(H_prev), -bf16(C_prev)
 #pragma unroll
-            for (int cp = 0; cp < 7; cp += 2) {
+            for (int cp = 0; cp < 7 && !(kMode == kK1E); cp += 2) {
             uint32_t ru2[2][16], rh2[2][16], rc2[2][16];
 #pragma unroll
             for (int hf = 0; hf < 2 && cp + hf < 7; ++hf) {
@@ -440,19 +459,28 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(comp_ready);
-                if (kWsKeepL2) {
-                    bulk_s2g_hint(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB, ws_pol);
-                    bulk_s2g_hint(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off,
-                                  img_rows * kRowB, ws_pol);
-                } else {
-                    bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
-                    bulk_s2g(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off, img_rows * kRowB);
+                if (!(kMode == kK1E)) {
+                    if (kWsKeepL2) {
+                        bulk_s2g_hint(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB, ws_pol);
+                        bulk_s2g_hint(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off,
+                                      img_rows * kRowB, ws_pol);
+                    } else {
+                        bulk_s2g(ws + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
+                        bulk_s2g(ws + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off,
+                                 img_rows * kRowB);
+                    }
+                    if (kMode == kK1RevA) {  // the reverse scan's slot F - f holds A_f as well
+                        uint8_t *wr = p.ws_rev + ((size_t)bh * (p.F + 1) + (p.F - f)) * kFrameWs;
+                        bulk_s2g(wr + img_off, sm + kK1OffAimg + img_off, img_rows * kRowB);
+                        bulk_s2g(wr + kAimgPanel + img_off, sm + kK1OffAimg + kAimgPanel + img_off,
+                                 img_rows * kRowB);
+                    }
+                    bulk_commit();
                 }
-                bulk_commit();
             }
         }
         // chunk composites out: wait for the last frame's composite MMAs
-        if (ok && (ok = mbar_wait_warp(comp_done, (nf - 1) & 1, abort_flag))) {
+        if (ok && !(kMode == kK1E) && (ok = mbar_wait_warp(comp_done, (nf - 1) & 1, abort_flag))) {
             tc_fence_after();
             float *comp = p.ws_comp + ((size_t)bh * p.n_chunks + chunk_idx) * 2 * kStateFloats;
 #pragma unroll
@@ -488,6 +516,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
     return tmem;
 }
 
+template <int kMode>
 __global__ void __launch_bounds__(kK1Threads, 1)
     k1_frame_stats_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                           const K1Params p)
@@ -495,7 +524,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int aborted;
-    k1_body<false>(mapK, mapV, p, sm, &aborted);
+    k1_body<false, kMode>(mapK, mapV, p, sm, &aborted);
 }
 
 // ===================================================================== K1b
@@ -1354,7 +1383,12 @@ cudaError_t prepare_tc_kernels()
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevTc) return cudaErrorInvalidDevice;
     if (g_tc_attrs[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k1_frame_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1Smem);
+    e = cudaFuncSetAttribute(k1_frame_stats_kernel<kK1Fwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1Smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k1_frame_stats_kernel<kK1RevA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kK1Smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k1_frame_stats_kernel<kK1E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK1Smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k2_scan_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kK2Smem);
     if (e != cudaSuccess) return e;
@@ -1384,6 +1418,7 @@ K1Params k1_params(const float *beta, const float *gamma, const TcPlan &pl, floa
     p1.c = c;
     p1.reverse = reverse;
     p1.withhold_loads = pl.withhold_loads;
+    p1.ws_rev = nullptr;
     return p1;
 }
 }  // namespace
@@ -1406,7 +1441,7 @@ cudaError_t launch_frame_composite_tc(const void *k, const void *v, const float 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int BH = pl.B * pl.H;
     const K1Params p1 = k1_params(beta, gamma, pl, c, 0, ws, status);
-    if ((e = launch_pdl(k1_frame_stats_kernel, dim3(BH * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1)) !=
+    if ((e = launch_pdl(k1_frame_stats_kernel<kK1Fwd>, dim3(BH * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1)) !=
         cudaSuccess)
         return e;
     const float *comp = p1.ws_comp;
@@ -1435,15 +1470,22 @@ cudaError_t launch_state_compose_tc(const float *S, const float *C, const float 
 // K1 alone over a plan: per-frame A_f image and U_f (and chunk composites) in the workspace.
 cudaError_t launch_frame_stats_tc(const void *k, const void *v, const float *beta, const float *gamma,
                                   const TcPlan &pl, float c, int reverse, void *workspace, unsigned *status,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, uint8_t *ws_rev, int e_mode)
 {
     CUtensorMap mk, mv;
     if (!make_token_map(&mk, k, pl.B, pl.H, pl.F, pl.N, kTS) || !make_token_map(&mv, v, pl.B, pl.H, pl.F, pl.N, kTS))
         return cudaErrorInvalidValue;
     cudaError_t e = prepare_tc_kernels();
     if (e != cudaSuccess) return e;
-    const K1Params p1 = k1_params(beta, gamma, pl, c, reverse, static_cast<uint8_t *>(workspace), status);
-    return launch_pdl(k1_frame_stats_kernel, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv,
+    K1Params p1 = k1_params(beta, gamma, pl, c, reverse, static_cast<uint8_t *>(workspace), status);
+    p1.ws_rev = ws_rev;
+    if (ws_rev && e_mode)
+        return launch_pdl(k1_frame_stats_kernel<kK1E>, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream,
+                          mk, mv, p1);
+    if (ws_rev)
+        return launch_pdl(k1_frame_stats_kernel<kK1RevA>, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem,
+                          stream, mk, mv, p1);
+    return launch_pdl(k1_frame_stats_kernel<kK1Fwd>, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv,
                       p1);
 }
 
@@ -1545,7 +1587,7 @@ cudaError_t launch_frame_fwd_tc(const void *q, const void *k, const void *v, con
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const K1Params p1 = k1_params(beta, gamma, pl, c, reverse, ws, status);
     if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return e;
-    e = launch_pdl(k1_frame_stats_kernel, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1);
+    e = launch_pdl(k1_frame_stats_kernel<kK1Fwd>, dim3(pl.B * pl.H * pl.n_chunks), kK1Threads, kK1Smem, stream, mk, mv, p1);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     return launch_scan_output_tc(q, gamma, S_in, S_out, o, pl, reverse, ws, status, stream, events);
