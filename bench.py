@@ -614,7 +614,7 @@ def measure_backward(x, K, stream, peaks):
     del ws
     return {"ms_per_step": round(ms, 4), "tokens_per_s": round(B * F * N / (ms * 1e-3), 1),
             "algorithmic_bytes": alg, "path_frac_hbm": round(alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "steps": K, "gpu_launches_per_step": 12, "workspace_bytes": nb}
+            "steps": K, "gpu_launches_per_step": 11, "workspace_bytes": nb}
 
 
 def run_e2e(x, K, W, world):
