@@ -473,7 +473,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     } else if (warp < 6 && kMode == 1) {
         // the item's Dsym_f and G_f images, ready-made by the frame-gradient
         // kernel: two bulk copies once the previous item's MMAs have read the
-        // slots (the next item's images are prefetched into L2 meanwhile)
+        // slots.  (Prefetching the next item's images into L2 meanwhile was
+        // measured 18 us slower per backward on the 20-head layer.)
         if (warp == 2 && lane == 0) {
             bool ok = true;
             int i = 0, issued = 0;
@@ -483,7 +484,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 bulk_g2s(sm + kGOffImg, imgs(it), kImgBytes, img_ready);
                 bulk_g2s(sm + kGOffImg + kImgBytes, imgs(it) + kImgBytes, kImgBytes, img_ready);
                 ++issued;
-                if (it + (int)gridDim.x < n_items) bulk_prefetch_l2(imgs(it + gridDim.x), 2 * kImgBytes);
             }
             if (*abort_flag && issued) mbar_wait_drain(img_ready, (issued - 1) & 1);
         }

@@ -528,15 +528,19 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 }
 
 // ===================================================================== K1b
-// S_start(c) for every chunk, row-parallel fp32: rows [8*y, 8*y+8) of chain x.
-// The chain is sequential over chunks, S_start(c+1) = S_start(c) C_c + H_c, so
-// each step's composite C_c (50 KB) is bulk-copied into shared memory while
-// the previous step computes (two buffers, one mbarrier each).
-constexpr int kK1bRows = 8;
-constexpr int kK1bThreads = 224;
-constexpr uint32_t kK1bOffS = 2 * (uint32_t)kStateBytes;           // S rows [8][112]
-constexpr uint32_t kK1bOffBar = kK1bOffS + kK1bRows * kD * 4;      // 2 mbarriers + abort flag
+// S_start(c) for every chunk, row-parallel fp32: rows [16*y, 16*y+16) of chain
+// x, seven CTAs per chain (one wave for the 20-head layer).  The chain is
+// sequential over chunks, S_start(c+1) = S_start(c) C_c + H_c; the composites
+// C_c (50 KB each) are bulk-copied into a ring of four shared-memory buffers,
+// up to four steps ahead, so that a step rarely waits for its copy.
+constexpr int kK1bRows = 16;
+constexpr int kK1bThreads = 448;                                    // 112 columns x 4 groups of 4 rows
+constexpr int kK1bBufs = 4;
+constexpr uint32_t kK1bOffS = kK1bBufs * (uint32_t)kStateBytes;     // S rows [16][112]
+constexpr uint32_t kK1bOffBar = kK1bOffS + kK1bRows * kD * 4;       // kK1bBufs mbarriers + abort flag
 constexpr uint32_t kK1bSmem = kK1bOffBar + 64;
+static_assert(kD % kK1bRows == 0 && kK1bThreads == kD * (kK1bRows / 4), "K1b row split");
+static_assert(kK1bSmem <= kMaxSmem, "K1b shared memory");
 // K1b modes: the start state is the identity (instead of S_in), and/or the input
 // composites are zero.  With both the scan composes the transition composites,
 // C_0 C_1 ... C_{n-1}; with neither it is the chunk-boundary scan proper.
@@ -548,17 +552,15 @@ __global__ void __launch_bounds__(kK1bThreads)
                               int n_chunks, unsigned *status, int mode)
 {
     extern __shared__ __align__(128) uint8_t k1b_smem[];
-    float *Cb0 = reinterpret_cast<float *>(k1b_smem);
-    float *Cb1 = reinterpret_cast<float *>(k1b_smem + kStateBytes);
     float(*Srows)[kD] = reinterpret_cast<float(*)[kD]>(k1b_smem + kK1bOffS);
     uint64_t *bar = reinterpret_cast<uint64_t *>(k1b_smem + kK1bOffBar);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + kK1bBufs);
+    auto cbuf = [&](int i) { return reinterpret_cast<float *>(k1b_smem + (size_t)i * kStateBytes); };
     const int bh = blockIdx.x, r0 = blockIdx.y * kK1bRows;
     const int t = threadIdx.x, j = t % kD, rp = t / kD;  // rows r0 + 4*rp + 0..3
     const float *cC = compC + (size_t)bh * chain_stride, *cH = compH + (size_t)bh * chain_stride;
     if (t == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < kK1bBufs; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -569,49 +571,67 @@ __global__ void __launch_bounds__(kK1bThreads)
         Srows[rr][cc] = (mode & kK1bIdentityIn) ? (r0 + rr == cc ? 1.f : 0.f)
                         : S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
     }
-    __syncthreads();
     // composite steps to apply: without S_out the state after the last chunk is not needed
     const int steps = S_out ? n_chunks : n_chunks - 1;
-    if (t == 0 && steps > 0) {
-        mbar_arrive_expect_tx(&bar[0], (uint32_t)kStateBytes);
-        bulk_g2s(Cb0, cC, (uint32_t)kStateBytes, &bar[0]);
-    }
-    int issued = steps > 0 ? 1 : 0;
-    for (int c = 0; c < n_chunks; ++c) {
+    int issued = 0;
+    if (t == 0)
+        for (; issued < steps && issued < kK1bBufs; ++issued) {
+            mbar_arrive_expect_tx(&bar[issued], (uint32_t)kStateBytes);
+            bulk_g2s(cbuf(issued), cC + (size_t)issued * chunk_stride, (uint32_t)kStateBytes, &bar[issued]);
+        }
+    // this thread's entries of H_c, loaded one step ahead
+    const bool zero_h = (mode & kK1bZeroH) != 0;
+    const float *h_ptr = cH + (r0 + 4 * rp) * kD + j;
+    float h_next[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h_next[q] = (zero_h || steps == 0) ? 0.f : h_ptr[q * kD];
+    __syncthreads();
+    int c = 0;  // on abort: the step whose copy was not seen to land
+    for (; c < n_chunks; ++c) {
         if (ws_start) {
             float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
             for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
                 dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
         }
         if (c >= steps) break;
-        // the other buffer was last read in step c-1 (closed by the barrier below): refill it
-        if (t == 0 && c + 1 < steps) {
-            mbar_arrive_expect_tx(&bar[(c + 1) & 1], (uint32_t)kStateBytes);
-            bulk_g2s((c + 1) & 1 ? Cb1 : Cb0, cC + (size_t)(c + 1) * chunk_stride, (uint32_t)kStateBytes,
-                     &bar[(c + 1) & 1]);
-            ++issued;
-        }
-        const float *Hc = cH + (size_t)c * chunk_stride;
         float acc[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = (mode & kK1bZeroH) ? 0.f : Hc[(r0 + 4 * rp + q) * kD + j];
-        if (t == 0 && !mbar_wait(&bar[c & 1], (c >> 1) & 1, abort_flag)) *abort_flag = 1;
+        for (int q = 0; q < 4; ++q) acc[q] = h_next[q];
+        h_ptr += chunk_stride;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h_next[q] = (zero_h || c + 1 >= steps) ? 0.f : h_ptr[q * kD];
+        const int buf = c % kK1bBufs;
+        if (t == 0 && !mbar_wait(&bar[buf], (c / kK1bBufs) & 1, abort_flag)) *abort_flag = 1;
         __syncthreads();
         if (*abort_flag) break;
-        const float *C = (c & 1) ? Cb1 : Cb0;
-        for (int l = 0; l < kD; ++l) {
-            const float cl = C[l * kD + j];
+        const float *C = cbuf(buf);
+        for (int l = 0; l < kD; l += 4) {  // four k steps per float4 of each S row (a broadcast load)
+            float cl[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = fmaf(Srows[4 * rp + q][l], cl, acc[q]);
+            for (int k = 0; k < 4; ++k) cl[k] = C[(l + k) * kD + j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(&Srows[4 * rp + q][l]);
+                acc[q] = fmaf(s4.x, cl[0], acc[q]);
+                acc[q] = fmaf(s4.y, cl[1], acc[q]);
+                acc[q] = fmaf(s4.z, cl[2], acc[q]);
+                acc[q] = fmaf(s4.w, cl[3], acc[q]);
+            }
         }
-        __syncthreads();
+        __syncthreads();  // every thread is done with this buffer and with the old rows
+        if (t == 0 && c + kK1bBufs < steps) {
+            mbar_arrive_expect_tx(&bar[buf], (uint32_t)kStateBytes);
+            bulk_g2s(cbuf(buf), cC + (size_t)(c + kK1bBufs) * chunk_stride, (uint32_t)kStateBytes, &bar[buf]);
+            ++issued;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) Srows[4 * rp + q][j] = acc[q];
         __syncthreads();
     }
     if (*abort_flag) {
         if (t == 0) {
-            for (int i = 0; i < issued; ++i) mbar_wait_drain(&bar[i & 1], (i >> 1) & 1);
+            // copies 0..c-1 were waited for; each later one is its buffer's pending phase
+            for (int i = c; i < issued; ++i) mbar_wait_drain(&bar[i % kK1bBufs], (i / kK1bBufs) & 1);
             if (status) atomicOr(status, kStatusTimeout);
         }
         return;
@@ -640,8 +660,8 @@ struct K2Params {
 // kernel runs it on four warps with all 112 columns; the fused chained scan,
 // whose 448 threads allow 128 registers each, on eight warps with 56 columns.
 // As soon as S_f's images are written, S <- gamma_f S + U_f (U_f read from
-// global memory, where it was prefetched into L2 a frame ahead, quad-major: a
-// warp's lanes read 512 contiguous bytes), overlapping the S A_f GEMM; when
+// global memory, quad-major: a warp's lanes read 512 contiguous bytes, four
+// 8-column chunks ahead of their use), overlapping the S A_f GEMM; when
 // that lands, S <- S - S_f A_f.
 template <int kCols, int kC0>
 __device__ __forceinline__ void k2_state_role(const K2Params &p, uint8_t *sm, uint32_t tmem, uint64_t *s_ready,
@@ -827,17 +847,22 @@ __device__ __forceinline__ void k2_body(const CUtensorMap &mapQ, const CUtensorM
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producers
-        // Lane 0 streams the per-frame A_f images (and prefetches U_f into L2
-        // for the state warps), lane 1 the Q tiles, so that neither stream
-        // waits behind the other's buffer reuse.
+        // Lane 0 streams the per-frame A_f images, lane 1 the Q tiles, so that
+        // neither stream waits behind the other's buffer reuse.  Without
+        // outputs lane 0 also prefetches the next frame's U_f into L2 for the
+        // state warps; with outputs it does not: a frame ahead, about half of
+        // the prefetched lines were evicted by the Q/O stream before their
+        // loads (107 MB more DRAM reads per layer, K2 226 -> 239 us).
         if (lane == 0) {
             int a_issued = 0;
-            bulk_prefetch_l2(ws_chain + kAimgBytes, kUBytes);
+            const bool prefetch_u = p.states_only != 0;
+            if (prefetch_u) bulk_prefetch_l2(ws_chain + kAimgBytes, kUBytes);
             for (int it = 0; it < nf; ++it) {
                 if (it >= 1 && !mbar_wait(a_empty, (it - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(a_full, kAimgBytes);
                 bulk_g2s(sm + kK2OffA, ws_chain + (size_t)it * kFrameWs, kAimgBytes, a_full);
-                if (it + 1 < nf) bulk_prefetch_l2(ws_chain + (size_t)(it + 1) * kFrameWs + kAimgBytes, kUBytes);
+                if (prefetch_u && it + 1 < nf)
+                    bulk_prefetch_l2(ws_chain + (size_t)(it + 1) * kFrameWs + kAimgBytes, kUBytes);
                 ++a_issued;
             }
             if (*abort_flag && a_issued)  // let the copy in flight land before the CTA exits
