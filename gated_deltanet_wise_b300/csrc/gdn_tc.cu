@@ -531,34 +531,63 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 // S_start(c) for every chunk, row-parallel fp32: rows [16*y, 16*y+16) of chain
 // x, seven CTAs per chain (one wave for the 20-head layer).  The chain is
 // sequential over chunks, S_start(c+1) = S_start(c) C_c + H_c; the composites
-// C_c (50 KB each) are bulk-copied into a ring of four shared-memory buffers,
-// up to four steps ahead, so that a step rarely waits for its copy.
+// C_c (50 KB each) are bulk-copied into a ring of three shared-memory buffers,
+// up to three steps ahead, so that a step does not wait for its copy.
+// The product of a step: four thread groups split the 112-long contraction
+// into quarters, and each thread keeps a 4 x kTC block of its quarter's
+// partial sums in registers: rows rg, rg+4, rg+8, rg+12 of the CTA's 16 and
+// columns kTC*cg.. (rg = i % 4, cg = i / 4 for thread i of its group).  Per
+// four k steps a thread loads four float4 of S and kTC float4 of C.  A 128-bit
+// shared load is served a quarter-warp at a time whatever its addresses, so
+// loads per FMA set the rate (one column and four rows per thread: 2.8 us a
+// step; 4 x 4 blocks over the full contraction on 112 threads: 2.45 us; split
+// four ways: 1.55 us).  Groups 1..3 leave their partial blocks in shared memory
+// and group 0 adds them up.  The S rows are 116 floats apart, so the four rows
+// a quarter-warp reads at one k fall in four different bank groups.
+// With a zero start state (no S_in) the first step is S_start(1) = H_0.
+#ifndef GDN_K1B_TC
+#define GDN_K1B_TC 4
+#endif
 constexpr int kK1bRows = 16;
-constexpr int kK1bThreads = 448;                                    // 112 columns x 4 groups of 4 rows
-constexpr int kK1bBufs = 4;
-constexpr uint32_t kK1bOffS = kK1bBufs * (uint32_t)kStateBytes;     // S rows [16][112]
-constexpr uint32_t kK1bOffBar = kK1bOffS + kK1bRows * kD * 4;       // kK1bBufs mbarriers + abort flag
+constexpr int kK1bTC = GDN_K1B_TC;                                   // columns per thread block (4 or 8)
+constexpr int kK1bGroups = 4;                                       // contraction quarters
+constexpr int kK1bTiles = (kK1bRows / 4) * (kD / kK1bTC);            // threads per group
+constexpr int kK1bThreads = kK1bTiles * kK1bGroups;
+constexpr int kK1bLen = kD / kK1bGroups;                            // contraction length per group
+constexpr int kK1bPitch = kD + 4;                                   // S and partial row pitch (floats)
+constexpr int kK1bBufs = 3;
+constexpr uint32_t kK1bRowsBytes = kK1bRows * kK1bPitch * 4;
+constexpr uint32_t kK1bOffS = kK1bBufs * (uint32_t)kStateBytes;     // S rows [16][116]
+constexpr uint32_t kK1bOffP = kK1bOffS + kK1bRowsBytes;             // partials of groups 1..3
+constexpr uint32_t kK1bOffBar = kK1bOffP + (kK1bGroups - 1) * kK1bRowsBytes;  // mbarriers + abort flag
 constexpr uint32_t kK1bSmem = kK1bOffBar + 64;
-static_assert(kD % kK1bRows == 0 && kK1bThreads == kD * (kK1bRows / 4), "K1b row split");
-static_assert(kK1bSmem <= kMaxSmem, "K1b shared memory");
+static_assert((kK1bTC == 4 || kK1bTC == 8) && kD % kK1bTC == 0 && kK1bRows == 16, "K1b blocks");
+static_assert(kK1bLen % 4 == 0 && kK1bLen * kK1bGroups == kD && kK1bThreads <= 1024, "K1b contraction split");
+static_assert(kK1bPitch % 4 == 0 && (kK1bPitch % 32) % 8 == 4, "K1b row pitch: 16-byte rows, bank groups");
+static_assert(kK1bOffS % 16 == 0 && kK1bSmem <= kMaxSmem, "K1b shared memory");
 // K1b modes: the start state is the identity (instead of S_in), and/or the input
 // composites are zero.  With both the scan composes the transition composites,
 // C_0 C_1 ... C_{n-1}; with neither it is the chunk-boundary scan proper.
 constexpr int kK1bIdentityIn = 1, kK1bZeroH = 2;
 
-__global__ void __launch_bounds__(kK1bThreads)
+__global__ void __launch_bounds__(kK1bThreads, 1)
     k1b_chunk_boundary_kernel(const float *__restrict__ compC, const float *__restrict__ compH, size_t chain_stride,
                               size_t chunk_stride, float *__restrict__ ws_start, const float *S_in, float *S_out,
                               int n_chunks, unsigned *status, int mode)
 {
+    constexpr int kC4 = kK1bTC / 4;  // float4 per block row
     extern __shared__ __align__(128) uint8_t k1b_smem[];
-    float(*Srows)[kD] = reinterpret_cast<float(*)[kD]>(k1b_smem + kK1bOffS);
+    float(*Srows)[kK1bPitch] = reinterpret_cast<float(*)[kK1bPitch]>(k1b_smem + kK1bOffS);
+    float(*Part)[kK1bRows][kK1bPitch] = reinterpret_cast<float(*)[kK1bRows][kK1bPitch]>(k1b_smem + kK1bOffP);
     uint64_t *bar = reinterpret_cast<uint64_t *>(k1b_smem + kK1bOffBar);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + kK1bBufs);
     auto cbuf = [&](int i) { return reinterpret_cast<float *>(k1b_smem + (size_t)i * kStateBytes); };
     const int bh = blockIdx.x, r0 = blockIdx.y * kK1bRows;
-    const int t = threadIdx.x, j = t % kD, rp = t / kD;  // rows r0 + 4*rp + 0..3
+    const int t = threadIdx.x, grp = t / kK1bTiles, ti = t % kK1bTiles;
+    const int rg = ti & 3, cg = ti >> 2;  // rows rg + 4q (q = 0..3), columns kTC*cg..
+    const int l0 = grp * kK1bLen;         // this group's contraction quarter
     const float *cC = compC + (size_t)bh * chain_stride, *cH = compH + (size_t)bh * chain_stride;
+    const bool zero_start = !(mode & kK1bIdentityIn) && S_in == nullptr;
     if (t == 0) {
         for (int i = 0; i < kK1bBufs; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
@@ -579,44 +608,77 @@ __global__ void __launch_bounds__(kK1bThreads)
             mbar_arrive_expect_tx(&bar[issued], (uint32_t)kStateBytes);
             bulk_g2s(cbuf(issued), cC + (size_t)issued * chunk_stride, (uint32_t)kStateBytes, &bar[issued]);
         }
-    // this thread's entries of H_c, loaded one step ahead
-    const bool zero_h = (mode & kK1bZeroH) != 0;
-    const float *h_ptr = cH + (r0 + 4 * rp) * kD + j;
-    float h_next[4];
+    // group 0's block of H_c (the other groups start their partial sums from zero), loaded one step ahead
+    const bool load_h = grp == 0 && (mode & kK1bZeroH) == 0;
+    const float *h_ptr = cH + (r0 + rg) * kD + kK1bTC * cg;
+    float4 h_next[4][kC4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) h_next[q] = (zero_h || steps == 0) ? 0.f : h_ptr[q * kD];
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int u = 0; u < kC4; ++u)
+            h_next[q][u] = (load_h && steps > 0) ? *reinterpret_cast<const float4 *>(h_ptr + 4 * q * kD + 4 * u)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
     int c = 0;  // on abort: the step whose copy was not seen to land
     for (; c < n_chunks; ++c) {
         if (ws_start) {
-            float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats;
-            for (int e = t; e < kK1bRows * kD; e += kK1bThreads)
-                dst[(r0 + e / kD) * kD + e % kD] = Srows[e / kD][e % kD];
+            float *dst = ws_start + ((size_t)bh * n_chunks + c) * kStateFloats + (size_t)r0 * kD;
+            for (int e = t; e < kK1bRows * kD / 4; e += kK1bThreads) {
+                const int rr = e / (kD / 4), c4 = e % (kD / 4);
+                *reinterpret_cast<float4 *>(dst + rr * kD + 4 * c4) =
+                    *reinterpret_cast<const float4 *>(&Srows[rr][4 * c4]);
+            }
         }
         if (c >= steps) break;
-        float acc[4];
+        float4 acc[4][kC4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = h_next[q];
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int u = 0; u < kC4; ++u) acc[q][u] = h_next[q][u];
         h_ptr += chunk_stride;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) h_next[q] = (zero_h || c + 1 >= steps) ? 0.f : h_ptr[q * kD];
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int u = 0; u < kC4; ++u)
+                h_next[q][u] = (load_h && c + 1 < steps)
+                                   ? *reinterpret_cast<const float4 *>(h_ptr + 4 * q * kD + 4 * u)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         const int buf = c % kK1bBufs;
         if (t == 0 && !mbar_wait(&bar[buf], (c / kK1bBufs) & 1, abort_flag)) *abort_flag = 1;
         __syncthreads();
         if (*abort_flag) break;
-        const float *C = cbuf(buf);
-        for (int l = 0; l < kD; l += 4) {  // four k steps per float4 of each S row (a broadcast load)
-            float cl[4];
+        const bool product = !(c == 0 && zero_start);  // S_start(0) = 0: S_start(1) = H_0
+        if (product) {
+            const float *C = cbuf(buf) + kK1bTC * cg;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cl[k] = C[(l + k) * kD + j];
+            for (int l = l0; l < l0 + kK1bLen; l += 4) {
+                float4 cv[4][kC4], sv[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 s4 = *reinterpret_cast<const float4 *>(&Srows[4 * rp + q][l]);
-                acc[q] = fmaf(s4.x, cl[0], acc[q]);
-                acc[q] = fmaf(s4.y, cl[1], acc[q]);
-                acc[q] = fmaf(s4.z, cl[2], acc[q]);
-                acc[q] = fmaf(s4.w, cl[3], acc[q]);
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int u = 0; u < kC4; ++u) cv[k][u] = *reinterpret_cast<const float4 *>(C + (l + k) * kD + 4 * u);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sv[q] = *reinterpret_cast<const float4 *>(&Srows[rg + 4 * q][l]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float sk[4] = {sv[q].x, sv[q].y, sv[q].z, sv[q].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int u = 0; u < kC4; ++u) {
+                            acc[q][u].x = fmaf(sk[k], cv[k][u].x, acc[q][u].x);
+                            acc[q][u].y = fmaf(sk[k], cv[k][u].y, acc[q][u].y);
+                            acc[q][u].z = fmaf(sk[k], cv[k][u].z, acc[q][u].z);
+                            acc[q][u].w = fmaf(sk[k], cv[k][u].w, acc[q][u].w);
+                        }
+                }
             }
+            if (grp > 0)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int u = 0; u < kC4; ++u)
+                        *reinterpret_cast<float4 *>(&Part[grp - 1][rg + 4 * q][kK1bTC * cg + 4 * u]) = acc[q][u];
         }
         __syncthreads();  // every thread is done with this buffer and with the old rows
         if (t == 0 && c + kK1bBufs < steps) {
@@ -624,8 +686,21 @@ __global__ void __launch_bounds__(kK1bThreads)
             bulk_g2s(cbuf(buf), cC + (size_t)(c + kK1bBufs) * chunk_stride, (uint32_t)kStateBytes, &bar[buf]);
             ++issued;
         }
+        if (grp == 0)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) Srows[4 * rp + q][j] = acc[q];
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int u = 0; u < kC4; ++u) {
+                    float4 a = acc[q][u];
+                    if (product)
+#pragma unroll
+                        for (int g = 0; g < kK1bGroups - 1; ++g) {
+                            const float4 pp =
+                                *reinterpret_cast<const float4 *>(&Part[g][rg + 4 * q][kK1bTC * cg + 4 * u]);
+                            a.x += pp.x, a.y += pp.y, a.z += pp.z, a.w += pp.w;
+                        }
+                    *reinterpret_cast<float4 *>(&Srows[rg + 4 * q][kK1bTC * cg + 4 * u]) = a;
+                }
         __syncthreads();
     }
     if (*abort_flag) {
