@@ -506,7 +506,91 @@ def measure_variants(x, K, stream, alg, peaks):
         del ws
     out["backward"] = measure_backward(x, max(3, min(K, 10)), stream, peaks)
     out["block"] = measure_block(x, max(3, min(K, 10)), stream, peaks)
+    out["context_parallel"] = measure_context_parallel(x, max(3, min(K, 20)), stream)
     return out
+
+
+def measure_context_parallel(x, K, stream, world=2):
+    """Frame-split context parallelism with the ranks' work run one after another on this GPU.
+    Per rank: its composite pass over its frames (gdn_frame_composite), its start state composed
+    from the earlier ranks' composites onto S_in (gdn_state_compose once per earlier rank; the
+    all-gather that carries the composites between GPUs is not in it) and the rest of its forward
+    from the statistics in its workspace (gdn_frame_fwd_resume), against gdn_frame_fwd over the
+    same frames from the same start state.  K calls each after 3 warm-ups; `ratio` is the largest
+    rank's time over its plain forward."""
+    import torch
+    from gated_deltanet_wise_b300 import gdn
+    from gated_deltanet_wise_b300.context_parallel import frame_split
+    B, H, F, N, D = x.B, x.H, x.F, x.N, x.D
+    dev = x.q.device
+
+    def part(t, f0, f1, per_frame):
+        return t[:, f0 * per_frame:f1 * per_frame].contiguous()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(K):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / K
+
+    def ok(st, what):
+        if st != gdn.GDN_OK:
+            raise gdn.GdnError(st, what)
+
+    gathered = []  # (C, H) of the ranks before this one, as the all-gather delivers them
+    rank_ms, plain_ms, frames = [], [], []
+    for f0, f1 in frame_split(F, world):
+        Fr = f1 - f0
+        q, k, v = (part(t, f0, f1, N) for t in (x.q, x.k, x.v))
+        beta, gamma = part(x.beta, f0, f1, N), part(x.gamma, f0, f1, 1)
+        C = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
+        Hc, S_out = torch.empty_like(C), torch.empty_like(C)
+        S_buf = [torch.empty_like(C), torch.empty_like(C)]
+        o = torch.empty_like(q)
+        nb = gdn.gdn_frame_composite_workspace_size(B, H, Fr, N, D)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        prior = list(gathered)
+
+        def start_state():
+            S = x.S0
+            for i, (Cp, Hp) in enumerate(prior):
+                ok(gdn.gdn_state_compose(S, Cp, Hp, S_buf[i % 2], B * H, D, stream), "gdn_state_compose")
+                S = S_buf[i % 2]
+            return S
+
+        def rank_step():
+            ok(gdn.gdn_frame_composite(k, v, beta, gamma, C, Hc, B, H, Fr, N, D, 0.0, ws, nb, stream),
+               "gdn_frame_composite")
+            ok(gdn.gdn_frame_fwd_resume(q, gamma, start_state(), S_out, o, B, H, Fr, N, D, ws, nb, stream),
+               "gdn_frame_fwd_resume")
+
+        nbf = gdn.gdn_frame_fwd_workspace_size(B, H, Fr, N, D)
+        wsf = torch.empty(nbf, dtype=torch.uint8, device=dev)
+        of, Sf = torch.empty_like(q), torch.empty_like(C)
+        S_plain = start_state()
+        S_plain = None if S_plain is None else S_plain.clone()
+
+        def plain_step():
+            ok(gdn.gdn_frame_fwd(q, k, v, beta, gamma, S_plain, Sf, of, B, H, Fr, N, D, 0.0, wsf, nbf, stream),
+               "gdn_frame_fwd")
+
+        rank_ms.append(timed(rank_step))
+        plain_ms.append(timed(plain_step))
+        frames.append(Fr)
+        if gdn.gdn_device_status() != gdn.GDN_OK:
+            raise RuntimeError("device status reports a timed-out wait")
+        gathered.append((C.clone(), Hc.clone()))
+        del ws, wsf
+    return {"ranks": world, "frames": frames, "rank_ms": [round(m, 5) for m in rank_ms],
+            "plain_fwd_ms": [round(m, 5) for m in plain_ms],
+            "ratio": round(max(a / b for a, b in zip(rank_ms, plain_ms)), 4), "steps": K,
+            "note": "ranks run one after another on one GPU; the all-gather between GPUs is not timed"}
 
 
 def measure_block(x, K, stream, peaks):
