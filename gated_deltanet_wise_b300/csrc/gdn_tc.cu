@@ -534,34 +534,40 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 // C_c (50 KB each) are bulk-copied into a ring of three shared-memory buffers,
 // up to three steps ahead, so that a step does not wait for its copy.
 // The product of a step: four thread groups split the 112-long contraction
-// into quarters, and each thread keeps a 4 x kTC block of its quarter's
-// partial sums in registers: rows rg, rg+4, rg+8, rg+12 of the CTA's 16 and
-// columns kTC*cg.. (rg = i % 4, cg = i / 4 for thread i of its group).  Per
-// four k steps a thread loads four float4 of S and kTC float4 of C.  A 128-bit
-// shared load is served a quarter-warp at a time whatever its addresses, so
-// loads per FMA set the rate (one column and four rows per thread: 2.8 us a
-// step; 4 x 4 blocks over the full contraction on 112 threads: 2.45 us; split
-// four ways: 1.55 us).  Groups 1..3 leave their partial blocks in shared memory
-// and group 0 adds them up.  The S rows are 116 floats apart, so the four rows
-// a quarter-warp reads at one k fall in four different bank groups.
-// With a zero start state (no S_in) the first step is S_start(1) = H_0.
+// into quarters, and each thread keeps a kTR x kTC block of its quarter's
+// partial sums in registers: rows rg, rg + 16/kTR, .. of the CTA's 16 and
+// columns kTC*cg.. (rg = i % (16/kTR), cg = i / (16/kTR) for thread i of its
+// group).  Per four k steps a thread loads kTR float4 of S and 4*kTC/4 float4
+// of C.  A 128-bit shared load is served a quarter-warp at a time whatever its
+// addresses, so loads per FMA set the rate (one column and four rows per
+// thread: 2.8 us a step; 4 x 4 blocks over the full contraction on 112
+// threads: 2.45 us; split four ways: 1.55 us).  Every group leaves its partial
+// block in shared memory and all threads add the four up.  The S rows are 116
+// floats apart, so the rows a quarter-warp reads at one k fall in different
+// bank groups.  With a zero start state (no S_in) the first step is
+// S_start(1) = H_0.
+#ifndef GDN_K1B_TR
+#define GDN_K1B_TR 4
+#endif
 #ifndef GDN_K1B_TC
 #define GDN_K1B_TC 4
 #endif
 constexpr int kK1bRows = 16;
+constexpr int kK1bTR = GDN_K1B_TR;                                   // rows per thread block (4 or 8)
 constexpr int kK1bTC = GDN_K1B_TC;                                   // columns per thread block (4 or 8)
+constexpr int kK1bRG = kK1bRows / kK1bTR;                           // row sets of a group
 constexpr int kK1bGroups = 4;                                       // contraction quarters
-constexpr int kK1bTiles = (kK1bRows / 4) * (kD / kK1bTC);            // threads per group
+constexpr int kK1bTiles = kK1bRG * (kD / kK1bTC);                   // threads per group
 constexpr int kK1bThreads = kK1bTiles * kK1bGroups;
 constexpr int kK1bLen = kD / kK1bGroups;                            // contraction length per group
 constexpr int kK1bPitch = kD + 4;                                   // S and partial row pitch (floats)
 constexpr int kK1bBufs = 3;
 constexpr uint32_t kK1bRowsBytes = kK1bRows * kK1bPitch * 4;
 constexpr uint32_t kK1bOffS = kK1bBufs * (uint32_t)kStateBytes;     // S rows [16][116]
-constexpr uint32_t kK1bOffP = kK1bOffS + kK1bRowsBytes;             // partials of groups 1..3
-constexpr uint32_t kK1bOffBar = kK1bOffP + (kK1bGroups - 1) * kK1bRowsBytes;  // mbarriers + abort flag
+constexpr uint32_t kK1bOffP = kK1bOffS + kK1bRowsBytes;             // partial rows of the four groups
+constexpr uint32_t kK1bOffBar = kK1bOffP + kK1bGroups * kK1bRowsBytes;  // mbarriers + abort flag
 constexpr uint32_t kK1bSmem = kK1bOffBar + 64;
-static_assert((kK1bTC == 4 || kK1bTC == 8) && kD % kK1bTC == 0 && kK1bRows == 16, "K1b blocks");
+static_assert((kK1bTR == 4 || kK1bTR == 8) && (kK1bTC == 4 || kK1bTC == 8) && kD % kK1bTC == 0, "K1b blocks");
 static_assert(kK1bLen % 4 == 0 && kK1bLen * kK1bGroups == kD && kK1bThreads <= 1024, "K1b contraction split");
 static_assert(kK1bPitch % 4 == 0 && (kK1bPitch % 32) % 8 == 4, "K1b row pitch: 16-byte rows, bank groups");
 static_assert(kK1bOffS % 16 == 0 && kK1bSmem <= kMaxSmem, "K1b shared memory");
@@ -584,8 +590,8 @@ __global__ void __launch_bounds__(kK1bThreads, 1)
     auto cbuf = [&](int i) { return reinterpret_cast<float *>(k1b_smem + (size_t)i * kStateBytes); };
     const int bh = blockIdx.x, r0 = blockIdx.y * kK1bRows;
     const int t = threadIdx.x, grp = t / kK1bTiles, ti = t % kK1bTiles;
-    const int rg = ti & 3, cg = ti >> 2;  // rows rg + 4q (q = 0..3), columns kTC*cg..
-    const int l0 = grp * kK1bLen;         // this group's contraction quarter
+    const int rg = ti % kK1bRG, cg = ti / kK1bRG;  // rows rg + kK1bRG*q (q < kTR), columns kTC*cg..
+    const int l0 = grp * kK1bLen;                   // this group's contraction quarter
     const float *cC = compC + (size_t)bh * chain_stride, *cH = compH + (size_t)bh * chain_stride;
     const bool zero_start = !(mode & kK1bIdentityIn) && S_in == nullptr;
     if (t == 0) {
@@ -595,29 +601,31 @@ __global__ void __launch_bounds__(kK1bThreads, 1)
     }
     griddep_launch_dependents();
     griddep_wait();  // composites and S_in come from earlier kernels on the stream
-    for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
-        const int rr = e / kD, cc = e % kD;
-        Srows[rr][cc] = (mode & kK1bIdentityIn) ? (r0 + rr == cc ? 1.f : 0.f)
-                        : S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
-    }
     // composite steps to apply: without S_out the state after the last chunk is not needed
     const int steps = S_out ? n_chunks : n_chunks - 1;
+    // group 0's block of H_c (the other groups start their partial sums from zero), loaded one
+    // step ahead; the first load goes out before the start rows are filled
+    const bool load_h = grp == 0 && (mode & kK1bZeroH) == 0;
+    const float *h_ptr = cH + (r0 + rg) * kD + kK1bTC * cg;
+    float4 h_next[kK1bTR][kC4];
+#pragma unroll
+    for (int q = 0; q < kK1bTR; ++q)
+#pragma unroll
+        for (int u = 0; u < kC4; ++u)
+            h_next[q][u] = (load_h && steps > 0)
+                               ? *reinterpret_cast<const float4 *>(h_ptr + kK1bRG * q * kD + 4 * u)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
     int issued = 0;
     if (t == 0)
         for (; issued < steps && issued < kK1bBufs; ++issued) {
             mbar_arrive_expect_tx(&bar[issued], (uint32_t)kStateBytes);
             bulk_g2s(cbuf(issued), cC + (size_t)issued * chunk_stride, (uint32_t)kStateBytes, &bar[issued]);
         }
-    // group 0's block of H_c (the other groups start their partial sums from zero), loaded one step ahead
-    const bool load_h = grp == 0 && (mode & kK1bZeroH) == 0;
-    const float *h_ptr = cH + (r0 + rg) * kD + kK1bTC * cg;
-    float4 h_next[4][kC4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int u = 0; u < kC4; ++u)
-            h_next[q][u] = (load_h && steps > 0) ? *reinterpret_cast<const float4 *>(h_ptr + 4 * q * kD + 4 * u)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = t; e < kK1bRows * kD; e += kK1bThreads) {
+        const int rr = e / kD, cc = e % kD;
+        Srows[rr][cc] = (mode & kK1bIdentityIn) ? (r0 + rr == cc ? 1.f : 0.f)
+                        : S_in ? S_in[(size_t)bh * kStateFloats + (r0 + rr) * kD + cc] : 0.f;
+    }
     __syncthreads();
     int c = 0;  // on abort: the step whose copy was not seen to land
     for (; c < n_chunks; ++c) {
@@ -630,37 +638,36 @@ __global__ void __launch_bounds__(kK1bThreads, 1)
             }
         }
         if (c >= steps) break;
-        float4 acc[4][kC4];
+        float4 acc[kK1bTR][kC4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < kK1bTR; ++q)
 #pragma unroll
             for (int u = 0; u < kC4; ++u) acc[q][u] = h_next[q][u];
         h_ptr += chunk_stride;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < kK1bTR; ++q)
 #pragma unroll
             for (int u = 0; u < kC4; ++u)
                 h_next[q][u] = (load_h && c + 1 < steps)
-                                   ? *reinterpret_cast<const float4 *>(h_ptr + 4 * q * kD + 4 * u)
+                                   ? *reinterpret_cast<const float4 *>(h_ptr + kK1bRG * q * kD + 4 * u)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
         const int buf = c % kK1bBufs;
         if (t == 0 && !mbar_wait(&bar[buf], (c / kK1bBufs) & 1, abort_flag)) *abort_flag = 1;
         __syncthreads();
         if (*abort_flag) break;
-        const bool product = !(c == 0 && zero_start);  // S_start(0) = 0: S_start(1) = H_0
-        if (product) {
+        if (!(c == 0 && zero_start)) {  // S_start(0) = 0: S_start(1) = H_0
             const float *C = cbuf(buf) + kK1bTC * cg;
 #pragma unroll
             for (int l = l0; l < l0 + kK1bLen; l += 4) {
-                float4 cv[4][kC4], sv[4];
+                float4 cv[4][kC4], sv[kK1bTR];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
                     for (int u = 0; u < kC4; ++u) cv[k][u] = *reinterpret_cast<const float4 *>(C + (l + k) * kD + 4 * u);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) sv[q] = *reinterpret_cast<const float4 *>(&Srows[rg + 4 * q][l]);
+                for (int q = 0; q < kK1bTR; ++q) sv[q] = *reinterpret_cast<const float4 *>(&Srows[rg + kK1bRG * q][l]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < kK1bTR; ++q) {
                     const float sk[4] = {sv[q].x, sv[q].y, sv[q].z, sv[q].w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -673,34 +680,28 @@ __global__ void __launch_bounds__(kK1bThreads, 1)
                         }
                 }
             }
-            if (grp > 0)
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int u = 0; u < kC4; ++u)
-                        *reinterpret_cast<float4 *>(&Part[grp - 1][rg + 4 * q][kK1bTC * cg + 4 * u]) = acc[q][u];
         }
+#pragma unroll
+        for (int q = 0; q < kK1bTR; ++q)
+#pragma unroll
+            for (int u = 0; u < kC4; ++u)
+                *reinterpret_cast<float4 *>(&Part[grp][rg + kK1bRG * q][kK1bTC * cg + 4 * u]) = acc[q][u];
         __syncthreads();  // every thread is done with this buffer and with the old rows
         if (t == 0 && c + kK1bBufs < steps) {
             mbar_arrive_expect_tx(&bar[buf], (uint32_t)kStateBytes);
             bulk_g2s(cbuf(buf), cC + (size_t)(c + kK1bBufs) * chunk_stride, (uint32_t)kStateBytes, &bar[buf]);
             ++issued;
         }
-        if (grp == 0)
+        for (int e = t; e < kK1bRows * kD / 4; e += kK1bThreads) {  // the new rows: sum of the four partials
+            const int rr = e / (kD / 4), c4 = e % (kD / 4);
+            float4 a = *reinterpret_cast<const float4 *>(&Part[0][rr][4 * c4]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int u = 0; u < kC4; ++u) {
-                    float4 a = acc[q][u];
-                    if (product)
-#pragma unroll
-                        for (int g = 0; g < kK1bGroups - 1; ++g) {
-                            const float4 pp =
-                                *reinterpret_cast<const float4 *>(&Part[g][rg + 4 * q][kK1bTC * cg + 4 * u]);
-                            a.x += pp.x, a.y += pp.y, a.z += pp.z, a.w += pp.w;
-                        }
-                    *reinterpret_cast<float4 *>(&Srows[rg + 4 * q][kK1bTC * cg + 4 * u]) = a;
-                }
+            for (int g = 1; g < kK1bGroups; ++g) {
+                const float4 pp = *reinterpret_cast<const float4 *>(&Part[g][rr][4 * c4]);
+                a.x += pp.x, a.y += pp.y, a.z += pp.z, a.w += pp.w;
+            }
+            *reinterpret_cast<float4 *>(&Srows[rr][4 * c4]) = a;
+        }
         __syncthreads();
     }
     if (*abort_flag) {
