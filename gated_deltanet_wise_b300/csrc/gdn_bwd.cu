@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol = policy_stream();
             int g = 0;  // tiles issued by this CTA
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {

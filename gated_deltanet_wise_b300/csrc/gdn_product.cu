@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const long long items = (long long)p.B * p.H * p.F * p.n_sc;
     const long long stride = (long long)gridDim.x * kTPairs;
     const long long first = (long long)blockIdx.x * kTPairs + pr;
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = policy_stream();
     // item -> (chain, processing position, sub-chunk) and the key tile's TMA coordinates
     auto decode = [&](long long item, int &bh, int &f, int &sc, int &h, int &bf) {
         sc = (int)(item % p.n_sc);
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol = policy_stream();
             int issued = 0;
             for (int sc = 0; sc < n_sc; ++sc) {
                 const int kb = sc & 1;

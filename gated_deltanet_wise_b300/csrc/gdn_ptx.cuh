@@ -207,10 +207,17 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ uint64_t policy_evict_first()
+// L2 policy of the streamed token-row tile loads (k, v, q, dO).  A head's 224-byte
+// row segment shares its first and last 64-byte DRAM blocks with the neighbouring
+// heads, whose CTAs read the same token rows at about the same time.  Under an
+// evict-first policy those shared blocks left L2 before the neighbour's load and
+// were fetched twice (the 20-head layer's scan/output kernel read 113 MB more and
+// took 227 instead of 213 us; the statistics kernel read 22 MB above its k, v,
+// beta bytes); evict-normal keeps them for the neighbour.
+__device__ __forceinline__ uint64_t policy_stream()
 {
     uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // ------------------------------------------------------ TMA producer
         bool ok = true;
         int st_issued = 0, q_issued = 0;
-        const uint64_t pol = policy_evict_first();
+        const uint64_t pol = policy_stream();
         if (lane == 0) {
             for (int st = 0; st < n_st; ++st) {
                 const int s = st % kSStages, use = st / kSStages;

@@ -57,7 +57,7 @@ namespace gdn {
 #define GDN_WS_L2HINT 1
 #endif
 // K1 writes the per-frame workspace with an evict-last L2 policy (its k, v reads
-// and K2's q reads are evict-first), so that part of the 190 MB workspace of the
+// and K2's q reads are evict-normal), so that part of the 190 MB workspace of the
 // 20-head layer is still in the 126 MB L2 when K2 reads it: K2 246 -> 241 us.
 constexpr bool kWsKeepL2 = GDN_WS_L2HINT != 0;
 constexpr int kTS = GDN_K1_TS;                        // tokens per stage (one TMA box height)
@@ -192,7 +192,7 @@ __device__ __forceinline__ uint32_t k1_body(const CUtensorMap &mapK, const CUten
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol = policy_stream();
             int it = 0;
             bool ok = !p.withhold_loads;  // withheld: no stage ever fills, the consumers' waits expire
             for (int fl = 0; fl < nf && ok; ++fl) {
@@ -944,7 +944,7 @@ __device__ __forceinline__ void k2_body(const CUtensorMap &mapQ, const CUtensorM
             if (*abort_flag && a_issued)  // let the copy in flight land before the CTA exits
                 mbar_wait_drain(a_full, (a_issued - 1) & 1);
         } else if (lane == 1) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol = policy_stream();
             int qc = 0;
             bool ok = true;
             for (int it = 1; it <= nf && ok; ++it) {
