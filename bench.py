@@ -750,7 +750,7 @@ def run_reference(args):
     oracle.build()
     x = make_workload(args.workload, device="cpu", seed=0, F=8)
     threads = oracle.num_threads()
-    heads = min(x.H, threads)
+    heads = x.H  # every chain of the layer, as the in-run cpu_baseline samples it
     t1 = oracle_sample(x, heads, 1)
     # size each step to ~2 s so that warm-up + steps finish within a few minutes
     frames = max(1, min(x.F, int(2.0 / max(t1, 1e-3))))
