@@ -512,11 +512,12 @@ def measure_variants(x, K, stream, alg, peaks):
 
 def measure_context_parallel(x, K, stream, world=2):
     """Frame-split context parallelism with the ranks' work run one after another on this GPU.
-    Per rank: its composite pass over its frames (gdn_frame_composite), its start state composed
-    from the earlier ranks' composites onto S_in (gdn_state_compose once per earlier rank; the
-    all-gather that carries the composites between GPUs is not in it) and the rest of its forward
-    from the statistics in its workspace (gdn_frame_fwd_resume), against gdn_frame_fwd over the
-    same frames from the same start state.  K calls each after 3 warm-ups; `ratio` is the largest
+    Per rank: its composite pass over its frames (gdn_frame_composite; on the last rank, whose
+    composites no rank composes, the statistics pass alone), its start state composed from the
+    earlier ranks' composites onto S_in (gdn_state_compose once per earlier rank; the all-gather
+    that carries the composites between GPUs is not in it) and the rest of its forward from the
+    statistics in its workspace (gdn_frame_fwd_resume), against gdn_frame_fwd over the same
+    frames from the same start state.  K calls each after 3 warm-ups; `ratio` is the largest
     rank's time over its plain forward."""
     import torch
     from gated_deltanet_wise_b300 import gdn
@@ -545,7 +546,8 @@ def measure_context_parallel(x, K, stream, world=2):
 
     gathered = []  # (C, H) of the ranks before this one, as the all-gather delivers them
     rank_ms, plain_ms, frames = [], [], []
-    for f0, f1 in frame_split(F, world):
+    for r, (f0, f1) in enumerate(frame_split(F, world)):
+        last = r == world - 1
         Fr = f1 - f0
         q, k, v = (part(t, f0, f1, N) for t in (x.q, x.k, x.v))
         beta, gamma = part(x.beta, f0, f1, N), part(x.gamma, f0, f1, 1)
@@ -565,8 +567,8 @@ def measure_context_parallel(x, K, stream, world=2):
             return S
 
         def rank_step():
-            ok(gdn.gdn_frame_composite(k, v, beta, gamma, C, Hc, B, H, Fr, N, D, 0.0, ws, nb, stream),
-               "gdn_frame_composite")
+            ok(gdn.gdn_frame_composite(k, v, beta, gamma, None if last else C, None if last else Hc,
+                                       B, H, Fr, N, D, 0.0, ws, nb, stream), "gdn_frame_composite")
             ok(gdn.gdn_frame_fwd_resume(q, gamma, start_state(), S_out, o, B, H, Fr, N, D, ws, nb, stream),
                "gdn_frame_fwd_resume")
 

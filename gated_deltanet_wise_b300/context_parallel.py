@@ -15,10 +15,11 @@ the maps of ranks 0..p-1 onto the initial state,
     S_start(p) = (...((S_in C_0 + H_0) C_1 + H_1) ...) C_{p-1} + H_{p-1},
 
 and runs its frames from S_start(p).  The last rank's final state is the
-layer's S_out.  The arithmetic runs in the CUDA library
-(gdn_frame_composite, gdn_state_compose, gdn_frame_fwd); this module holds only
-the split and the exchange, and takes its three operations as arguments so
-that the exchange logic can be exercised without a GPU.
+layer's S_out, and its own composites are never composed, so it runs only the
+statistics pass its forward resumes from.  The arithmetic runs in the CUDA
+library (gdn_frame_composite, gdn_state_compose, gdn_frame_fwd_resume); this
+module holds only the split and the exchange, and takes its operations as
+arguments so that the exchange logic can be exercised without a GPU.
 """
 from __future__ import annotations
 
@@ -41,11 +42,15 @@ def frame_split(F: int, world: int) -> List[Tuple[int, int]]:
 
 @dataclass
 class CpOps:
-    """The three per-rank operations: composite(k, v, beta, gamma) -> (C, H);
-    compose(S or None, C, H) -> S C + H; forward(q, k, v, beta, gamma, S) -> (o, S_out)."""
+    """The per-rank operations: composite(k, v, beta, gamma) -> (C, H);
+    compose(S or None, C, H) -> S C + H; forward(q, k, v, beta, gamma, S) -> (o, S_out);
+    and optionally statistics(k, v, beta, gamma) -> placeholders shaped and typed like
+    (C, H), called instead of composite on the last rank, whose composites no rank reads
+    (the library form still runs the statistics pass its forward resumes from)."""
     composite: Callable
     compose: Callable
     forward: Callable
+    statistics: Optional[Callable] = None
 
 
 def library_ops(key_scale: float = 0.0) -> CpOps:
@@ -62,13 +67,19 @@ def library_ops(key_scale: float = 0.0) -> CpOps:
     def composite(k, v, beta, gamma):
         return gdn.frame_composite(k, v, beta, gamma, key_scale=key_scale, workspace=ws)
 
+    def statistics(k, v, beta, gamma):
+        import torch
+        gdn.frame_composite(k, v, beta, gamma, key_scale=key_scale, workspace=ws, outputs=False)
+        z = torch.zeros(k.shape[0], k.shape[2], k.shape[3], k.shape[3], dtype=torch.float32, device=k.device)
+        return z, z
+
     def compose(S, C, H):
         return gdn.state_compose(S, C, H)
 
     def forward(q, k, v, beta, gamma, S):
         return gdn.frame_fwd_resume(q, gamma, S, workspace=ws)
 
-    return CpOps(composite, compose, forward)
+    return CpOps(composite, compose, forward, statistics)
 
 
 def start_state(S_in, composites: Sequence[Tuple[object, object]], rank: int, compose: Callable):
@@ -94,7 +105,9 @@ def cp_forward(q, k, v, beta, gamma, S_in=None, *, ops: Optional[CpOps] = None, 
     ops = ops or library_ops()
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
-    C, H = ops.composite(k, v, beta, gamma)
+    # the last rank's composites are gathered but no rank composes them
+    last = rank == world - 1 and ops.statistics is not None
+    C, H = (ops.statistics if last else ops.composite)(k, v, beta, gamma)
     CH = torch.stack([C, H]).contiguous()   # one message per rank: (C_p, H_p) back to back
     parts = [torch.empty_like(CH) for _ in range(world)]
     dist.all_gather(parts, CH, group=group)

@@ -444,13 +444,15 @@ def frame_fwd_f32(q, k, v, beta, gamma, S_in=None, *, key_scale: float = 0.0, st
 
 
 def frame_composite(k, v, beta, gamma, *, key_scale: float = 0.0, workspace: Optional[Workspace] = None,
-                    stream=None):
-    """Per-chain composites (C, H) of the frames given, each [B, H, D, D] fp32."""
+                    stream=None, outputs: bool = True):
+    """Per-chain composites (C, H) of the frames given, each [B, H, D, D] fp32.  With
+    outputs=False only the frame-statistics pass runs (C_out = H_out = NULL) and (None, None)
+    comes back: the workspace still holds what gdn_frame_fwd_resume needs."""
     B, H, F, N, D = _shape(k, gamma)
     for t, n in ((k, "k"), (v, "v")):
         _check(t, torch.bfloat16, n)
-    C = torch.empty(B, H, D, D, dtype=torch.float32, device=k.device)
-    Hc = torch.empty_like(C)
+    C = torch.empty(B, H, D, D, dtype=torch.float32, device=k.device) if outputs else None
+    Hc = torch.empty_like(C) if outputs else None
     nbytes = gdn_frame_composite_workspace_size(B, H, F, N, D)
     if nbytes == 2 ** 64 - 1:
         raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_frame_composite_workspace_size")

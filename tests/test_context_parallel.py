@@ -33,7 +33,7 @@ def _inputs(F, seed=0):
     return q, k, v, beta, gamma, S0
 
 
-def _oracle_ops():
+def _oracle_ops(with_statistics=False):
     import oracle
 
     def composite(k, v, beta, gamma):
@@ -52,10 +52,15 @@ def _oracle_ops():
                                     None if S is None else S.numpy().astype(np.float32), key_scale=0.5)
         return torch.from_numpy(o), torch.from_numpy(S_out)
 
-    return CpOps(composite, compose, forward)
+    def statistics(k, v, beta, gamma):
+        # the last rank's placeholders: NaN, so that a rank composing them would show it
+        nan = torch.full((B, H, D, D), float("nan"), dtype=torch.float64)
+        return nan, nan.clone()
+
+    return CpOps(composite, compose, forward, statistics if with_statistics else None)
 
 
-def _rank_main(rank, world, port, F, out_dir):
+def _rank_main(rank, world, port, F, out_dir, with_statistics=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -65,7 +70,7 @@ def _rank_main(rank, world, port, F, out_dir):
         sl = slice(f0 * N, f1 * N)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
         o, S_end = cp_forward(t(q[:, sl]), t(k[:, sl]), t(v[:, sl]), t(beta[:, sl]), t(gamma[:, f0:f1]),
-                              torch.from_numpy(S0.astype(np.float64)), ops=_oracle_ops())
+                              torch.from_numpy(S0.astype(np.float64)), ops=_oracle_ops(with_statistics))
         np.save(os.path.join(out_dir, f"o_{rank}.npy"), o.numpy())
         np.save(os.path.join(out_dir, f"S_{rank}.npy"), S_end.numpy())
     finally:
@@ -78,10 +83,12 @@ def _free_port():
         return s.getsockname()[1]
 
 
-@pytest.mark.parametrize("world,F", [(2, 6), (2, 5), (3, 7)])
-def test_ranks_reproduce_one_sequential_pass(tmp_path, world, F):
+@pytest.mark.parametrize("world,F,with_statistics", [(2, 6, False), (2, 5, False), (3, 7, False), (3, 7, True)])
+def test_ranks_reproduce_one_sequential_pass(tmp_path, world, F, with_statistics):
+    """with_statistics: the last rank forms no composites (NaN placeholders go into the
+    all-gather); the result is unchanged because no rank composes them."""
     import oracle
-    mp.spawn(_rank_main, args=(world, _free_port(), F, str(tmp_path)), nprocs=world, join=True)
+    mp.spawn(_rank_main, args=(world, _free_port(), F, str(tmp_path), with_statistics), nprocs=world, join=True)
     q, k, v, beta, gamma, S0 = _inputs(F)
     o_ref, S_ref = oracle.frame_fwd(q, k, v, beta, gamma, S0, key_scale=0.5)
     o = np.concatenate([np.load(tmp_path / f"o_{r}.npy") for r in range(world)], axis=1)
