@@ -118,6 +118,10 @@ def test_host_side_validation_without_gpu(L):
     assert comp(fake, fake, fake, None, fake, fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_INVALID_ARG
     assert comp(fake, fake, fake, fake, fake, fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_WORKSPACE
     assert comp(fake, fake, fake, fake, P(0x10004), fake, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    # no composites wanted (the last rank of a frame split): the null outputs pass validation,
+    # and the call goes on to the workspace check like any other
+    assert comp(fake, fake, fake, fake, None, None, 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_WORKSPACE
+    assert comp(fake, fake, fake, fake, None, P(0x10004), 1, 1, 2, 8, 112, 0.0, None, 0, None) == gdn.GDN_ERR_INVALID_ARG
     assert gdn.gdn_frame_composite_workspace_size(1, 20, 16, 880, 112) >= 20 * 16 * 80000
     assert gdn.gdn_frame_composite_workspace_size(1, 20, 0, 880, 112) == 0
     cmp_ = L.gdn_state_compose
